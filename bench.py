@@ -1,0 +1,360 @@
+#!/usr/bin/env python
+"""Throughput of the grouped MXFP8 MoE expert MLP (route + forward + backward)
+on GB300, through the library's C ABI.
+
+One step = one pass of the whole path over one batch: top-k routing, permute,
+weight and activation quantisation, gate-up GEMM with fused ScaledSwiGLU and
+re-quantisation, down GEMM, combine, then the backward (dy quantisation,
+dgrad-down with fused dSwiGLU, wgrad-down, dgrad-gate-up, wgrad-gate-up,
+combine dx, dprobs).  Default workload: one Mixtral-8x7B MoE layer
+(T=16384 tokens = batch 4 x seq 4096, H=4096, I=14336, E=8, top-2), seeded
+synthetic inputs.
+
+  value   : GEMM TFLOP/s of the whole step (18*R*H*I per step), inputs resident
+            in HBM, timed with CUDA events on the launching stream.
+  e2e     : the same metric with inputs copied host->device and y, dx copied
+            back each step (pinned host buffers), through the C ABI.
+  roofline: the dominant kernel, timed live per launch with events around its
+            stage call, against the MXFP8 peak (2 x measured dense bf16).
+  cpu_baseline: the CPU oracle on a bounded sample of the same workload.
+
+--impl reference runs that CPU oracle as the reference arm.
+Multi-GPU (torchrun): every rank runs an independent replica (the path does
+not exchange data); value = all ranks' work / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "grouped MoE MLP fwd+bwd TFLOP/s & tokens/s; % of MXFP8 tensor-core peak"
+FALLBACK_BF16_SUSTAINED = 1700.0     # TFLOP/s, used only without a measured peaks file
+FALLBACK_HBM = 6800.0                # GB/s
+
+# CPU sample of the workload for the oracle: the first T_S tokens, all experts,
+# full hidden size, the intermediate dimension cut to its first I_S columns.
+CPU_SAMPLE_TOKENS = 512
+CPU_SAMPLE_I = 256
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": FALLBACK_BF16_SUSTAINED, "hbm_gbs": FALLBACK_HBM}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip() == "Active":
+                    reasons.add(n)
+        loaded = [s for s in sm if s > 0.5 * (max(sm) if sm else 1)]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------- CPU oracle --
+def cpu_sample_inputs(inp, wl):
+    import torch
+    T_s, I_s, I = min(CPU_SAMPLE_TOKENS, wl.T), min(CPU_SAMPLE_I, wl.I), wl.I
+    wgu = torch.cat([inp["w_gate_up"][:, :I_s], inp["w_gate_up"][:, I:I + I_s]], 1)
+    return {"logits": inp["logits"][:T_s].numpy(), "x": inp["x"][:T_s].double().numpy(),
+            "w_gate_up": wgu.double().numpy(), "w_down": inp["w_down"][:, :, :I_s].double().numpy(),
+            "dy": inp["dy"][:T_s].double().numpy(), "T": T_s, "I": I_s}
+
+
+def cpu_sample_run(s, k):
+    from oracle import moe
+    ids, probs = moe.route_topk(s["logits"], k)
+    ctx = moe.mlp_fwd(s["x"], ids, probs, s["w_gate_up"], s["w_down"])
+    moe.mlp_bwd(ctx, s["dy"])
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(inp, wl, reps: int = 1) -> dict:
+    s = cpu_sample_inputs(inp, wl)
+    flops = 18.0 * s["T"] * wl.k * wl.H * s["I"]
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        cpu_sample_run(s, wl.k)
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"fwd+bwd of the first {s['T']} tokens, all {wl.E} experts, H={wl.H}, intermediate cut to "
+                      f"its first {s['I']} columns ({flops / 1e9:.1f} GFLOP, {dt:.1f} s), fp64 numpy oracle",
+            "seconds": dt}
+
+
+# ------------------------------------------------------------------- GPU --
+def traffic_for(stage: str, workload: str) -> int | None:
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current source of the kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    src = os.path.join(ROOT, "mxfp8_grouped_gemm_gb300", "csrc", d.get("source", "gemm.cu"))
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] if os.path.exists(src) else None
+    e = d.get("entries", {}).get(f"{workload}/{stage}")
+    if not e or e.get("source_sha") != h:
+        return None
+    return int(e["bytes_per_launch"])
+
+
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    import mxfp8_grouped_gemm_gb300 as m
+    import synthetic
+    from mxfp8_grouped_gemm_gb300 import build as libbuild
+
+    libbuild.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    if not m.mxg_device_supported():
+        raise SystemExit("bench: current device is not sm_103 (GB300)")
+    wl = synthetic.WORKLOADS[args.workload]
+    inp = synthetic.make_inputs(wl)
+    if "dy" not in inp:
+        inp["dy"] = synthetic.random_bf16((wl.T, wl.H), 77)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    layer = m.GroupedMLP(T, H, I, E, k, device=dev)
+    d = {n: v.to(dev) for n, v in inp.items() if isinstance(v, torch.Tensor)}
+    stream = torch.cuda.current_stream(dev)
+
+    def step_full():
+        ids, probs = layer.route(d["logits"])
+        layer.forward(d["x"], ids, probs, d["w_gate_up"], d["w_down"])
+        layer.backward(d["dy"])
+
+    for _ in range(args.warmup):
+        step_full()
+    torch.cuda.synchronize(dev)
+    if layer.status() != 0:
+        raise SystemExit(f"bench: device status {m.status_string(layer.status())}")
+
+    # ---- device-resident timed region: every stage bracketed by events ----
+    stages = ["route"] + [f"fwd.{s}" for s in m.FWD_STAGES] + [f"bwd.{s}" for s in m.BWD_STAGES]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = m.mxg_launch_count()
+    for s in range(args.steps):
+        e = evs[s]
+        e[0].record(stream)
+        ids, probs = layer.route(d["logits"])
+        e[1].record(stream)
+        i = 2
+        for st in range(len(m.FWD_STAGES)):
+            layer.forward(d["x"], ids, probs, d["w_gate_up"], d["w_down"], stage=st)
+            e[i].record(stream)
+            i += 1
+        for st in range(len(m.BWD_STAGES)):
+            layer.backward(d["dy"], stage=st)
+            e[i].record(stream)
+            i += 1
+    torch.cuda.synchronize(dev)
+    launches = (m.mxg_launch_count() - launches0) / args.steps
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = evs[0][0].elapsed_time(evs[-1][-1])
+    stage_ms = {st: statistics.mean(evs[s][j].elapsed_time(evs[s][j + 1]) for s in range(args.steps))
+                for j, st in enumerate(stages)}
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: inp[n].pin_memory() for n in ("logits", "x", "dy")}
+        y_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        dx_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = y_h.numel() * 2 + dx_h.numel() * 2
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        ea.record(stream)
+        for _ in range(args.steps):
+            for n in pin:
+                d[n].copy_(pin[n], non_blocking=True)
+            ids, probs = layer.route(d["logits"])
+            layer.forward(d["x"], ids, probs, d["w_gate_up"], d["w_down"])
+            layer.backward(d["dy"])
+            y_h.copy_(layer.y, non_blocking=True)
+            dx_h.copy_(layer.dx, non_blocking=True)
+        eb.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = ea.elapsed_time(eb) / args.steps
+        e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
+    clk = clocks.stop()
+    if layer.status() != 0:
+        raise SystemExit(f"bench: device status {m.status_string(layer.status())}")
+
+    ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms, e2e["ms"] if e2e else 0.0], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_max = float(t[0]), float(t[1])
+        if e2e:
+            e2e["ms"] = e2e_max
+    flops = wl.gemm_flops(True)
+    value = world * flops / (ms * 1e-3) / 1e12
+    split = layer.split_sizes.cpu().numpy()
+
+    peaks, peaks_kind = load_peaks()
+    p_mx = 2.0 * float(peaks["bf16_tflops_sustained"])
+    R = T * k
+    stage_flops = {"fwd.gate_up": 4.0 * R * H * I, "fwd.down": 2.0 * R * H * I, "bwd.dgrad_down": 2.0 * R * H * I,
+                   "bwd.wgrad_down": 2.0 * R * H * I, "bwd.dgrad_gate_up": 4.0 * R * H * I,
+                   "bwd.wgrad_gate_up": 4.0 * R * H * I}
+    dom = max(stage_ms, key=lambda s_: stage_ms[s_])
+    if dom in stage_flops:
+        ach = stage_flops[dom] / (stage_ms[dom] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": round(p_mx, 1),
+                "unit": "TFLOP/s", "frac": round(ach / p_mx, 4), "traffic": traffic_for(dom, args.workload),
+                "peak_source": f"2 x {peaks_kind} sustained dense bf16 ({peaks['bf16_tflops_sustained']} TFLOP/s)"}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                "frac": None, "traffic": None}
+    gemm_ms = sum(stage_ms[s_] for s_ in stage_flops)
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: Mixtral-8x7B MoE layer T={T} H={H} I={I} E={E} top-{k}"
+                   if wl.name == "mixtral" else f"{wl.name}: T={T} H={H} I={I} E={E} top-{k}",
+                   "tokens_per_step": T, "gemm_flops_per_step": flops,
+                   "l2": "no flush: every step streams > 10 GB (weights 2.8 GB) through HBM, inputs > L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": round(world * T / (ms * 1e-3), 1),
+        "gemm_tflops": round(world * flops / (gemm_ms * 1e-3) / 1e12, 2),
+        "frac_of_mxfp8_peak": round(value / world / p_mx, 4),
+        "stages_ms": {s_: round(v, 4) for s_, v in stage_ms.items()},
+        "split_sizes": {"min": int(split.min()), "max": int(split.max()), "mean": float(split.mean()),
+                        "zeros": int((split == 0).sum())},
+        "roofline": roof,
+        "gpu_launches": int(round(launches)),
+        "clocks": clk,
+    }
+    if e2e:
+        res["e2e"] = {"value": round(world * flops / (e2e["ms"] * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                      "ms_per_step": round(e2e["ms"], 4), "h2d_bytes_per_step": e2e["h2d"],
+                      "d2h_bytes_per_step": e2e["d2h"]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(inp, wl)
+    return res
+
+
+def run_reference(args):
+    import synthetic
+    wl = synthetic.WORKLOADS[args.workload]
+    inp = synthetic.make_inputs(wl)
+    if "dy" not in inp:
+        inp["dy"] = synthetic.random_bf16((wl.T, wl.H), 77)
+    s = cpu_sample_inputs(inp, wl)
+    flops = 18.0 * s["T"] * wl.k * wl.H * s["I"]
+    for _ in range(args.warmup):
+        cpu_sample_run(s, wl.k)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_sample_run(s, wl.k)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = flops / dt / 1e12
+    sample = (f"each step: fwd+bwd of the first {s['T']} tokens, all {wl.E} experts, H={wl.H}, intermediate cut "
+              f"to its first {s['I']} columns ({flops / 1e9:.1f} GFLOP), fp64 numpy CPU oracle")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{wl.name}: T={wl.T} H={wl.H} I={wl.I} E={wl.E} top-{wl.k} (bounded sample)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

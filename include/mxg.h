@@ -1,0 +1,243 @@
+/*
+ * mxg — grouped MXFP8 MoE expert MLP for GB300 (sm_103a).  C ABI.
+ *
+ * The path: top-k routing, a permute of tokens into per-expert groups with one
+ * count per expert (split_sizes), MXFP8 quantisation (E4M3 values, one E8M0
+ * scale per 32 consecutive values along the contraction axis), a grouped
+ * gate-up GEMM fused with ScaledSwiGLU (x routing probability) and
+ * re-quantisation, a grouped down GEMM, and an unpermute/combine — plus the
+ * backward (dgrad and wgrad grouped GEMMs; the wgrad operands are quantised
+ * column-wise over tokens).
+ *
+ * Sources (web pages about the BioNeMo Mixtral MoE recipe):
+ *   [Grouped]  "BioNeMo Uses Grouped Kernels and MXFP8" (toolai.io)
+ *   [Overhead] "How BioNeMo cuts overhead in biological AI training"
+ *              (roboticlifestyle.com)
+ *
+ * Conventions for every call:
+ *   - Returns an mxg_status; 0 (MXG_OK) means the work was enqueued.
+ *   - Asynchronous on the caller's CUDA stream (`stream` is a cudaStream_t,
+ *     0 = legacy default stream).  No call synchronises the host.
+ *   - No call allocates device or host memory.  Every buffer is a device
+ *     pointer owned by the caller; scratch is passed in explicitly, sized by
+ *     the matching *_bytes() query.
+ *   - Argument errors are detected on the host before anything is launched and
+ *     returned as MXG_ERR_ARG / MXG_ERR_SHAPE / MXG_ERR_ALIGN /
+ *     MXG_ERR_WORKSPACE.  Errors only visible on the device (an expert id out
+ *     of range, inconsistent group offsets, a kernel wait that timed out) are
+ *     written to the caller's `dev_status` int32 (device memory, zero it before
+ *     the call; the first error wins) and the affected kernels skip the bad
+ *     work instead of faulting.
+ *   - bf16 tensors are passed as uint16_t bit patterns.  All matrices are
+ *     row-major and dense unless stated otherwise.
+ *   - Device pointers must be 16-byte aligned (MXG_ERR_ALIGN otherwise).
+ */
+#ifndef MXG_H_
+#define MXG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MXG_OK = 0,
+  MXG_ERR_ARG = 1,        /* null pointer, non-positive size, bad enum value        */
+  MXG_ERR_SHAPE = 2,      /* a dimension violates the call's divisibility rules      */
+  MXG_ERR_ALIGN = 3,      /* a device pointer is not 16-byte aligned                 */
+  MXG_ERR_ARCH = 4,       /* current device is not sm_103 / library not built for it */
+  MXG_ERR_WORKSPACE = 5,  /* caller's scratch/saved buffer is too small              */
+  MXG_ERR_CUDA = 6,       /* a CUDA runtime call or kernel launch failed             */
+  /* device-detected, reported through dev_status */
+  MXG_ERR_EXPERT_ID = 16, /* an expert id outside [0, E)                             */
+  MXG_ERR_OFFSETS = 17,   /* group offsets not monotone / not 128-aligned / too big  */
+  MXG_ERR_TIMEOUT = 18    /* a bounded wait inside a kernel gave up                  */
+} mxg_status;
+
+/* Layout of MXFP8 scale bytes. */
+enum {
+  /* row-wise: s[r][c/32]; column-wise (transposed): sT[c][r/32] */
+  MXG_LAYOUT_CANONICAL = 0,
+  /* the tensor-core operand layout: for a matrix with R rows (multiple of 128)
+     and contraction length K (multiple of 128), the scale of (row r, 32-block
+     b) sits at byte
+        ((b/4)*(R/128) + r/128)*512 + (r%32)*16 + ((r/32)%4)*4 + (b%4)
+     i.e. 512-byte atoms of 128 rows x 4 blocks, laid out K-chunk-major. */
+  MXG_LAYOUT_MMA = 1
+};
+
+/* Text for a status code (static storage). */
+const char* mxg_status_string(int status);
+
+/* 1 if the library's kernels can run on the current device (sm_103). */
+int mxg_device_supported(void);
+
+/* Number of kernel launches the library has enqueued since load (monotone
+   counter kept on the host; used to report launches per step). */
+uint64_t mxg_launch_count(void);
+
+/* ----------------------------------------------------------------------------
+ * Top-k routing.  [Grouped] Fig. 1: a top-2 router sends each token to two of
+ * eight experts and the outputs are combined as a weighted sum.
+ *   logits  fp32 [T][E] (device)
+ *   ids     int32 [T][k] out: the k largest logits per token, descending,
+ *           ties to the lower expert id
+ *   probs   fp32 [T][k] out: softmax over the chosen k logits (renormalised)
+ * Requires 1 <= k <= E <= 256, k <= 32.
+ */
+int mxg_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* probs, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * Permute index: counting sort of the flat index f = t*k + j by expert id,
+ * stable in f (bit-exact, deterministic).  [Grouped] "Grouping fragmented
+ * expert workloads" (split_sizes: one token count per expert); [Overhead]
+ * "Grouping the expert work".
+ *   ids             int32 [T][k] (device)
+ *   split_sizes     int32 [E] out: rows per expert
+ *   src_of_row      int32 [T*k] out: flat source index f of permuted row r
+ *   row_of_src      int32 [T*k] out: permuted row of flat index f (inverse)
+ *   padded_offsets  int32 [E+1] out: exclusive scan of split sizes each rounded
+ *                   up to a multiple of 128 (the grouped kernels' row layout)
+ *   ws              scratch of mxg_route_permute_workspace_bytes(T,k,E) bytes
+ * Ids outside [0,E) set MXG_ERR_EXPERT_ID in dev_status; such entries are
+ * dropped (their row_of_src is -1).
+ */
+size_t mxg_route_permute_workspace_bytes(int T, int k, int E);
+int mxg_route_permute(const int32_t* ids, int T, int k, int E, int32_t* split_sizes, int32_t* src_of_row,
+                      int32_t* row_of_src, int32_t* padded_offsets, void* ws, size_t ws_bytes,
+                      int32_t* dev_status, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * MXFP8 quantisation of a bf16 matrix x [rows][cols].  [Grouped] "Reducing
+ * memory pressure with MXFP8", Fig. 3; [Overhead] "How MXFP8 reduces memory
+ * use".  Scale rule (OCP MX): e = floor(log2(max|v| over the block)) - 8,
+ * clamped to [-127,127] (an all-zero block gets e = -127); scale byte e+127;
+ * codes = E4M3(v * 2^-e), round to nearest even, saturate to +-448.
+ *   q_row/s_row  (nullable) row-wise: blocks of 32 along cols.
+ *                q_row uint8 [rows][cols]; s_row per `layout`.
+ *   q_col/s_col  (nullable) column-wise: blocks of 32 consecutive rows,
+ *                stored transposed: q_col uint8 [cols][rows]; s_col per layout.
+ * Requires rows % 32 == 0 and cols % 128 == 0; the MMA layout also requires
+ * rows % 128 == 0.
+ */
+int mxg_mxfp8_quantize(const uint16_t* x, int rows, int cols, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                       uint8_t* s_col, int layout, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * Grouped MXFP8 GEMM, row-grouped (the GroupedLinear forward/dgrad shape;
+ * [Grouped] "Grouping fragmented expert workloads"): for each expert e, rows
+ * [padded_offsets[e], padded_offsets[e+1]) of A are multiplied by expert e's
+ * B: D[r][n] = sum_k deq(A)[r][k] * deq(B_e)[n][k], stored as bf16.
+ *   a, sa   uint8 codes [m_cap][K] + scales (MXG_LAYOUT_MMA, R = m_cap)
+ *   b, sb   uint8 codes [E*N][K] + scales (MXG_LAYOUT_MMA, R = E*N)
+ *   padded_offsets int32 [E+1] (device): 128-aligned, monotone, last <= m_cap
+ *   d       bf16 [m_cap][N]; rows outside the groups are not written
+ * Requires K % 128 == 0, N % 128 == 0, m_cap % 128 == 0.
+ */
+int mxg_grouped_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                     const int32_t* padded_offsets, int E, int m_cap, int N, int K, uint16_t* d,
+                     int32_t* dev_status, void* stream);
+
+/* Grouped MXFP8 GEMM, contraction-grouped (the weight-gradient shape): for
+ * each expert e, D_e[m][n] = sum over tokens t in [padded_offsets[e],
+ * padded_offsets[e+1]) of deq(A)[m][t] * deq(B)[n][t].  A and B are stored
+ * token-contiguous (the column-wise quantiser's output).
+ *   a, sa  uint8 [M][t_cap] + scales (MMA layout, R = M, K = t_cap)
+ *   b, sb  uint8 [N][t_cap] + scales (MMA layout, R = N, K = t_cap)
+ *   d      bf16 [E][M][N]; an expert with no tokens gets exact zeros.
+ * Requires M % 128 == 0, N % 128 == 0, t_cap % 128 == 0.
+ */
+int mxg_grouped_gemm_wgrad(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                           const int32_t* padded_offsets, int E, int M, int N, int t_cap, uint16_t* d,
+                           int32_t* dev_status, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * The whole grouped expert MLP.  [Grouped] "Fusing precision conversion and
+ * expert computation" and Fig. 4; [Overhead] "Why fused operations matter".
+ *   forward : permute -> quantise x (and W, both orientations) -> gate-up GEMM
+ *             with fused h = p * SiLU(g) * u and MXFP8 re-quantisation of h ->
+ *             down GEMM -> combine y[t] = sum_j Y[row(t,j)].  The routing
+ *             probability is applied once, inside the activation.
+ *   backward: quantise dy -> dgrad-down GEMM with fused dSwiGLU (emits dGU in
+ *             both MXFP8 orientations and d(prob)) -> wgrad-down -> dgrad-gate-up
+ *             -> wgrad-gate-up -> combine dx, reduce dprobs.
+ * Weight layout: w_gate_up [E][2I][H] (rows 0..I-1 gate, I..2I-1 up),
+ * w_down [E][H][I]; bf16 master weights, no bias.
+ * Shapes: H % 128 == 0, I % 128 == 0, 1 <= k <= E <= 256.
+ * `saved` (mxg_mlp_saved_bytes) is written by the forward and read by the
+ * backward; `workspace` (mxg_mlp_workspace_bytes) is scratch for either call.
+ */
+typedef struct {
+  int32_t T, H, I, E, k;
+  const uint16_t* x;         /* bf16 [T][H]                                  */
+  const int32_t* ids;        /* int32 [T][k] expert ids (e.g. from route_topk) */
+  const float* probs;        /* fp32 [T][k] routing probabilities            */
+  const uint16_t* w_gate_up; /* bf16 [E][2I][H]                              */
+  const uint16_t* w_down;    /* bf16 [E][H][I]                               */
+  uint16_t* y;               /* out bf16 [T][H]                              */
+  int32_t* split_sizes;      /* out int32 [E]                                */
+  void* saved;               /* caller-owned, kept for the backward          */
+  uint64_t saved_bytes;
+  void* workspace;
+  uint64_t workspace_bytes;
+  int32_t save_for_backward; /* 0: inference (skips what only backward needs) */
+  int32_t* dev_status;
+} mxg_mlp_fwd_args;
+
+typedef struct {
+  int32_t T, H, I, E, k;
+  const uint16_t* dy;        /* bf16 [T][H] upstream gradient               */
+  const void* saved;         /* written by the forward with save_for_backward */
+  uint64_t saved_bytes;
+  uint16_t* dx;              /* out bf16 [T][H]                              */
+  uint16_t* dw_gate_up;      /* out bf16 [E][2I][H]                          */
+  uint16_t* dw_down;         /* out bf16 [E][H][I]                           */
+  float* dprobs;             /* out fp32 [T][k]                              */
+  void* workspace;
+  uint64_t workspace_bytes;
+  int32_t* dev_status;
+} mxg_mlp_bwd_args;
+
+/* The forward and backward are sequences of stages, each one kernel launch
+ * (the permute is three).  *_stage() runs a single stage with the same
+ * arguments and checks; running every stage in order equals the full call.
+ * Used to time each kernel with events on the caller's stream. */
+enum {
+  MXG_FWD_PERMUTE = 0,       /* histogram -> scan -> stable scatter (3 launches)       */
+  MXG_FWD_QUANT_WEIGHTS = 1, /* W_gate_up then W_down, both orientations (2 launches) */
+  MXG_FWD_QUANT_X = 2,       /* gather x to the padded layout + quantise               */
+  MXG_FWD_GATE_UP = 3,       /* gate-up GEMM + ScaledSwiGLU + requantise               */
+  MXG_FWD_DOWN = 4,          /* down GEMM                                              */
+  MXG_FWD_COMBINE = 5,       /* y[t] = sum_j Y[row(t, j)]                              */
+  MXG_FWD_NUM_STAGES = 6
+};
+enum {
+  MXG_BWD_QUANT_DY = 0,      /* gather dy + quantise, both orientations               */
+  MXG_BWD_DGRAD_DOWN = 1,    /* dH GEMM + fused dSwiGLU                                */
+  MXG_BWD_WGRAD_DOWN = 2,    /* dW_down GEMM (token-grouped)                           */
+  MXG_BWD_DGRAD_GATE_UP = 3, /* dX GEMM                                                */
+  MXG_BWD_WGRAD_GATE_UP = 4, /* dW_gate_up GEMM (token-grouped)                        */
+  MXG_BWD_COMBINE_DX = 5,    /* dx[t] = sum_j dX[row(t, j)]                            */
+  MXG_BWD_DPROBS = 6,        /* dprobs[t, j] from the per-tile partials                */
+  MXG_BWD_NUM_STAGES = 7
+};
+int mxg_grouped_mlp_fwd_stage(const mxg_mlp_fwd_args* args, int stage, void* stream);
+int mxg_grouped_mlp_bwd_stage(const mxg_mlp_bwd_args* args, int stage, void* stream);
+
+size_t mxg_mlp_saved_bytes(int T, int H, int I, int E, int k);
+size_t mxg_mlp_workspace_bytes(int T, int H, int I, int E, int k);
+int mxg_grouped_mlp_fwd(const mxg_mlp_fwd_args* args, void* stream);
+int mxg_grouped_mlp_bwd(const mxg_mlp_bwd_args* args, void* stream);
+
+/* Debug views into `saved` (device pointers; NULL on bad arguments) used by the
+ * tests to compare intermediates: 0 = GU (bf16 [m_cap][2I], the gate-up GEMM
+ * output before the activation), 1 = padded_offsets (int32 [E+1]),
+ * 2 = row_of_src in the padded layout (int32 [T*k]). */
+const void* mxg_mlp_saved_view(const void* saved, int T, int H, int I, int E, int k, int which);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXG_H_ */

@@ -1,0 +1,261 @@
+"""ctypes binding of libmxg.so (include/mxg.h).  Argument marshalling only:
+every step of the path runs in the library's CUDA kernels.  The functions
+carry the C names; torch tensors provide device memory and the stream.
+
+There is no fallback: if the library is missing or the tensors are not CUDA
+tensors, the call raises."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmxg.so")
+
+MXG_LAYOUT_CANONICAL = 0
+MXG_LAYOUT_MMA = 1
+
+STATUS = {
+    0: "MXG_OK", 1: "MXG_ERR_ARG", 2: "MXG_ERR_SHAPE", 3: "MXG_ERR_ALIGN", 4: "MXG_ERR_ARCH",
+    5: "MXG_ERR_WORKSPACE", 6: "MXG_ERR_CUDA", 16: "MXG_ERR_EXPERT_ID", 17: "MXG_ERR_OFFSETS",
+    18: "MXG_ERR_TIMEOUT",
+}
+
+EXPORTS = [
+    "mxg_status_string", "mxg_device_supported", "mxg_launch_count", "mxg_route_topk",
+    "mxg_route_permute_workspace_bytes", "mxg_route_permute", "mxg_mxfp8_quantize", "mxg_grouped_gemm",
+    "mxg_grouped_gemm_wgrad", "mxg_mlp_saved_bytes", "mxg_mlp_workspace_bytes", "mxg_grouped_mlp_fwd",
+    "mxg_grouped_mlp_bwd", "mxg_mlp_saved_view", "mxg_grouped_mlp_fwd_stage", "mxg_grouped_mlp_bwd_stage",
+]
+
+FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
+BWD_STAGES = ["quant_dy", "dgrad_down", "wgrad_down", "dgrad_gate_up", "wgrad_gate_up", "combine_dx", "dprobs"]
+
+
+class MxgError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} -> {STATUS.get(code, code)}: {status_string(code)}")
+
+
+class MlpFwdArgs(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("x", ctypes.c_void_p), ("ids", ctypes.c_void_p),
+                ("probs", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("split_sizes", ctypes.c_void_p), ("saved", ctypes.c_void_p),
+                ("saved_bytes", ctypes.c_uint64), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_uint64), ("save_for_backward", ctypes.c_int32),
+                ("dev_status", ctypes.c_void_p)]
+
+
+class MlpBwdArgs(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("dy", ctypes.c_void_p), ("saved", ctypes.c_void_p),
+                ("saved_bytes", ctypes.c_uint64), ("dx", ctypes.c_void_p), ("dw_gate_up", ctypes.c_void_p),
+                ("dw_down", ctypes.c_void_p), ("dprobs", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_uint64), ("dev_status", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmxg.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m mxfp8_grouped_gemm_gb300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    I32, U64, SZ, P = ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t, ctypes.c_void_p
+    sig = {
+        "mxg_status_string": (ctypes.c_char_p, [I32]),
+        "mxg_device_supported": (I32, []),
+        "mxg_launch_count": (U64, []),
+        "mxg_route_topk": (I32, [P, I32, I32, I32, P, P, P]),
+        "mxg_route_permute_workspace_bytes": (SZ, [I32, I32, I32]),
+        "mxg_route_permute": (I32, [P, I32, I32, I32, P, P, P, P, P, SZ, P, P]),
+        "mxg_mxfp8_quantize": (I32, [P, I32, I32, P, P, P, P, I32, P]),
+        "mxg_grouped_gemm": (I32, [P, P, P, P, P, I32, I32, I32, I32, P, P, P]),
+        "mxg_grouped_gemm_wgrad": (I32, [P, P, P, P, P, I32, I32, I32, I32, P, P, P]),
+        "mxg_mlp_saved_bytes": (SZ, [I32, I32, I32, I32, I32]),
+        "mxg_mlp_workspace_bytes": (SZ, [I32, I32, I32, I32, I32]),
+        "mxg_grouped_mlp_fwd": (I32, [ctypes.POINTER(MlpFwdArgs), P]),
+        "mxg_grouped_mlp_bwd": (I32, [ctypes.POINTER(MlpBwdArgs), P]),
+        "mxg_mlp_saved_view": (P, [P, I32, I32, I32, I32, I32, I32]),
+        "mxg_grouped_mlp_fwd_stage": (I32, [ctypes.POINTER(MlpFwdArgs), I32, P]),
+        "mxg_grouped_mlp_bwd_stage": (I32, [ctypes.POINTER(MlpBwdArgs), I32, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def status_string(code: int) -> str:
+    return lib().mxg_status_string(int(code)).decode()
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise MxgError(fn, code)
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name: str = "tensor") -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _bits(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+
+
+# ------------------------------------------------------------------ entries --
+
+def mxg_device_supported() -> bool:
+    return bool(lib().mxg_device_supported())
+
+
+def mxg_launch_count() -> int:
+    return int(lib().mxg_launch_count())
+
+
+def mxg_route_topk(logits: torch.Tensor, k: int, ids=None, probs=None, stream=None):
+    T, E = logits.shape
+    ids = torch.empty((T, k), dtype=torch.int32, device=logits.device) if ids is None else ids
+    probs = torch.empty((T, k), dtype=torch.float32, device=logits.device) if probs is None else probs
+    _check("mxg_route_topk", lib().mxg_route_topk(_ptr(logits, torch.float32, "logits"), T, E, k,
+                                                  _ptr(ids, torch.int32, "ids"), _ptr(probs, torch.float32, "probs"),
+                                                  _stream(stream)))
+    return ids, probs
+
+
+def mxg_route_permute(ids: torch.Tensor, E: int, dev_status: torch.Tensor, stream=None) -> dict:
+    T, k = ids.shape
+    dev = ids.device
+    ws_bytes = int(lib().mxg_route_permute_workspace_bytes(T, k, E))
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    out = {"split_sizes": torch.empty(E, dtype=torch.int32, device=dev),
+           "src_of_row": torch.empty(T * k, dtype=torch.int32, device=dev),
+           "row_of_src": torch.empty(T * k, dtype=torch.int32, device=dev),
+           "padded_offsets": torch.empty(E + 1, dtype=torch.int32, device=dev)}
+    _check("mxg_route_permute", lib().mxg_route_permute(
+        _ptr(ids, torch.int32, "ids"), T, k, E, _ptr(out["split_sizes"]), _ptr(out["src_of_row"]),
+        _ptr(out["row_of_src"]), _ptr(out["padded_offsets"]), _ptr(ws), ws_bytes,
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+    return out
+
+
+def mxfp8_scale_bytes(rows: int, cols: int) -> int:
+    return rows * cols // 32
+
+
+def mxg_mxfp8_quantize(x: torch.Tensor, row: bool = True, col: bool = False, layout: int = MXG_LAYOUT_CANONICAL,
+                       stream=None) -> dict:
+    """x bf16 [rows, cols] -> {'q_row','s_row'} and/or {'q_col','s_col'} (uint8)."""
+    rows, cols = x.shape
+    dev = x.device
+    out = {}
+    if row:
+        out["q_row"] = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        out["s_row"] = torch.empty(rows * cols // 32, dtype=torch.uint8, device=dev)
+    if col:
+        out["q_col"] = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+        out["s_col"] = torch.empty(rows * cols // 32, dtype=torch.uint8, device=dev)
+    _check("mxg_mxfp8_quantize", lib().mxg_mxfp8_quantize(
+        _ptr(_bits(x), None, "x"), rows, cols, _ptr(out.get("q_row")), _ptr(out.get("s_row")),
+        _ptr(out.get("q_col")), _ptr(out.get("s_col")), layout, _stream(stream)))
+    return out
+
+
+def mxg_grouped_gemm(a, sa, b, sb, padded_offsets, E: int, N: int, K: int, dev_status, d=None, stream=None):
+    m_cap = a.shape[0]
+    d = torch.empty((m_cap, N), dtype=torch.bfloat16, device=a.device) if d is None else d
+    _check("mxg_grouped_gemm", lib().mxg_grouped_gemm(
+        _ptr(a, torch.uint8, "a"), _ptr(sa, torch.uint8, "sa"), _ptr(b, torch.uint8, "b"), _ptr(sb, torch.uint8, "sb"),
+        _ptr(padded_offsets, torch.int32, "padded_offsets"), E, m_cap, N, K, _ptr(_bits(d)),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+    return d
+
+
+def mxg_grouped_gemm_wgrad(a, sa, b, sb, padded_offsets, E: int, dev_status, d=None, stream=None):
+    M, t_cap = a.shape
+    N = b.shape[0]
+    d = torch.empty((E, M, N), dtype=torch.bfloat16, device=a.device) if d is None else d
+    _check("mxg_grouped_gemm_wgrad", lib().mxg_grouped_gemm_wgrad(
+        _ptr(a, torch.uint8, "a"), _ptr(sa, torch.uint8, "sa"), _ptr(b, torch.uint8, "b"), _ptr(sb, torch.uint8, "sb"),
+        _ptr(padded_offsets, torch.int32, "padded_offsets"), E, M, N, t_cap, _ptr(_bits(d)),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+    return d
+
+
+def mxg_mlp_saved_bytes(T, H, I, E, k) -> int:
+    return int(lib().mxg_mlp_saved_bytes(T, H, I, E, k))
+
+
+def mxg_mlp_workspace_bytes(T, H, I, E, k) -> int:
+    return int(lib().mxg_mlp_workspace_bytes(T, H, I, E, k))
+
+
+def mxg_mlp_saved_view(saved: torch.Tensor, T, H, I, E, k, which: int) -> int:
+    return int(lib().mxg_mlp_saved_view(_ptr(saved), T, H, I, E, k, which) or 0)
+
+
+def mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, saved, workspace, dev_status, y=None, split_sizes=None,
+                        save_for_backward: bool = True, stream=None, stage: int | None = None):
+    """Full forward, or one stage of it (FWD_STAGES index) when ``stage`` is given."""
+    T, H = x.shape
+    k = ids.shape[1]
+    E, N2, _ = w_gate_up.shape
+    I = N2 // 2
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if y is None else y
+    split_sizes = torch.empty(E, dtype=torch.int32, device=x.device) if split_sizes is None else split_sizes
+    a = MlpFwdArgs(T, H, I, E, k, _ptr(_bits(x), torch.int16, "x"), _ptr(ids, torch.int32, "ids"),
+                   _ptr(probs, torch.float32, "probs"), _ptr(_bits(w_gate_up), torch.int16, "w_gate_up"),
+                   _ptr(_bits(w_down), torch.int16, "w_down"), _ptr(_bits(y)), _ptr(split_sizes, torch.int32),
+                   _ptr(saved, torch.uint8, "saved"), saved.numel(), _ptr(workspace, torch.uint8, "workspace"),
+                   workspace.numel(), 1 if save_for_backward else 0, _ptr(dev_status, torch.int32, "dev_status"))
+    if stage is None:
+        _check("mxg_grouped_mlp_fwd", lib().mxg_grouped_mlp_fwd(ctypes.byref(a), _stream(stream)))
+    else:
+        _check("mxg_grouped_mlp_fwd_stage", lib().mxg_grouped_mlp_fwd_stage(ctypes.byref(a), stage, _stream(stream)))
+    return y, split_sizes
+
+
+def mxg_grouped_mlp_bwd(dy, saved, workspace, dev_status, E: int, I: int, k: int, dx=None, dw_gate_up=None,
+                        dw_down=None, dprobs=None, stream=None, stage: int | None = None):
+    """Full backward, or one stage of it (BWD_STAGES index) when ``stage`` is given."""
+    T, H = dy.shape
+    dev = dy.device
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if dx is None else dx
+    dw_gate_up = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev) if dw_gate_up is None else dw_gate_up
+    dw_down = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev) if dw_down is None else dw_down
+    dprobs = torch.empty((T, k), dtype=torch.float32, device=dev) if dprobs is None else dprobs
+    a = MlpBwdArgs(T, H, I, E, k, _ptr(_bits(dy), torch.int16, "dy"), _ptr(saved, torch.uint8, "saved"),
+                   saved.numel(), _ptr(_bits(dx)), _ptr(_bits(dw_gate_up)), _ptr(_bits(dw_down)),
+                   _ptr(dprobs, torch.float32), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+                   _ptr(dev_status, torch.int32, "dev_status"))
+    if stage is None:
+        _check("mxg_grouped_mlp_bwd", lib().mxg_grouped_mlp_bwd(ctypes.byref(a), _stream(stream)))
+    else:
+        _check("mxg_grouped_mlp_bwd_stage", lib().mxg_grouped_mlp_bwd_stage(ctypes.byref(a), stage, _stream(stream)))
+    return dx, dw_gate_up, dw_down, dprobs

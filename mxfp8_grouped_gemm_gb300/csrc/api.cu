@@ -1,0 +1,664 @@
+// C-ABI entry points: argument validation, the layout of the caller-owned
+// saved/workspace buffers, and the launch sequence of the forward and backward
+// passes.  Nothing here allocates or synchronises; every call only enqueues
+// work on the caller's stream.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mxg {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int64_t kAlign = 256;
+
+inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Row capacity of the per-expert padded layout: every group starts on a
+// multiple of 128 rows, so sum_e roundup(m_e, 128) <= roundup(T*k, 128) + 128*E.
+inline int64_t row_cap(int64_t T, int64_t k, int64_t E) { return align_up(T * k, 128) + 128 * E; }
+
+struct Carver {
+  int64_t off = 0;
+  int64_t take(int64_t bytes) {
+    const int64_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  }
+};
+
+// Byte offsets of every buffer inside `saved` and `workspace`.
+struct Plan {
+  int64_t T, H, I, E, k, R, Rc;
+  // saved (forward -> backward)
+  int64_t poff, prow_src, prow_of_src, probs_perm, gu, xc, sxc, hc, shc, wguT, swguT, wdT, swdT, saved_bytes;
+  // forward scratch
+  int64_t counts, bases, offsets, xq, sxq, hq, shq, wgu, swgu, wd, swd, yperm, fwd_bytes;
+  // backward scratch
+  int64_t dyq, sdyq, dyc, sdyc, dguq, sdguq, dguc, sdguc, dxperm, dp, bwd_bytes;
+  int64_t dp_ld;
+
+  Plan(int64_t T_, int64_t H_, int64_t I_, int64_t E_, int64_t k_) : T(T_), H(H_), I(I_), E(E_), k(k_) {
+    R = T * k;
+    Rc = row_cap(T, k, E);
+    Carver s;
+    poff = s.take(4 * (E + 1));
+    prow_src = s.take(4 * Rc);
+    prow_of_src = s.take(4 * R);
+    probs_perm = s.take(4 * Rc);
+    gu = s.take(2 * Rc * 2 * I);
+    xc = s.take(H * Rc);
+    sxc = s.take(H * Rc / 32);
+    hc = s.take(I * Rc);
+    shc = s.take(I * Rc / 32);
+    wguT = s.take(E * H * 2 * I);
+    swguT = s.take(E * H * 2 * I / 32);
+    wdT = s.take(E * I * H);
+    swdT = s.take(E * I * H / 32);
+    saved_bytes = s.off;
+
+    Carver f;
+    const int64_t nblk = permute_num_blocks(static_cast<int>(R));
+    counts = f.take(4 * nblk * E);
+    bases = f.take(4 * nblk * E);
+    offsets = f.take(4 * (E + 1));
+    xq = f.take(Rc * H);
+    sxq = f.take(Rc * H / 32);
+    hq = f.take(Rc * I);
+    shq = f.take(Rc * I / 32);
+    wgu = f.take(E * 2 * I * H);
+    swgu = f.take(E * 2 * I * H / 32);
+    wd = f.take(E * H * I);
+    swd = f.take(E * H * I / 32);
+    yperm = f.take(2 * Rc * H);
+    fwd_bytes = f.off;
+
+    Carver b;
+    const int bn = gemm_pick_bn(EPI_DSWIGLU, static_cast<int>(I));
+    dp_ld = I / bn;
+    dyq = b.take(Rc * H);
+    sdyq = b.take(Rc * H / 32);
+    dyc = b.take(H * Rc);
+    sdyc = b.take(H * Rc / 32);
+    dguq = b.take(Rc * 2 * I);
+    sdguq = b.take(Rc * 2 * I / 32);
+    dguc = b.take(2 * I * Rc);
+    sdguc = b.take(2 * I * Rc / 32);
+    dxperm = b.take(2 * Rc * H);
+    dp = b.take(4 * Rc * dp_ld);
+    bwd_bytes = b.off;
+  }
+  int64_t ws_bytes() const { return fwd_bytes > bwd_bytes ? fwd_bytes : bwd_bytes; }
+};
+
+template <typename T>
+inline T* at(void* base, int64_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
+}
+template <typename T>
+inline const T* at(const void* base, int64_t off) {
+  return reinterpret_cast<const T*>(static_cast<const uint8_t*>(base) + off);
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA; }
+
+#define MXG_TRY(expr)                                 \
+  do {                                                \
+    if ((expr) != cudaSuccess) return MXG_ERR_CUDA;   \
+  } while (0)
+
+bool mlp_shape_ok(int T, int H, int I, int E, int k) {
+  if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return false;
+  if (H % 128 || I % 128) return false;
+  if (k > E || E > 256 || k > 32) return false;
+  return true;
+}
+
+}  // namespace
+}  // namespace mxg
+
+using namespace mxg;
+
+extern "C" {
+
+const char* mxg_status_string(int status) {
+  switch (status) {
+    case MXG_OK: return "ok";
+    case MXG_ERR_ARG: return "invalid argument (null pointer, non-positive size or bad enum)";
+    case MXG_ERR_SHAPE: return "shape violates the call's divisibility rules";
+    case MXG_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case MXG_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case MXG_ERR_WORKSPACE: return "scratch or saved buffer too small";
+    case MXG_ERR_CUDA: return "CUDA runtime error or kernel launch failure";
+    case MXG_ERR_EXPERT_ID: return "expert id outside [0, E)";
+    case MXG_ERR_OFFSETS: return "group offsets not monotone, not 128-aligned or beyond capacity";
+    case MXG_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
+    default: return "unknown status";
+  }
+}
+
+int mxg_device_supported(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return 0;
+  return (major == 10 && minor == 3) ? 1 : 0;
+}
+
+uint64_t mxg_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int mxg_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* probs, void* stream) {
+  if (!logits || !ids || !probs) return MXG_ERR_ARG;
+  if (T <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
+  if (k > E || E > 256 || k > 32) return MXG_ERR_SHAPE;
+  if (!aligned16(logits) || !aligned16(ids) || !aligned16(probs)) return MXG_ERR_ALIGN;
+  return cuda_status(launch_topk(logits, T, E, k, ids, probs, static_cast<cudaStream_t>(stream)));
+}
+
+size_t mxg_route_permute_workspace_bytes(int T, int k, int E) {
+  if (T <= 0 || k <= 0 || E <= 0) return 0;
+  const int64_t nblk = permute_num_blocks(T * k);
+  return static_cast<size_t>(align_up(4 * nblk * E, kAlign) * 2 + align_up(4 * (E + 1), kAlign));
+}
+
+int mxg_route_permute(const int32_t* ids, int T, int k, int E, int32_t* split_sizes, int32_t* src_of_row,
+                      int32_t* row_of_src, int32_t* padded_offsets, void* ws, size_t ws_bytes,
+                      int32_t* dev_status, void* stream) {
+  if (!ids || !split_sizes || !src_of_row || !row_of_src || !padded_offsets || !ws || !dev_status)
+    return MXG_ERR_ARG;
+  if (T <= 0 || k <= 0 || E <= 0) return MXG_ERR_ARG;
+  if (k > E || E > 256) return MXG_ERR_SHAPE;
+  if (!aligned16(ids) || !aligned16(split_sizes) || !aligned16(src_of_row) || !aligned16(row_of_src) ||
+      !aligned16(padded_offsets) || !aligned16(ws))
+    return MXG_ERR_ALIGN;
+  if (ws_bytes < mxg_route_permute_workspace_bytes(T, k, E)) return MXG_ERR_WORKSPACE;
+  const int64_t nblk = permute_num_blocks(T * k);
+  PermuteParams p{};
+  p.ids = ids;
+  p.R = T * k;
+  p.E = E;
+  p.counts = at<int32_t>(ws, 0);
+  p.bases = at<int32_t>(ws, align_up(4 * nblk * E, kAlign));
+  p.offsets = at<int32_t>(ws, 2 * align_up(4 * nblk * E, kAlign));
+  p.padded_offsets = padded_offsets;
+  p.split_sizes = split_sizes;
+  p.src_of_row = src_of_row;
+  p.row_of_src = row_of_src;
+  p.status = dev_status;
+  return cuda_status(launch_permute(p, static_cast<cudaStream_t>(stream)));
+}
+
+int mxg_mxfp8_quantize(const uint16_t* x, int rows, int cols, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                       uint8_t* s_col, int layout, void* stream) {
+  if (!x || rows <= 0 || cols <= 0) return MXG_ERR_ARG;
+  if (layout != MXG_LAYOUT_CANONICAL && layout != MXG_LAYOUT_MMA) return MXG_ERR_ARG;
+  if ((q_row == nullptr) != (s_row == nullptr) || (q_col == nullptr) != (s_col == nullptr)) return MXG_ERR_ARG;
+  if (!q_row && !q_col) return MXG_ERR_ARG;
+  // the kernel tiles 32 rows x 128 columns
+  if (rows % 32 || cols % 128) return MXG_ERR_SHAPE;
+  if (layout == MXG_LAYOUT_MMA && rows % 128) return MXG_ERR_SHAPE;
+  if (!aligned16(x) || (q_row && !aligned16(q_row)) || (q_col && !aligned16(q_col))) return MXG_ERR_ALIGN;
+  QuantParams p{};
+  p.x = x;
+  p.ld_x = cols;
+  p.x_batch_stride = 0;
+  p.src_div = 1;
+  p.rows = rows;
+  p.cols = cols;
+  p.batch = 1;
+  p.q_row = q_row;
+  p.s_row = s_row;
+  p.sf_row_rows = rows;
+  p.q_col = q_col;
+  p.s_col = s_col;
+  p.ld_col = rows;
+  p.sf_col_rows = cols;
+  p.layout = layout;
+  return cuda_status(launch_quant(p, static_cast<cudaStream_t>(stream)));
+}
+
+int mxg_grouped_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                     const int32_t* padded_offsets, int E, int m_cap, int N, int K, uint16_t* d,
+                     int32_t* dev_status, void* stream) {
+  if (!a || !sa || !b || !sb || !padded_offsets || !d || !dev_status) return MXG_ERR_ARG;
+  if (E <= 0 || m_cap <= 0 || N <= 0 || K <= 0) return MXG_ERR_ARG;
+  if (E > 256 || K % 128 || N % 128 || m_cap % 128) return MXG_ERR_SHAPE;
+  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(d) ||
+      !aligned16(padded_offsets))
+    return MXG_ERR_ALIGN;
+  GemmArgs g{};
+  g.epi = EPI_BF16;
+  g.kgroup = false;
+  g.a = a;
+  g.sa = sa;
+  g.a_rows = m_cap;
+  g.a_cols = K;
+  g.b = b;
+  g.sb = sb;
+  g.b_rows = static_cast<int64_t>(E) * N;
+  g.b_cols = K;
+  g.poff = padded_offsets;
+  g.E = E;
+  g.M = m_cap;
+  g.N = N;
+  g.K = K;
+  g.b_rows_per_expert = N;
+  g.d = d;
+  g.ldd = N;
+  g.status = dev_status;
+  g.tiles_upper = static_cast<int64_t>(m_cap / 128) * (N / gemm_pick_bn(EPI_BF16, N));
+  return cuda_status(launch_gemm(g, static_cast<cudaStream_t>(stream)));
+}
+
+int mxg_grouped_gemm_wgrad(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                           const int32_t* padded_offsets, int E, int M, int N, int t_cap, uint16_t* d,
+                           int32_t* dev_status, void* stream) {
+  if (!a || !sa || !b || !sb || !padded_offsets || !d || !dev_status) return MXG_ERR_ARG;
+  if (E <= 0 || M <= 0 || N <= 0 || t_cap <= 0) return MXG_ERR_ARG;
+  if (E > 256 || M % 128 || N % 128 || t_cap % 128) return MXG_ERR_SHAPE;
+  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(d) ||
+      !aligned16(padded_offsets))
+    return MXG_ERR_ALIGN;
+  GemmArgs g{};
+  g.epi = EPI_BF16;
+  g.kgroup = true;
+  g.a = a;
+  g.sa = sa;
+  g.a_rows = M;
+  g.a_cols = t_cap;
+  g.b = b;
+  g.sb = sb;
+  g.b_rows = N;
+  g.b_cols = t_cap;
+  g.poff = padded_offsets;
+  g.E = E;
+  g.M = M;
+  g.N = N;
+  g.d = d;
+  g.ldd = N;
+  g.status = dev_status;
+  g.tiles_upper = static_cast<int64_t>(E) * (M / 128) * (N / gemm_pick_bn(EPI_BF16, N));
+  return cuda_status(launch_gemm(g, static_cast<cudaStream_t>(stream)));
+}
+
+size_t mxg_mlp_saved_bytes(int T, int H, int I, int E, int k) {
+  if (!mlp_shape_ok(T, H, I, E, k)) return 0;
+  return static_cast<size_t>(Plan(T, H, I, E, k).saved_bytes);
+}
+
+size_t mxg_mlp_workspace_bytes(int T, int H, int I, int E, int k) {
+  if (!mlp_shape_ok(T, H, I, E, k)) return 0;
+  return static_cast<size_t>(Plan(T, H, I, E, k).ws_bytes());
+}
+
+const void* mxg_mlp_saved_view(const void* saved, int T, int H, int I, int E, int k, int which) {
+  if (!saved || !mlp_shape_ok(T, H, I, E, k)) return nullptr;
+  const Plan pl(T, H, I, E, k);
+  switch (which) {
+    case 0: return at<uint8_t>(saved, pl.gu);
+    case 1: return at<uint8_t>(saved, pl.poff);
+    case 2: return at<uint8_t>(saved, pl.prow_of_src);
+    default: return nullptr;
+  }
+}
+
+static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
+  if (!A) return MXG_ERR_ARG;
+  const int T = A->T, H = A->H, I = A->I, E = A->E, k = A->k;
+  if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
+  if (!mlp_shape_ok(T, H, I, E, k)) return MXG_ERR_SHAPE;
+  if (!A->x || !A->ids || !A->probs || !A->w_gate_up || !A->w_down || !A->y || !A->split_sizes || !A->saved ||
+      !A->workspace || !A->dev_status)
+    return MXG_ERR_ARG;
+  if (!aligned16(A->x) || !aligned16(A->ids) || !aligned16(A->probs) || !aligned16(A->w_gate_up) ||
+      !aligned16(A->w_down) || !aligned16(A->y) || !aligned16(A->split_sizes) || !aligned16(A->saved) ||
+      !aligned16(A->workspace))
+    return MXG_ERR_ALIGN;
+  const Plan pl(T, H, I, E, k);
+  if (A->saved_bytes < static_cast<uint64_t>(pl.saved_bytes) ||
+      A->workspace_bytes < static_cast<uint64_t>(pl.ws_bytes()))
+    return MXG_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* sv = A->saved;
+  void* ws = A->workspace;
+  const bool save = A->save_for_backward != 0;
+  int32_t* st = A->dev_status;
+  const int32_t* poff = at<int32_t>(sv, pl.poff);
+  auto run = [stage](int id) { return stage < 0 || stage == id; };
+
+  // F2: permute (histogram -> scan -> stable scatter) into the padded layout
+  if (run(MXG_FWD_PERMUTE)) {
+  MXG_TRY(cudaMemsetAsync(at<int32_t>(sv, pl.prow_src), 0xFF, 4 * pl.Rc, s));
+  PermuteParams pp{};
+  pp.ids = A->ids;
+  pp.R = static_cast<int32_t>(pl.R);
+  pp.E = E;
+  pp.counts = at<int32_t>(ws, pl.counts);
+  pp.bases = at<int32_t>(ws, pl.bases);
+  pp.offsets = at<int32_t>(ws, pl.offsets);
+  pp.padded_offsets = at<int32_t>(sv, pl.poff);
+  pp.split_sizes = A->split_sizes;
+  pp.prow_src = at<int32_t>(sv, pl.prow_src);
+  pp.prow_of_src = at<int32_t>(sv, pl.prow_of_src);
+  pp.status = st;
+  MXG_TRY(launch_permute(pp, s));
+  }
+
+  // F4: weights, both orientations in one pass (the transposed ones only for backward)
+  if (run(MXG_FWD_QUANT_WEIGHTS)) {
+  QuantParams wq{};
+  wq.x = A->w_gate_up;
+  wq.ld_x = H;
+  wq.x_batch_stride = 2 * pl.I * H;
+  wq.src_div = 1;
+  wq.rows = 2 * I;
+  wq.cols = H;
+  wq.batch = E;
+  wq.q_row = at<uint8_t>(ws, pl.wgu);
+  wq.s_row = at<uint8_t>(ws, pl.swgu);
+  wq.sf_row_rows = pl.E * 2 * I;
+  if (save) {
+    wq.q_col = at<uint8_t>(sv, pl.wguT);
+    wq.s_col = at<uint8_t>(sv, pl.swguT);
+    wq.ld_col = 2 * I;
+    wq.sf_col_rows = pl.E * H;
+  }
+  wq.layout = MXG_LAYOUT_MMA;
+  MXG_TRY(launch_quant(wq, s));
+  QuantParams dq = wq;
+  dq.x = A->w_down;
+  dq.ld_x = I;
+  dq.x_batch_stride = pl.H * I;
+  dq.rows = H;
+  dq.cols = I;
+  dq.q_row = at<uint8_t>(ws, pl.wd);
+  dq.s_row = at<uint8_t>(ws, pl.swd);
+  dq.sf_row_rows = pl.E * H;
+  if (save) {
+    dq.q_col = at<uint8_t>(sv, pl.wdT);
+    dq.s_col = at<uint8_t>(sv, pl.swdT);
+    dq.ld_col = H;
+    dq.sf_col_rows = pl.E * I;
+  }
+  MXG_TRY(launch_quant(dq, s));
+  }
+
+  // F3: gather x into the padded per-expert layout and quantise (row-wise along
+  // H for the gate-up GEMM; token-column-wise for the gate-up weight gradient)
+  if (run(MXG_FWD_QUANT_X)) {
+  QuantParams xq{};
+  xq.x = A->x;
+  xq.ld_x = H;
+  xq.src_rows = at<int32_t>(sv, pl.prow_src);
+  xq.src_div = k;
+  xq.probs = A->probs;
+  xq.probs_perm = at<float>(sv, pl.probs_perm);
+  xq.rows = static_cast<int32_t>(pl.Rc);
+  xq.cols = H;
+  xq.batch = 1;
+  xq.rows_valid = poff + E;
+  xq.q_row = at<uint8_t>(ws, pl.xq);
+  xq.s_row = at<uint8_t>(ws, pl.sxq);
+  xq.sf_row_rows = pl.Rc;
+  if (save) {
+    xq.q_col = at<uint8_t>(sv, pl.xc);
+    xq.s_col = at<uint8_t>(sv, pl.sxc);
+    xq.ld_col = pl.Rc;
+    xq.sf_col_rows = H;
+  }
+  xq.layout = MXG_LAYOUT_MMA;
+  MXG_TRY(launch_quant(xq, s));
+  }
+
+  // F5: gate-up grouped GEMM + ScaledSwiGLU + MXFP8 re-quantisation of h
+  if (run(MXG_FWD_GATE_UP)) {
+  GemmArgs g{};
+  g.epi = EPI_SWIGLU;
+  g.a = at<uint8_t>(ws, pl.xq);
+  g.sa = at<uint8_t>(ws, pl.sxq);
+  g.a_rows = pl.Rc;
+  g.a_cols = H;
+  g.b = at<uint8_t>(ws, pl.wgu);
+  g.sb = at<uint8_t>(ws, pl.swgu);
+  g.b_rows = pl.E * 2 * I;
+  g.b_cols = H;
+  g.poff = poff;
+  g.E = E;
+  g.M = static_cast<int32_t>(pl.Rc);
+  g.N = 2 * I;
+  g.K = H;
+  g.b_rows_per_expert = 2 * I;
+  g.I = I;
+  g.probs_perm = at<float>(sv, pl.probs_perm);
+  g.gu_save = save ? at<uint16_t>(sv, pl.gu) : nullptr;
+  g.q_out = at<uint8_t>(ws, pl.hq);
+  g.s_out = at<uint8_t>(ws, pl.shq);
+  g.q_out_ld = I;
+  g.s_out_rows = pl.Rc;
+  if (save) {
+    g.qc_out = at<uint8_t>(sv, pl.hc);
+    g.sc_out = at<uint8_t>(sv, pl.shc);
+    g.qc_ld = pl.Rc;
+    g.sc_rows = I;
+  }
+  g.status = st;
+  g.tiles_upper = (pl.Rc / 128) * (I / 128);
+  MXG_TRY(launch_gemm(g, s));
+  }
+
+  // F6: down grouped GEMM
+  if (run(MXG_FWD_DOWN)) {
+  GemmArgs d{};
+  d.epi = EPI_BF16;
+  d.a = at<uint8_t>(ws, pl.hq);
+  d.sa = at<uint8_t>(ws, pl.shq);
+  d.a_rows = pl.Rc;
+  d.a_cols = I;
+  d.b = at<uint8_t>(ws, pl.wd);
+  d.sb = at<uint8_t>(ws, pl.swd);
+  d.b_rows = pl.E * H;
+  d.b_cols = I;
+  d.poff = poff;
+  d.E = E;
+  d.M = static_cast<int32_t>(pl.Rc);
+  d.N = H;
+  d.K = I;
+  d.b_rows_per_expert = H;
+  d.d = at<uint16_t>(ws, pl.yperm);
+  d.ldd = H;
+  d.status = st;
+  d.tiles_upper = (pl.Rc / 128) * (H / gemm_pick_bn(EPI_BF16, H));
+  MXG_TRY(launch_gemm(d, s));
+  }
+
+  // F7: combine
+  if (run(MXG_FWD_COMBINE))
+    MXG_TRY(launch_combine(at<uint16_t>(ws, pl.yperm), at<int32_t>(sv, pl.prow_of_src), T, k, H, A->y, s));
+  return MXG_OK;
+}
+
+int mxg_grouped_mlp_fwd(const mxg_mlp_fwd_args* A, void* stream) { return fwd_impl(A, -1, stream); }
+
+int mxg_grouped_mlp_fwd_stage(const mxg_mlp_fwd_args* A, int stage, void* stream) {
+  if (stage < 0 || stage >= MXG_FWD_NUM_STAGES) return MXG_ERR_ARG;
+  return fwd_impl(A, stage, stream);
+}
+
+static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
+  if (!A) return MXG_ERR_ARG;
+  const int T = A->T, H = A->H, I = A->I, E = A->E, k = A->k;
+  if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
+  if (!mlp_shape_ok(T, H, I, E, k)) return MXG_ERR_SHAPE;
+  if (!A->dy || !A->saved || !A->dx || !A->dw_gate_up || !A->dw_down || !A->dprobs || !A->workspace ||
+      !A->dev_status)
+    return MXG_ERR_ARG;
+  if (!aligned16(A->dy) || !aligned16(A->saved) || !aligned16(A->dx) || !aligned16(A->dw_gate_up) ||
+      !aligned16(A->dw_down) || !aligned16(A->dprobs) || !aligned16(A->workspace))
+    return MXG_ERR_ALIGN;
+  const Plan pl(T, H, I, E, k);
+  if (A->saved_bytes < static_cast<uint64_t>(pl.saved_bytes) ||
+      A->workspace_bytes < static_cast<uint64_t>(pl.ws_bytes()))
+    return MXG_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* sv = A->saved;
+  void* ws = A->workspace;
+  int32_t* st = A->dev_status;
+  const int32_t* poff = at<int32_t>(sv, pl.poff);
+  auto run = [stage](int id) { return stage < 0 || stage == id; };
+
+  // B1: gather dy and quantise (row-wise along H for dgrad, token-column-wise for wgrad)
+  if (run(MXG_BWD_QUANT_DY)) {
+  QuantParams yq{};
+  yq.x = A->dy;
+  yq.ld_x = H;
+  yq.src_rows = at<int32_t>(sv, pl.prow_src);
+  yq.src_div = k;
+  yq.rows = static_cast<int32_t>(pl.Rc);
+  yq.cols = H;
+  yq.batch = 1;
+  yq.rows_valid = poff + E;
+  yq.q_row = at<uint8_t>(ws, pl.dyq);
+  yq.s_row = at<uint8_t>(ws, pl.sdyq);
+  yq.sf_row_rows = pl.Rc;
+  yq.q_col = at<uint8_t>(ws, pl.dyc);
+  yq.s_col = at<uint8_t>(ws, pl.sdyc);
+  yq.ld_col = pl.Rc;
+  yq.sf_col_rows = H;
+  yq.layout = MXG_LAYOUT_MMA;
+  MXG_TRY(launch_quant(yq, s));
+  }
+
+  // B2: dH = dY W_down (MX along H) with fused dSwiGLU -> dGU (both orientations), d(prob) partials
+  if (run(MXG_BWD_DGRAD_DOWN)) {
+  GemmArgs g{};
+  g.epi = EPI_DSWIGLU;
+  g.a = at<uint8_t>(ws, pl.dyq);
+  g.sa = at<uint8_t>(ws, pl.sdyq);
+  g.a_rows = pl.Rc;
+  g.a_cols = H;
+  g.b = at<uint8_t>(sv, pl.wdT);
+  g.sb = at<uint8_t>(sv, pl.swdT);
+  g.b_rows = pl.E * I;
+  g.b_cols = H;
+  g.poff = poff;
+  g.E = E;
+  g.M = static_cast<int32_t>(pl.Rc);
+  g.N = I;
+  g.K = H;
+  g.b_rows_per_expert = I;
+  g.I = I;
+  g.probs_perm = at<float>(sv, pl.probs_perm);
+  g.gu_save = const_cast<uint16_t*>(at<uint16_t>(sv, pl.gu));
+  g.q_out = at<uint8_t>(ws, pl.dguq);
+  g.s_out = at<uint8_t>(ws, pl.sdguq);
+  g.q_out_ld = 2 * I;
+  g.s_out_rows = pl.Rc;
+  g.qc_out = at<uint8_t>(ws, pl.dguc);
+  g.sc_out = at<uint8_t>(ws, pl.sdguc);
+  g.qc_ld = pl.Rc;
+  g.sc_rows = 2 * I;
+  g.dp_part = at<float>(ws, pl.dp);
+  g.dp_ld = static_cast<int32_t>(pl.dp_ld);
+  g.status = st;
+  g.tiles_upper = (pl.Rc / 128) * pl.dp_ld;
+  MXG_TRY(launch_gemm(g, s));
+  }
+
+  // B3: dW_down[e] = dYc^T Hc over the tokens of e
+  if (run(MXG_BWD_WGRAD_DOWN)) {
+  GemmArgs w{};
+  w.epi = EPI_BF16;
+  w.kgroup = true;
+  w.a = at<uint8_t>(ws, pl.dyc);
+  w.sa = at<uint8_t>(ws, pl.sdyc);
+  w.a_rows = H;
+  w.a_cols = pl.Rc;
+  w.b = at<uint8_t>(sv, pl.hc);
+  w.sb = at<uint8_t>(sv, pl.shc);
+  w.b_rows = I;
+  w.b_cols = pl.Rc;
+  w.poff = poff;
+  w.E = E;
+  w.M = H;
+  w.N = I;
+  w.d = A->dw_down;
+  w.ldd = I;
+  w.status = st;
+  w.tiles_upper = pl.E * (H / 128) * (I / gemm_pick_bn(EPI_BF16, I));
+  MXG_TRY(launch_gemm(w, s));
+  }
+
+  // B4: dX_perm = dGU W_gate_up (MX along 2I)
+  if (run(MXG_BWD_DGRAD_GATE_UP)) {
+  GemmArgs x{};
+  x.epi = EPI_BF16;
+  x.a = at<uint8_t>(ws, pl.dguq);
+  x.sa = at<uint8_t>(ws, pl.sdguq);
+  x.a_rows = pl.Rc;
+  x.a_cols = 2 * I;
+  x.b = at<uint8_t>(sv, pl.wguT);
+  x.sb = at<uint8_t>(sv, pl.swguT);
+  x.b_rows = pl.E * H;
+  x.b_cols = 2 * I;
+  x.poff = poff;
+  x.E = E;
+  x.M = static_cast<int32_t>(pl.Rc);
+  x.N = H;
+  x.K = 2 * I;
+  x.b_rows_per_expert = H;
+  x.d = at<uint16_t>(ws, pl.dxperm);
+  x.ldd = H;
+  x.status = st;
+  x.tiles_upper = (pl.Rc / 128) * (H / gemm_pick_bn(EPI_BF16, H));
+  MXG_TRY(launch_gemm(x, s));
+  }
+
+  // B5: dW_gate_up[e] = dGUc^T Xc over the tokens of e
+  if (run(MXG_BWD_WGRAD_GATE_UP)) {
+  GemmArgs v{};
+  v.epi = EPI_BF16;
+  v.kgroup = true;
+  v.a = at<uint8_t>(ws, pl.dguc);
+  v.sa = at<uint8_t>(ws, pl.sdguc);
+  v.a_rows = 2 * I;
+  v.a_cols = pl.Rc;
+  v.b = at<uint8_t>(sv, pl.xc);
+  v.sb = at<uint8_t>(sv, pl.sxc);
+  v.b_rows = H;
+  v.b_cols = pl.Rc;
+  v.poff = poff;
+  v.E = E;
+  v.M = 2 * I;
+  v.N = H;
+  v.d = A->dw_gate_up;
+  v.ldd = H;
+  v.status = st;
+  v.tiles_upper = pl.E * (2 * I / 128) * (H / gemm_pick_bn(EPI_BF16, H));
+  MXG_TRY(launch_gemm(v, s));
+  }
+
+  // B6, B7: combine dx, reduce d(prob)
+  const int32_t* prow_of_src = at<int32_t>(sv, pl.prow_of_src);
+  if (run(MXG_BWD_COMBINE_DX))
+    MXG_TRY(launch_combine(at<uint16_t>(ws, pl.dxperm), prow_of_src, T, k, H, A->dx, s));
+  if (run(MXG_BWD_DPROBS))
+    MXG_TRY(launch_dprob(at<float>(ws, pl.dp), static_cast<int>(pl.dp_ld), prow_of_src, static_cast<int>(pl.R),
+                         A->dprobs, s));
+  return MXG_OK;
+}
+
+int mxg_grouped_mlp_bwd(const mxg_mlp_bwd_args* A, void* stream) { return bwd_impl(A, -1, stream); }
+
+int mxg_grouped_mlp_bwd_stage(const mxg_mlp_bwd_args* A, int stage, void* stream) {
+  if (stage < 0 || stage >= MXG_BWD_NUM_STAGES) return MXG_ERR_ARG;
+  return bwd_impl(A, stage, stream);
+}
+
+}  // extern "C"

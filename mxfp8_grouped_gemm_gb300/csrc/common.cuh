@@ -1,0 +1,80 @@
+// Shared device helpers: status reporting, bf16 packing, MXFP8 encoding and
+// the tensor-core scale-factor layout.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/mxg.h"
+
+namespace mxg {
+
+// A kernel wait that has not completed after this long gives up and reports
+// MXG_ERR_TIMEOUT (all legitimate waits are microseconds).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// ------------------------------------------------------------- bf16 helpers
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Two fp32 -> packed bf16x2 (round to nearest even); lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------ MXFP8 encode
+// Scale byte from the bit pattern of a block's max magnitude (a finite fp32
+// >= 0): shared exponent floor(log2 amax) - 8, clamped at -127, plus bias 127.
+// For a normal amax with exponent field Ef that is Ef - 8; below 2^-119 (and
+// for zero) it clamps to byte 0.
+__device__ __forceinline__ uint32_t mx_scale_byte(uint32_t amax_bits) {
+  const int ef = static_cast<int>(amax_bits >> 23);
+  return static_cast<uint32_t>(ef > 8 ? ef - 8 : 0);
+}
+
+// 2^(127 - byte) as fp32: the factor that brings the block into E4M3 range.
+__device__ __forceinline__ float mx_inv_scale(uint32_t byte) {
+  return __uint_as_float((254u - byte) << 23);
+}
+
+// Two fp32 -> two E4M3 codes (round to nearest even, saturate to +-448);
+// a in the low byte, b in the high byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// 32 values already multiplied by the inverse scale -> 32 codes in 8 words.
+__device__ __forceinline__ void encode32(const float (&v)[32], uint32_t (&w)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = cvt_e4m3x2(v[4 * i + 0], v[4 * i + 1]);
+    const uint32_t hi = cvt_e4m3x2(v[4 * i + 2], v[4 * i + 3]);
+    w[i] = lo | (hi << 16);
+  }
+}
+
+// ------------------------------------------------------- scale-factor layout
+// Byte offset of the scale of (row r, 32-block b) for a matrix with `rows`
+// rows (multiple of 128): 512-byte atoms of 128 rows x 4 blocks, K-chunk-major.
+// Inside an atom, 32 "lines" of 16 bytes: line (r%32) holds the 4 blocks of
+// rows r%32, 32+r%32, 64+r%32, 96+r%32 — what the tensor core's 32x128b
+// shared->TMEM copy expects.
+__host__ __device__ __forceinline__ int64_t sf_mma_offset(int64_t r, int64_t b, int64_t rows) {
+  return ((b >> 2) * (rows >> 7) + (r >> 7)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3);
+}
+
+__host__ __device__ __forceinline__ int64_t sf_offset(int layout, int64_t r, int64_t b, int64_t rows,
+                                                       int64_t nblocks) {
+  return layout == MXG_LAYOUT_MMA ? sf_mma_offset(r, b, rows) : r * nblocks + b;
+}
+
+}  // namespace mxg

@@ -1,0 +1,544 @@
+// Persistent grouped MXFP8 GEMM for sm_103a: TMA-fed, tcgen05 block-scaled
+// MMA (kind::mxf8f6f4, E4M3 x E4M3, E8M0 scale per 32 along K), fp32
+// accumulators in TMEM, warp-specialised.
+//
+// Grouping (BioNeMo Uses Grouped Kernels and MXFP8, "Grouping fragmented
+// expert workloads"): every expert keeps its own weight matrix; one launch
+// covers all experts.  Two shapes:
+//   row-grouped   : rows [poff[e], poff[e+1]) of A use expert e's B
+//                   (forward GEMMs and activation gradients);
+//   token-grouped : the contraction runs over tokens [poff[e], poff[e+1]),
+//                   one output matrix per expert (weight gradients).
+// The tile scheduler reads the 128-aligned group offsets on the device; the
+// host never sees the split sizes.
+//
+// Epilogues (TMEM -> registers, one thread per output row):
+//   EPI_BF16    : store fp32 accumulators as bf16.
+//   EPI_SWIGLU  : gate-up tile = 128 gate + 128 up columns; h = p*SiLU(g)*u
+//                 (ScaledSwiGLU, "Fusing precision conversion and expert
+//                 computation"), re-quantised to MXFP8 row-wise (the down
+//                 GEMM's A) and token-column-wise (the down wgrad's B); the
+//                 pre-activation g|u is kept in bf16 for the backward.
+//   EPI_DSWIGLU : dH tile -> dg = dH p u s (1 + g (1-s)), du = dH p g s
+//                 (s = sigmoid(g)), d(prob) partial sum_i dH g s u; dGU
+//                 quantised row-wise (dgrad A) and token-column-wise (wgrad A).
+//
+// CTA = 6 warps: warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs,
+// warps 2-5 run the epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+// Tile 128 x BN x 128 (BN = 256 or 128); 4/6-stage smem ring; the
+// accumulator is double-buffered in TMEM when it fits next to the scale
+// factors (BN = 128).  Every wait is bounded; a wait that gives up records
+// MXG_ERR_TIMEOUT, stops the CTA's pipeline and still frees TMEM.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mxg {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;
+constexpr int kThreads = 192;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kAcc = BN == 256 ? 1 : 2;
+  static constexpr int kABytes = BM * BK;
+  static constexpr int kBBytes = BN * BK;
+  static constexpr int kSfaBytes = BM * 4;  // 128 rows x 4 blocks of 32
+  static constexpr int kSfbBytes = BN * 4;
+  static constexpr uint32_t kTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kStageBytes = (kTx + 1023) / 1024 * 1024;
+  static constexpr uint32_t kSfaCol = kAcc * BN;      // TMEM columns of the scale factors
+  static constexpr uint32_t kSfbCol = kSfaCol + 4;
+  static constexpr int kCtrlBytes = 2048;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kCtrlBytes;
+  static_assert(kSfbCol + BN / 32 <= 512, "TMEM budget");
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+struct TileCoord {
+  int e;      // expert
+  int m0;     // first row of the tile (padded row, or row of D_e)
+  int nt;     // column-tile index
+  int kbeg;   // first contraction index
+  int num_k;  // number of 128-wide contraction steps
+};
+
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+__device__ __forceinline__ void store_bf16_32(uint16_t* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+}
+
+__device__ __forceinline__ void load_bf16_32(const uint16_t* src, float (&v)[32]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 q = s[i];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = u2f(w[j] << 16);
+      v[8 * i + 2 * j + 1] = u2f(w[j] & 0xffff0000u);
+    }
+  }
+}
+
+// Row-wise MX of one thread's 32 consecutive values: codes to dst (32 bytes),
+// scale byte returned.
+__device__ __forceinline__ uint32_t row_quant32(const float (&h)[32], uint8_t* dst) {
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = max(amax, f2u(h[i]) & 0x7fffffffu);
+  const uint32_t sb = mx_scale_byte(amax);
+  const float inv = mx_inv_scale(sb);
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = h[i] * inv;
+  uint32_t w[8];
+  encode32(v, w);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return sb;
+}
+
+// Column-wise MX across the warp: lane l holds row tok0+l; for each of the 32
+// columns col0+i the warp's 32 rows form one block (tok0 is 32-aligned and
+// inside one expert group).  Codes go to qc[(col0+i)*ld + tok0 + lane].
+__device__ __forceinline__ void col_quant32(const float (&h)[32], uint8_t* qc, uint8_t* sc, int64_t ld,
+                                            int64_t sc_rows, int64_t col0, int64_t tok0, int lane) {
+  uint32_t my_sb = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, f2u(h[i]) & 0x7fffffffu);
+    const uint32_t sb = mx_scale_byte(m);
+    qc[(col0 + i) * ld + tok0 + lane] = static_cast<uint8_t>(cvt_e4m3x2(h[i] * mx_inv_scale(sb), 0.f) & 0xffu);
+    if (lane == i) my_sb = sb;
+  }
+  sc[sf_mma_offset(col0 + lane, tok0 >> 5, sc_rows)] = static_cast<uint8_t>(my_sb);
+}
+
+template <int BN, bool KG>
+__device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int row) {
+  uint16_t* drow = KG ? P.d + static_cast<int64_t>(tc.e) * P.M * P.N + static_cast<int64_t>(tc.m0 + row) * P.N +
+                            tc.nt * BN
+                      : P.d + static_cast<int64_t>(tc.m0 + row) * P.ldd + tc.nt * BN;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; c += 2) {
+    uint32_t r0[32], r1[32];
+    tmem_ld_32x32b_x32(tb + c * 32, r0);
+    tmem_ld_32x32b_x32(tb + (c + 1) * 32, r1);
+    tmem_ld_wait();
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = u2f(r0[i]);
+    store_bf16_32(drow + c * 32, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = u2f(r1[i]);
+    store_bf16_32(drow + (c + 1) * 32, v);
+  }
+}
+
+// Gate-up tile: accumulator columns [0,128) = gate j0.., [128,256) = up j0..
+__device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane) {
+  const int64_t tok0 = tc.m0 + q * 32;
+  const int64_t r = tok0 + lane;
+  const float p = P.probs_perm[r];
+  const int64_t I = P.I;
+  const int j0 = tc.nt * 128;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t g[32], u[32];
+    tmem_ld_32x32b_x32(tb + c * 32, g);
+    tmem_ld_32x32b_x32(tb + 128 + c * 32, u);
+    tmem_ld_wait();
+    const int64_t col = j0 + c * 32;
+    float h[32];
+    if (P.gu_save != nullptr) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) h[i] = u2f(g[i]);
+      store_bf16_32(P.gu_save + r * (2 * I) + col, h);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) h[i] = u2f(u[i]);
+      store_bf16_32(P.gu_save + r * (2 * I) + I + col, h);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float gf = u2f(g[i]);
+      h[i] = p * (gf / (1.f + __expf(-gf))) * u2f(u[i]);
+    }
+    const uint32_t sb = row_quant32(h, P.q_out + r * P.q_out_ld + col);
+    P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
+    if (P.qc_out != nullptr) col_quant32(h, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
+  }
+}
+
+// dgrad-down tile: accumulator = dH columns j0.., j0 + BN.
+template <int BN>
+__device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q,
+                                            int lane) {
+  const int64_t tok0 = tc.m0 + q * 32;
+  const int64_t r = tok0 + lane;
+  const float p = P.probs_perm[r];
+  const int64_t I = P.I;
+  const int j0 = tc.nt * BN;
+  float dp = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t dh[32];
+    tmem_ld_32x32b_x32(tb + c * 32, dh);
+    const int64_t col = j0 + c * 32;
+    float g[32], u[32], dg[32];
+    load_bf16_32(P.gu_save + r * (2 * I) + col, g);
+    load_bf16_32(P.gu_save + r * (2 * I) + I + col, u);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float gf = g[i], uf = u[i];
+      const float s = 1.f / (1.f + __expf(-gf));
+      const float sl = gf * s;
+      const float a = u2f(dh[i]) * p;
+      dg[i] = a * uf * s * (1.f + gf * (1.f - s));
+      u[i] = a * sl;                       // du
+      dp += u2f(dh[i]) * sl * uf;
+    }
+    uint32_t sb = row_quant32(dg, P.q_out + r * P.q_out_ld + col);
+    P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
+    col_quant32(dg, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
+    sb = row_quant32(u, P.q_out + r * P.q_out_ld + I + col);
+    P.s_out[sf_mma_offset(r, (I + col) >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
+    col_quant32(u, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
+  }
+  P.dp_part[r * P.dp_ld + tc.nt] = dp;
+}
+
+template <int BN, int EPI, bool KG>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs P) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ctrl = smem + C::kStages * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + C::kAcc;
+  uint64_t* drained = tempty + C::kAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drained + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* never_set = reinterpret_cast<int*>(tmem_slot + 2);
+  int* s_poff = reinterpret_cast<int*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = P.E;
+  for (int i = threadIdx.x; i <= E; i += kThreads) s_poff[i] = P.poff[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < C::kAcc; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drained, 1);
+    *abort_flag = 0;
+    *never_set = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  __syncthreads();
+
+  // Group offsets must be 128-aligned, monotone and inside the capacity.
+  bool ok = true;
+  const int64_t cap = KG ? P.a_cols : P.M;
+  for (int e = 0; e < E; ++e) {
+    const int a = s_poff[e], b = s_poff[e + 1];
+    if (a < 0 || (a & 127) || b < a) ok = false;
+  }
+  if ((s_poff[E] & 127) || s_poff[E] > cap) ok = false;
+  if (!ok) {
+    if (threadIdx.x == 0) report(P.status, MXG_ERR_OFFSETS);
+    return;
+  }
+
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int ntn = (KG || EPI != EPI_SWIGLU) ? P.N / BN : P.I / 128;
+  const int mtn_kg = P.M / BM;
+  const int64_t total = KG ? static_cast<int64_t>(E) * mtn_kg * ntn : static_cast<int64_t>(s_poff[E] >> 7) * ntn;
+
+  auto decode = [&](int64_t t) {
+    TileCoord tc;
+    if (KG) {
+      const int64_t tpe = static_cast<int64_t>(mtn_kg) * ntn;
+      tc.e = static_cast<int>(t / tpe);
+      const int local = static_cast<int>(t - tc.e * tpe);
+      tc.nt = local / mtn_kg;
+      tc.m0 = (local - tc.nt * mtn_kg) * BM;
+      tc.kbeg = s_poff[tc.e];
+      tc.num_k = (s_poff[tc.e + 1] - s_poff[tc.e]) / BK;
+    } else {
+      int e = 0;
+      while (e + 1 < E && static_cast<int64_t>(s_poff[e + 1] >> 7) * ntn <= t) ++e;
+      const int local = static_cast<int>(t - static_cast<int64_t>(s_poff[e] >> 7) * ntn);
+      const int mcount = (s_poff[e + 1] - s_poff[e]) >> 7;
+      tc.e = e;
+      tc.nt = local / mcount;
+      tc.m0 = s_poff[e] + (local - tc.nt * mcount) * BM;
+      tc.kbeg = 0;
+      tc.num_k = P.K / BK;
+    }
+    return tc;
+  };
+  auto fail = [&]() {
+    report(P.status, MXG_ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool aborted = false;
+      for (int64_t t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
+        const TileCoord tc = decode(t);
+        const int a_row = tc.m0;
+        int b_row0, b_row1 = 0;
+        if (KG) {
+          b_row0 = tc.nt * BN;
+        } else if (EPI == EPI_SWIGLU) {
+          b_row0 = tc.e * P.b_rows_per_expert + tc.nt * 128;
+          b_row1 = b_row0 + P.I;
+        } else {
+          b_row0 = tc.e * P.b_rows_per_expert + tc.nt * BN;
+        }
+        for (int kb = 0; kb < tc.num_k; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, kWaitLimitNs)) {
+            fail();
+            aborted = true;
+            break;
+          }
+          uint8_t* sA = smem + stage * C::kStageBytes;
+          uint8_t* sB = sA + C::kABytes;
+          uint8_t* sSfa = sB + C::kBBytes;
+          uint8_t* sSfb = sSfa + C::kSfaBytes;
+          const int kx = tc.kbeg + kb * BK;
+          const int64_t kc = kx >> 7;
+          mbar_arrive_expect_tx(&full[stage], C::kTx);
+          tma_load_2d(sA, &tmA, kx, a_row, &full[stage]);
+          bulk_load(sSfa, P.sa + (kc * (P.a_rows >> 7) + (a_row >> 7)) * 512, 512, &full[stage]);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
+            tma_load_2d(sB + 128 * BK, &tmB, kx, b_row1, &full[stage]);
+            bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (b_row0 >> 7)) * 512, 512, &full[stage]);
+            bulk_load(sSfb + 512, P.sb + (kc * (P.b_rows >> 7) + (b_row1 >> 7)) * 512, 512, &full[stage]);
+          } else {
+            tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
+            bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (b_row0 >> 7)) * 512, BN * 4, &full[stage]);
+          }
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (aborted) {  // let copies already in flight land before the CTA exits
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      const uint32_t sfa_t = tmem + C::kSfaCol;
+      const uint32_t sfb_t = tmem + C::kSfbCol;
+      bool aborted = false;
+      for (int64_t t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
+        const TileCoord tc = decode(t);
+        if (tc.num_k == 0) continue;
+        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, kWaitLimitNs)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_t = tmem + acc * BN;
+        for (int kb = 0; kb < tc.num_k; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+            fail();
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          uint8_t* sA = smem + stage * C::kStageBytes;
+          uint8_t* sB = sA + C::kABytes;
+          uint8_t* sSfa = sB + C::kBBytes;
+          uint8_t* sSfb = sSfa + C::kSfaBytes;
+          tmem_cp_32x128b_warpx4(sfa_t, smem_desc(smem_u32(sSfa), 0, 128, kLayoutNone));
+#pragma unroll
+          for (int i = 0; i < BN / 128; ++i)
+            tmem_cp_32x128b_warpx4(sfb_t + 4 * i, smem_desc(smem_u32(sSfb + 512 * i), 0, 128, kLayoutNone));
+          const uint64_t adesc = smem_desc(smem_u32(sA), 0, 1024, kLayoutSwizzle128B);
+          const uint64_t bdesc = smem_desc(smem_u32(sB), 0, 1024, kLayoutSwizzle128B);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            mma_mxf8(d_t, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8_e4m3(BM, BN, k, k), sfa_t, sfb_t,
+                     (kb | k) != 0 ? 1u : 0u);
+          mma_commit(&empty[stage]);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (aborted) break;
+        mma_commit(&tfull[acc]);
+        if (++acc == C::kAcc) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // all MMAs issued by this thread are complete before TMEM is released
+      mma_commit(drained);
+      mbar_wait_bounded(drained, 0, never_set, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+      const TileCoord tc = decode(t);
+      if (tc.num_k == 0) {
+        // token-grouped tile of an expert without tokens: exact zeros
+        uint16_t* drow = P.d + static_cast<int64_t>(tc.e) * P.M * P.N + static_cast<int64_t>(tc.m0 + row) * P.N +
+                         tc.nt * BN;
+#pragma unroll 4
+        for (int c = 0; c < BN / 8; ++c) reinterpret_cast<uint4*>(drow)[c] = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
+      bool got = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, kWaitLimitNs);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (EPI == EPI_SWIGLU) {
+        epi_swiglu(P, tc, tb, q, lane);
+      } else if (EPI == EPI_DSWIGLU) {
+        epi_dswiglu<BN>(P, tc, tb, q, lane);
+      } else {
+        epi_bf16<BN, KG>(P, tc, tb, row);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == C::kAcc) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------- host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D uint8 tensor map over [rows][cols] with a 128-byte-wide swizzled box.
+bool encode_u8(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, uint32_t box_cols,
+               uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <int BN, int EPI, bool KG>
+cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  if (!encode_u8(&ta, g.a, g.a_cols, g.a_rows, BK, BM)) return cudaErrorInvalidValue;
+  if (!encode_u8(&tb, g.b, g.b_cols, g.b_rows, BK, EPI == EPI_SWIGLU ? 128 : BN)) return cudaErrorInvalidValue;
+  auto kern = gemm_kernel<BN, EPI, KG>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::kSmem);
+  if (err != cudaSuccess) return err;
+  int64_t grid = num_sms();
+  if (g.tiles_upper < grid) grid = g.tiles_upper;
+  if (grid < 1) grid = 1;
+  kern<<<static_cast<unsigned>(grid), kThreads, Cfg<BN>::kSmem, s>>>(ta, tb, g);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_pick_bn(int epi, int N) {
+  if (epi == EPI_SWIGLU) return 256;
+  return N % 256 == 0 ? 256 : 128;
+}
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
+  const int bn = gemm_pick_bn(g.epi, g.epi == EPI_DSWIGLU ? g.I : g.N);
+  if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false>(g, s);
+  if (g.epi == EPI_DSWIGLU)
+    return bn == 256 ? launch_impl<256, EPI_DSWIGLU, false>(g, s) : launch_impl<128, EPI_DSWIGLU, false>(g, s);
+  if (g.kgroup) return bn == 256 ? launch_impl<256, EPI_BF16, true>(g, s) : launch_impl<128, EPI_BF16, true>(g, s);
+  return bn == 256 ? launch_impl<256, EPI_BF16, false>(g, s) : launch_impl<128, EPI_BF16, false>(g, s);
+}
+
+}  // namespace mxg

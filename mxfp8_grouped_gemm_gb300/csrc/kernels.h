@@ -1,0 +1,102 @@
+// Internal launchers shared by the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace mxg {
+
+void count_launch();
+
+// ---------------------------------------------------------------- quantiser
+struct QuantParams {
+  const uint16_t* x;          // bf16 source
+  int64_t ld_x;               // source row stride (elements)
+  int64_t x_batch_stride;     // elements between batches (blockIdx.z)
+  const int32_t* src_rows;    // nullable: row p reads source row src_rows[p]/src_div; -1 = zero row
+  int32_t src_div;
+  const float* probs;         // nullable: probs_perm[p] = probs[src_rows[p]] (0 for padding)
+  float* probs_perm;
+  int32_t rows;               // rows per batch (multiple of 32)
+  int32_t cols;               // columns (multiple of 128)
+  int32_t batch;
+  const int32_t* rows_valid;  // nullable device scalar: row blocks at or past it are skipped
+  uint8_t* q_row;             // nullable: [batch*rows][cols]
+  uint8_t* s_row;
+  int64_t sf_row_rows;        // rows of the row-wise matrix (MMA layout)
+  uint8_t* q_col;             // nullable: [batch*cols][ld_col], rows of x become columns
+  uint8_t* s_col;
+  int64_t ld_col;
+  int64_t sf_col_rows;        // rows of the column-wise matrix (MMA layout)
+  int32_t layout;             // MXG_LAYOUT_*
+};
+cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
+
+// ------------------------------------------------------------ route/permute
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* probs, cudaStream_t s);
+
+struct PermuteParams {
+  const int32_t* ids;
+  int32_t R, E;
+  int32_t* counts;            // scratch [nblk][E]
+  int32_t* bases;             // scratch [nblk][E]
+  int32_t* offsets;           // [E+1]
+  int32_t* padded_offsets;    // [E+1]
+  int32_t* split_sizes;       // [E]
+  int32_t* src_of_row;        // nullable [R] (unpadded)
+  int32_t* row_of_src;        // nullable [R] (unpadded)
+  int32_t* prow_src;          // nullable [m_cap] padded row -> flat index (prefilled with -1)
+  int32_t* prow_of_src;       // nullable [R] flat index -> padded row
+  int32_t* status;
+};
+int permute_num_blocks(int R);
+cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
+
+// ------------------------------------------------------------------ combine
+cudaError_t launch_combine(const uint16_t* src, const int32_t* prow_of_src, int T, int k, int H, uint16_t* out,
+                           cudaStream_t s);
+cudaError_t launch_dprob(const float* part, int ld, const int32_t* prow_of_src, int R, float* dprobs,
+                         cudaStream_t s);
+
+// --------------------------------------------------------------------- GEMM
+enum Epi { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
+
+struct GemmArgs {
+  int epi;
+  bool kgroup;
+  const uint8_t* a;           // codes
+  const uint8_t* sa;
+  int64_t a_rows;             // rows of the A matrix (SF layout, tensor map)
+  int64_t a_cols;             // contraction extent stored in A (K, or token capacity)
+  const uint8_t* b;
+  const uint8_t* sb;
+  int64_t b_rows;
+  int64_t b_cols;
+  const int32_t* poff;
+  int32_t E;
+  int32_t M;                  // K-grouped: rows of each D_e; M-grouped: row capacity
+  int32_t N;                  // output columns (SwiGLU: 2I)
+  int32_t K;                  // M-grouped contraction length
+  int32_t b_rows_per_expert;  // M-grouped
+  int32_t I;                  // SwiGLU / dSwiGLU intermediate size
+  uint16_t* d;
+  int64_t ldd;
+  const float* probs_perm;
+  uint16_t* gu_save;
+  uint8_t* q_out;
+  uint8_t* s_out;
+  int64_t q_out_ld;
+  int64_t s_out_rows;
+  uint8_t* qc_out;
+  uint8_t* sc_out;
+  int64_t qc_ld;
+  int64_t sc_rows;
+  float* dp_part;
+  int32_t dp_ld;
+  int32_t* status;
+  int64_t tiles_upper;        // host bound on the number of tiles (grid sizing)
+};
+int gemm_pick_bn(int epi, int N);
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s);
+
+}  // namespace mxg

@@ -1,0 +1,201 @@
+// Top-k routing and the bit-exact permute (histogram -> scan -> stable scatter).
+//
+// Routing: BioNeMo Uses Grouped Kernels and MXFP8, Fig. 1 (a top-2 router sends
+// each token to two of eight experts; outputs combined as a weighted sum).
+// Permute: same page, "Grouping fragmented expert workloads" (split_sizes,
+// one count per expert).  Within an expert, rows keep the order of the flat
+// index t*k + j, so the result is deterministic and needs no atomics to
+// decide the order.
+#include <cfloat>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mxg {
+
+namespace {
+
+// ----------------------------------------------------------------- top-k ----
+// One warp per token; lane l holds logits l, l+32, ... (E <= 256).
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                   int32_t* __restrict__ ids, float* __restrict__ probs) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  const float* row = logits + static_cast<int64_t>(warp) * E;
+  float v[8];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int e = lane + 32 * q;
+    v[q] = e < E ? row[e] : -FLT_MAX;
+    if (e >= E) taken |= 1u << q;
+  }
+  float my_val = 0.f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -FLT_MAX;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (!(taken >> q & 1u) && (bi == 0x7fffffff || v[q] > bv)) {   // first max within the lane = lowest id
+        bv = v[q];
+        bi = lane + 32 * q;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_val = bv;
+      my_id = bi;
+    }
+  }
+  const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
+  const float w = lane < k ? expf(my_val - vmax) : 0.f;
+  float sum = w;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    ids[static_cast<int64_t>(warp) * k + lane] = my_id;
+    probs[static_cast<int64_t>(warp) * k + lane] = w / sum;
+  }
+}
+
+// --------------------------------------------------------------- permute ----
+constexpr int kChunk = 4096;     // flat entries per CTA
+constexpr int kThreads = 256;
+constexpr int kMaxE = 256;
+
+__global__ void __launch_bounds__(kThreads) count_kernel(const PermuteParams P) {
+  __shared__ int hist[kMaxE];
+  for (int e = threadIdx.x; e < P.E; e += kThreads) hist[e] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kChunk;
+  for (int i = threadIdx.x; i < kChunk; i += kThreads) {
+    const int f = base + i;
+    if (f >= P.R) break;
+    const int e = P.ids[f];
+    if (e < 0 || e >= P.E) report(P.status, MXG_ERR_EXPERT_ID);
+    else atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < P.E; e += kThreads) P.counts[blockIdx.x * P.E + e] = hist[e];
+}
+
+// One CTA: per-expert totals, exclusive scans (plain and 128-padded) and the
+// per-(chunk, expert) starting rows.
+__global__ void __launch_bounds__(kThreads) scan_kernel(const PermuteParams P, int nblk) {
+  __shared__ int tot[kMaxE];
+  __shared__ int off[kMaxE + 1];
+  __shared__ int poff[kMaxE + 1];
+  for (int e = threadIdx.x; e < P.E; e += kThreads) {
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+      P.bases[b * P.E + e] = run;
+      run += P.counts[b * P.E + e];
+    }
+    tot[e] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    off[0] = 0;
+    poff[0] = 0;
+    for (int e = 0; e < P.E; ++e) {
+      off[e + 1] = off[e] + tot[e];
+      poff[e + 1] = poff[e] + ((tot[e] + 127) & ~127);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= P.E; e += kThreads) {
+    P.offsets[e] = off[e];
+    P.padded_offsets[e] = poff[e];
+    if (e < P.E) P.split_sizes[e] = tot[e];
+  }
+  for (int e = threadIdx.x; e < P.E; e += kThreads)
+    for (int b = 0; b < nblk; ++b) P.bases[b * P.E + e] += off[e];
+}
+
+__global__ void __launch_bounds__(kThreads) scatter_kernel(const PermuteParams P) {
+  __shared__ int run[kMaxE];
+  __shared__ int off[kMaxE + 1];
+  __shared__ int poff[kMaxE + 1];
+  __shared__ int wcnt[kThreads / 32][kMaxE];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < P.E; e += kThreads) run[e] = P.bases[blockIdx.x * P.E + e];
+  for (int e = threadIdx.x; e <= P.E; e += kThreads) {
+    off[e] = P.offsets[e];
+    poff[e] = P.padded_offsets[e];
+  }
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int base = blockIdx.x * kChunk;
+  for (int it = 0; it < kChunk / kThreads; ++it) {
+    const int f = base + it * kThreads + threadIdx.x;
+    int e = -1;
+    if (f < P.R) {
+      e = P.ids[f];
+      if (e < 0 || e >= P.E) e = -1;
+    }
+    for (int i = threadIdx.x; i < (kThreads / 32) * P.E; i += kThreads) (&wcnt[0][0])[(i / P.E) * kMaxE + i % P.E] = 0;
+    __syncthreads();
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    if (e >= 0 && rank == 0) wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int pre = 0;
+      for (int w = 0; w < warp; ++w) pre += wcnt[w][e];
+      const int r = run[e] + pre + rank;
+      const int pr = poff[e] + (r - off[e]);
+      if (P.src_of_row) P.src_of_row[r] = f;
+      if (P.row_of_src) P.row_of_src[f] = r;
+      if (P.prow_src) P.prow_src[pr] = f;
+      if (P.prow_of_src) P.prow_of_src[f] = pr;
+    } else if (f < P.R) {
+      if (P.row_of_src) P.row_of_src[f] = -1;
+      if (P.prow_of_src) P.prow_of_src[f] = -1;
+    }
+    __syncthreads();
+    for (int ee = threadIdx.x; ee < P.E; ee += kThreads) {
+      int s = 0;
+      for (int w = 0; w < kThreads / 32; ++w) s += wcnt[w][ee];
+      run[ee] += s;
+    }
+    __syncthreads();
+    if (base + (it + 1) * kThreads >= P.R) break;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* probs, cudaStream_t s) {
+  const int warps_per_block = 8;
+  const int grid = (T + warps_per_block - 1) / warps_per_block;
+  if (grid == 0) return cudaSuccess;
+  topk_kernel<<<grid, warps_per_block * 32, 0, s>>>(logits, T, E, k, ids, probs);
+  count_launch();
+  return cudaGetLastError();
+}
+
+int permute_num_blocks(int R) { return (R + kChunk - 1) / kChunk; }
+
+cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s) {
+  const int nblk = permute_num_blocks(p.R);
+  if (nblk == 0) return cudaSuccess;
+  count_kernel<<<nblk, kThreads, 0, s>>>(p);
+  count_launch();
+  scan_kernel<<<1, kThreads, 0, s>>>(p, nblk);
+  count_launch();
+  scatter_kernel<<<nblk, kThreads, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace mxg

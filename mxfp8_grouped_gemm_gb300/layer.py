@@ -1,0 +1,67 @@
+"""GroupedMLP: owns the caller-side buffers (saved activations, scratch,
+device status word) of one grouped expert MLP shape and runs the library's
+route -> forward -> backward calls on the current stream."""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+
+class GroupedMLP:
+    def __init__(self, T: int, H: int, I: int, E: int, k: int, device="cuda"):
+        self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        self.device = torch.device(device)
+        saved = _lib.mxg_mlp_saved_bytes(T, H, I, E, k)
+        ws = _lib.mxg_mlp_workspace_bytes(T, H, I, E, k)
+        if saved == 0 or ws == 0:
+            raise ValueError(f"unsupported shape T={T} H={H} I={I} E={E} k={k} (H, I multiples of 128; k <= E <= 256)")
+        self.saved = torch.empty(saved, dtype=torch.uint8, device=self.device)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.ids = torch.empty((T, k), dtype=torch.int32, device=self.device)
+        self.probs = torch.empty((T, k), dtype=torch.float32, device=self.device)
+        self.y = torch.empty((T, H), dtype=torch.bfloat16, device=self.device)
+        self.split_sizes = torch.empty(E, dtype=torch.int32, device=self.device)
+        self.dx = torch.empty((T, H), dtype=torch.bfloat16, device=self.device)
+        self.dw_gate_up = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=self.device)
+        self.dw_down = torch.empty((E, H, I), dtype=torch.bfloat16, device=self.device)
+        self.dprobs = torch.empty((T, k), dtype=torch.float32, device=self.device)
+
+    def route(self, logits, stream=None):
+        return _lib.mxg_route_topk(logits, self.k, self.ids, self.probs, stream=stream)
+
+    def forward(self, x, ids, probs, w_gate_up, w_down, save_for_backward=True, stream=None, stage=None):
+        return _lib.mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, self.saved, self.workspace,
+                                        self.dev_status, y=self.y, split_sizes=self.split_sizes,
+                                        save_for_backward=save_for_backward, stream=stream, stage=stage)
+
+    def backward(self, dy, stream=None, stage=None):
+        return _lib.mxg_grouped_mlp_bwd(dy, self.saved, self.workspace, self.dev_status, self.E, self.I, self.k,
+                                        dx=self.dx, dw_gate_up=self.dw_gate_up, dw_down=self.dw_down,
+                                        dprobs=self.dprobs, stream=stream, stage=stage)
+
+    def step(self, logits, x, w_gate_up, w_down, dy, stream=None):
+        """One pass of the whole path: route, forward (saving for backward), backward."""
+        ids, probs = self.route(logits, stream=stream)
+        self.forward(x, ids, probs, w_gate_up, w_down, True, stream=stream)
+        return self.backward(dy, stream=stream)
+
+    def status(self) -> int:
+        return int(self.dev_status.item())
+
+    def gu_view(self) -> torch.Tensor:
+        """The gate-up GEMM output (bf16 [m_cap, 2I]) kept in the saved buffer."""
+        base = self.saved.data_ptr()
+        off = _lib.mxg_mlp_saved_view(self.saved, self.T, self.H, self.I, self.E, self.k, 0) - base
+        m_cap = self.padded_rows_capacity()
+        return self.saved[off:off + m_cap * 2 * self.I * 2].view(torch.bfloat16).view(m_cap, 2 * self.I)
+
+    def padded_offsets(self) -> torch.Tensor:
+        base = self.saved.data_ptr()
+        off = _lib.mxg_mlp_saved_view(self.saved, self.T, self.H, self.I, self.E, self.k, 1) - base
+        return self.saved[off:off + 4 * (self.E + 1)].view(torch.int32)
+
+    def padded_rows_capacity(self) -> int:
+        R = self.T * self.k
+        return (R + 127) // 128 * 128 + 128 * self.E

@@ -12,8 +12,11 @@ involved: seeded normal draws with the shapes below stand in for activations,
 master weights, router logits and upstream gradients.
 
 Generation recipe (per named workload with index c):
-  numpy Generator(PCG64(SeedSequence(1000 + c))), spawned into six child
-  streams used in this fixed order: logits, x, W_gate_up, W_down, dy, zipf.
+  SeedSequence(1000 + c) spawned into six children used in this fixed order:
+  logits, x, W_gate_up, W_down, dy, zipf; each drives a numpy
+  Generator(PCG64).  The two weight children are spawned once more into one
+  stream per expert (drawn in parallel threads, each expert from its own
+  stream, so the result does not depend on the thread count).
   fp32 normal draws are rounded to bf16 (round-to-nearest-even, via torch).
   logits ~ N(0,1) fp32; x ~ N(0,1); W ~ N(0, 0.02); dy ~ N(0,1).
 
@@ -28,7 +31,9 @@ multiple of 128 the seed is advanced by one (recorded in ``seed_used``).
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
+import os
 
 import numpy as np
 import torch
@@ -90,6 +95,23 @@ def _normal_bf16(rng: np.random.Generator, shape, std: float, chunk_rows: int | 
     return out
 
 
+def _expert_weights(ss: np.random.SeedSequence, E: int, shape, std: float) -> torch.Tensor:
+    """[E, *shape] bf16, expert e drawn from the e-th child of ``ss``."""
+    out = torch.empty((E,) + tuple(shape), dtype=torch.bfloat16)
+    children = ss.spawn(E)
+
+    def one(e):
+        g = np.random.Generator(np.random.PCG64(children[e]))
+        a = g.standard_normal(tuple(shape), dtype=np.float32)
+        a *= np.float32(std)
+        out[e] = to_bf16(a)
+
+    workers = max(1, min(E, os.cpu_count() or 1, 16))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(one, range(E)))
+    return out
+
+
 def _skew_logits(rng_logits, rng_zipf, T, E, k):
     assert k == 2 and E >= 3
     empty = rng_zipf.choice(E, size=2, replace=False)
@@ -131,7 +153,9 @@ def make_inputs(wl: Workload | str, seed_offset: int = 0, with_weights: bool = T
     off = seed_offset
     while True:
         ss = np.random.SeedSequence(1000 + wl.index + off)
-        r_logits, r_x, r_wgu, r_wd, r_dy, r_zipf = [np.random.Generator(np.random.PCG64(s)) for s in ss.spawn(6)]
+        kids = ss.spawn(6)
+        r_logits, r_x, _, _, r_dy, r_zipf = [np.random.Generator(np.random.PCG64(s)) for s in kids]
+        ss_wgu, ss_wd = kids[2], kids[3]
         out: dict = {"seed_used": 1000 + wl.index + off}
         if wl.skew:
             logits, counts, empty = _skew_logits(r_logits, r_zipf, wl.T, wl.E, wl.k)
@@ -146,8 +170,8 @@ def make_inputs(wl: Workload | str, seed_offset: int = 0, with_weights: bool = T
     out["logits"] = torch.from_numpy(logits)
     out["x"] = _normal_bf16(r_x, (wl.T, wl.H), 1.0, chunk_rows=4096)
     if with_weights:
-        out["w_gate_up"] = _normal_bf16(r_wgu, (wl.E, 2 * wl.I, wl.H), WEIGHT_STD, chunk_rows=1)
-        out["w_down"] = _normal_bf16(r_wd, (wl.E, wl.H, wl.I), WEIGHT_STD, chunk_rows=1)
+        out["w_gate_up"] = _expert_weights(ss_wgu, wl.E, (2 * wl.I, wl.H), WEIGHT_STD)
+        out["w_down"] = _expert_weights(ss_wd, wl.E, (wl.H, wl.I), WEIGHT_STD)
     if wl.backward:
         out["dy"] = _normal_bf16(r_dy, (wl.T, wl.H), 1.0, chunk_rows=4096)
     return out

@@ -1,0 +1,45 @@
+"""Routing and permute parity: ids and every permutation index bit-exact
+against the oracle, probabilities to fp32 rounding; invalid ids reported."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import np_, require_gpu
+from oracle import moe
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("T,E,k", [(256, 4, 2), (4096, 8, 2), (8192, 64, 8), (1000, 256, 32), (77, 5, 1)])
+def test_topk_and_permute_bit_exact(T, E, k):
+    m = require_gpu()
+    rng = np.random.default_rng(T + E + k)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[: T // 10, 1] = logits[: T // 10, 0]          # planted exact ties
+    logits[T // 10: T // 5] = 0.5                         # whole rows tied
+    lg = torch.from_numpy(logits).cuda()
+    ids, probs = m.mxg_route_topk(lg, k)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    perm = m.mxg_route_permute(ids, E, st)
+    torch.cuda.synchronize()
+    ref_ids, ref_probs = moe.route_topk(logits, k)
+    assert np.array_equal(np_(ids), ref_ids)
+    np.testing.assert_allclose(np_(probs), ref_probs, rtol=2e-6, atol=1e-7)
+    ref = moe.permute(ref_ids, E)
+    assert int(st.item()) == 0
+    assert np.array_equal(np_(perm["split_sizes"]), ref["split_sizes"])
+    assert np.array_equal(np_(perm["padded_offsets"]), ref["padded_offsets"])
+    assert np.array_equal(np_(perm["src_of_row"]), ref["src_of_row"])
+    assert np.array_equal(np_(perm["row_of_src"]), ref["row_of_src"])
+
+
+def test_permute_reports_bad_expert_id():
+    m = require_gpu()
+    ids = torch.tensor([[0, 1], [2, 7], [1, 3], [9, 0]], dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    perm = m.mxg_route_permute(ids, 4, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 16                           # MXG_ERR_EXPERT_ID
+    row_of_src = np_(perm["row_of_src"])
+    assert row_of_src[3] == -1 and row_of_src[6] == -1    # dropped entries
+    assert int(np_(perm["split_sizes"]).sum()) == 6
