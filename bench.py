@@ -43,7 +43,8 @@ FALLBACK_HBM = 6800.0                # GB/s
 # CPU sample of the workload for the oracle: the first T_S tokens, all experts,
 # full hidden size, the intermediate dimension cut to its first I_S columns.
 CPU_SAMPLE_TOKENS = 512
-CPU_SAMPLE_I = 256
+CPU_SAMPLE_I = 1024          # the reported cpu_baseline (~10-30 s of host work)
+CPU_SAMPLE_I_REF = 256       # per step of the reference arm (K + W steps within a few minutes)
 
 
 def parse():
@@ -112,9 +113,9 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- CPU oracle --
-def cpu_sample_inputs(inp, wl):
+def cpu_sample_inputs(inp, wl, i_cut=CPU_SAMPLE_I):
     import torch
-    T_s, I_s, I = min(CPU_SAMPLE_TOKENS, wl.T), min(CPU_SAMPLE_I, wl.I), wl.I
+    T_s, I_s, I = min(CPU_SAMPLE_TOKENS, wl.T), min(i_cut, wl.I), wl.I
     wgu = torch.cat([inp["w_gate_up"][:, :I_s], inp["w_gate_up"][:, I:I + I_s]], 1)
     return {"logits": inp["logits"][:T_s].numpy(), "x": inp["x"][:T_s].double().numpy(),
             "w_gate_up": wgu.double().numpy(), "w_down": inp["w_down"][:, :, :I_s].double().numpy(),
@@ -317,7 +318,7 @@ def run_reference(args):
     inp = synthetic.make_inputs(wl)
     if "dy" not in inp:
         inp["dy"] = synthetic.random_bf16((wl.T, wl.H), 77)
-    s = cpu_sample_inputs(inp, wl)
+    s = cpu_sample_inputs(inp, wl, CPU_SAMPLE_I_REF)
     flops = 18.0 * s["T"] * wl.k * wl.H * s["I"]
     for _ in range(args.warmup):
         cpu_sample_run(s, wl.k)

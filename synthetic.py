@@ -69,6 +69,9 @@ WORKLOADS = {
     "mixtral": Workload("mixtral", 3, T=16384, H=4096, I=14336, E=8, k=2),
     "skew": Workload("skew", 4, T=16384, H=4096, I=14336, E=8, k=2, skew=True),
     "fine": Workload("fine", 5, T=8192, H=2048, I=1024, E=64, k=8),
+    # one expert of the Mixtral layer at its uniform load (4096 rows): the same
+    # per-tile work as "mixtral" with ~1.5 GB on the device, for profiler captures
+    "mixtral_e1": Workload("mixtral_e1", 6, T=4096, H=4096, I=14336, E=1, k=1),
 }
 
 
