@@ -109,6 +109,29 @@ int mxg_route_permute(const int32_t* ids, int T, int k, int E, int32_t* split_si
                       int32_t* row_of_src, int32_t* padded_offsets, void* ws, size_t ws_bytes,
                       int32_t* dev_status, void* stream);
 
+/* Permute without caller scratch.  No counterpart in the paper: an addition for
+ * callers that cannot allocate device memory where they route tokens (code
+ * inside another framework's memory pool, or a runtime that hands out only the
+ * input and output buffers), so they cannot provide the `ws` buffer above.
+ * Same inputs, outputs, results and error reporting as mxg_route_permute; the
+ * scratch is a fixed 256 KB (MXG_NOALLOC_SCRATCH_BYTES) array in device memory
+ * that every GPU loading this library holds until the process exits.
+ *   - At most mxg_route_permute_noalloc_max_entries(E) routed entries (T*k);
+ *     larger calls return MXG_ERR_WORKSPACE without launching (16,773,120
+ *     entries for E = 8, 2,093,056 for E = 64, 520,192 for E = 256).
+ *   - The first call on each device looks up the array's device address (a
+ *     host-side runtime query, no allocation); make that first call before any
+ *     stream capture that contains the entry point.
+ *   - All calls share the one array.  Calls whose kernels overlap on the GPU
+ *     (different streams without ordering) race and give wrong results;
+ *     serialise them.  Nothing needs clearing between calls: every scratch
+ *     entry is written before it is read.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine. */
+#define MXG_NOALLOC_SCRATCH_BYTES 262144
+size_t mxg_route_permute_noalloc_max_entries(int E);
+int mxg_route_permute_noalloc(const int32_t* ids, int T, int k, int E, int32_t* split_sizes, int32_t* src_of_row,
+                              int32_t* row_of_src, int32_t* padded_offsets, int32_t* dev_status, void* stream);
+
 /* ----------------------------------------------------------------------------
  * MXFP8 quantisation of a bf16 matrix x [rows][cols].  [Grouped] "Reducing
  * memory pressure with MXFP8", Fig. 3; [Overhead] "How MXFP8 reduces memory

@@ -28,6 +28,7 @@ EXPORTS = [
     "mxg_route_permute_workspace_bytes", "mxg_route_permute", "mxg_mxfp8_quantize", "mxg_grouped_gemm",
     "mxg_grouped_gemm_wgrad", "mxg_mlp_saved_bytes", "mxg_mlp_workspace_bytes", "mxg_grouped_mlp_fwd",
     "mxg_grouped_mlp_bwd", "mxg_mlp_saved_view", "mxg_grouped_mlp_fwd_stage", "mxg_grouped_mlp_bwd_stage",
+    "mxg_route_permute_noalloc_max_entries", "mxg_route_permute_noalloc",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
         "mxg_grouped_mlp_bwd": (I32, [ctypes.POINTER(MlpBwdArgs), P]),
         "mxg_mlp_saved_view": (P, [P, I32, I32, I32, I32, I32, I32]),
         "mxg_grouped_mlp_fwd_stage": (I32, [ctypes.POINTER(MlpFwdArgs), I32, P]),
+        "mxg_route_permute_noalloc_max_entries": (SZ, [I32]),
+        "mxg_route_permute_noalloc": (I32, [P, I32, I32, I32, P, P, P, P, P, P]),
         "mxg_grouped_mlp_bwd_stage": (I32, [ctypes.POINTER(MlpBwdArgs), I32, P]),
     }
     for name, (res, args) in sig.items():
