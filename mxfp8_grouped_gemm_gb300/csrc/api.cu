@@ -80,8 +80,7 @@ struct Plan {
     fwd_bytes = f.off;
 
     Carver b;
-    const int bn = gemm_pick_bn(EPI_DSWIGLU, static_cast<int>(I));
-    dp_ld = I / bn;
+    dp_ld = dswiglu_partials(static_cast<int>(I));
     dyq = b.take(Rc * H);
     sdyq = b.take(Rc * H / 32);
     dyc = b.take(H * Rc);
@@ -567,7 +566,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   g.dp_part = at<float>(ws, pl.dp);
   g.dp_ld = static_cast<int32_t>(pl.dp_ld);
   g.status = st;
-  g.tiles_upper = (pl.Rc / 128) * pl.dp_ld;
+  g.tiles_upper = (pl.Rc / 128) * (I / gemm_pick_bn(EPI_DSWIGLU, I));
   MXG_TRY(launch_gemm(g, s));
   }
 

@@ -41,11 +41,20 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 128;
-constexpr int kThreads = 192;
+// warp 0 TMA, warp 1 MMA, warps 2-3 idle, warps 4-11 epilogue (two warpgroups)
+constexpr int kThreads = 384;
+// Register split (setmaxnreg): the control warpgroup gives registers up, the
+// epilogue warpgroups take them.  128*kRegsCtrl + 256*kRegsEpi must not exceed
+// the 384 * (registers per thread at launch) the block starts with; the host
+// checks this against the compiled register count before launching.
+constexpr int kRegsCtrl = 88;
+constexpr int kRegsEpi = 200;
 
-template <int BN>
+template <int BN, int EPI>
 struct Cfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kStages = BN == 256 ? 4 : (EPI == 2 ? 5 : 6);
+  // per epilogue warp: a 32 x 33 fp32 tile for the column-wise quantiser (dSwiGLU)
+  static constexpr int kXposeBytes = EPI == 2 ? 8 * 32 * 33 * 4 : 0;
   static constexpr int kAcc = BN == 256 ? 1 : 2;
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = BN * BK;
@@ -56,7 +65,7 @@ struct Cfg {
   static constexpr uint32_t kSfaCol = kAcc * BN;      // TMEM columns of the scale factors
   static constexpr uint32_t kSfbCol = kSfaCol + 4;
   static constexpr int kCtrlBytes = 2048;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kCtrlBytes;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kCtrlBytes + kXposeBytes;
   static_assert(kSfbCol + BN / 32 <= 512, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -129,54 +138,117 @@ __device__ __forceinline__ void col_quant32(const float (&h)[32], uint8_t* qc, u
   sc[sf_mma_offset(col0 + lane, tok0 >> 5, sc_rows)] = static_cast<uint8_t>(my_sb);
 }
 
-template <int BN, bool KG>
-__device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int row) {
-  uint16_t* drow = KG ? P.d + static_cast<int64_t>(tc.e) * P.M * P.N + static_cast<int64_t>(tc.m0 + row) * P.N +
-                            tc.nt * BN
-                      : P.d + static_cast<int64_t>(tc.m0 + row) * P.ldd + tc.nt * BN;
-#pragma unroll 1
-  for (int c = 0; c < BN / 32; c += 2) {
-    uint32_t r0[32], r1[32];
-    tmem_ld_32x32b_x32(tb + c * 32, r0);
-    tmem_ld_32x32b_x32(tb + (c + 1) * 32, r1);
-    tmem_ld_wait();
-    float v[32];
+// The same column-wise MX through a 32 x 33 fp32 shared tile: the warp writes
+// its 32 rows, each lane then reads one column (its 32 tokens), quantises it in
+// registers and writes the 32 codes as one contiguous run of the transposed
+// output.  Bank-conflict free in both directions.
+__device__ __forceinline__ void col_quant32_xpose(const float (&h)[32], float* xp, uint8_t* qc, uint8_t* sc,
+                                                  int64_t ld, int64_t sc_rows, int64_t col0, int64_t tok0,
+                                                  int lane) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = u2f(r0[i]);
-    store_bf16_32(drow + c * 32, v);
+  for (int i = 0; i < 32; ++i) xp[lane * 33 + i] = h[i];
+  __syncwarp();
+  float v[32];
+  uint32_t amax = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = u2f(r1[i]);
-    store_bf16_32(drow + (c + 1) * 32, v);
+  for (int i = 0; i < 32; ++i) {
+    v[i] = xp[i * 33 + lane];
+    amax = max(amax, f2u(v[i]) & 0x7fffffffu);
   }
+  __syncwarp();
+  const uint32_t sb = mx_scale_byte(amax);
+  const float inv = mx_inv_scale(sb);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] *= inv;
+  uint32_t w[8];
+  encode32(v, w);
+  uint4* d = reinterpret_cast<uint4*>(qc + (col0 + lane) * ld + tok0);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  sc[sf_mma_offset(col0 + lane, tok0 >> 5, sc_rows)] = static_cast<uint8_t>(sb);
+}
+
+// Hand the accumulator buffer back to the MMA warp (all of this warp's TMEM
+// loads have completed).
+__device__ __forceinline__ void release_acc(uint64_t* bar, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+// bf16 store.  The thread owns half of its row's BN columns; it drains them
+// from TMEM into packed bf16 registers, releases the accumulator, then stores,
+// so the next tile's MMAs overlap the global stores.
+template <int BN, bool KG>
+__device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int row, int hf,
+                                         uint64_t* tempty, int lane) {
+  constexpr int COLS = BN / 2;
+  uint32_t packed[COLS / 2];
+#pragma unroll
+  for (int c = 0; c < COLS / 32; c += 2) {
+    uint32_t r0[32], r1[32];
+    tmem_ld_32x32b_x32(tb + hf * COLS + c * 32, r0);
+    tmem_ld_32x32b_x32(tb + hf * COLS + (c + 1) * 32, r1);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      packed[c * 16 + i] = pack_bf16x2(u2f(r0[2 * i]), u2f(r0[2 * i + 1]));
+      packed[(c + 1) * 16 + i] = pack_bf16x2(u2f(r1[2 * i]), u2f(r1[2 * i + 1]));
+    }
+  }
+  release_acc(tempty, lane);
+  uint16_t* drow = KG ? P.d + static_cast<int64_t>(tc.e) * P.M * P.N + static_cast<int64_t>(tc.m0 + row) * P.N +
+                            tc.nt * BN + hf * COLS
+                      : P.d + static_cast<int64_t>(tc.m0 + row) * P.ldd + tc.nt * BN + hf * COLS;
+  uint4* d = reinterpret_cast<uint4*>(drow);
+#pragma unroll
+  for (int j = 0; j < COLS / 8; ++j)
+    d[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
 }
 
 // Gate-up tile: accumulator columns [0,128) = gate j0.., [128,256) = up j0..
-__device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane) {
+// The thread owns 64 h columns (half hf).  It drains its 128 accumulator
+// columns into registers, releases the accumulator, then computes h in fp32 and
+// quantises and stores while the next tile's MMAs run.
+__device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
+                                           int hf, uint64_t* tempty) {
   const int64_t tok0 = tc.m0 + q * 32;
   const int64_t r = tok0 + lane;
   const float p = P.probs_perm[r];
   const int64_t I = P.I;
-  const int j0 = tc.nt * 128;
-#pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
-    uint32_t g[32], u[32];
-    tmem_ld_32x32b_x32(tb + c * 32, g);
-    tmem_ld_32x32b_x32(tb + 128 + c * 32, u);
-    tmem_ld_wait();
+  const int j0 = tc.nt * 128 + hf * 64;
+  const bool save = P.gu_save != nullptr;
+  uint32_t g[2][32], u[2][32];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    tmem_ld_32x32b_x32(tb + hf * 64 + c * 32, g[c]);
+    tmem_ld_32x32b_x32(tb + 128 + hf * 64 + c * 32, u[c]);
+  }
+  tmem_ld_wait();
+  release_acc(tempty, lane);
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
     const int64_t col = j0 + c * 32;
     float h[32];
-    if (P.gu_save != nullptr) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) h[i] = u2f(g[i]);
-      store_bf16_32(P.gu_save + r * (2 * I) + col, h);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) h[i] = u2f(u[i]);
-      store_bf16_32(P.gu_save + r * (2 * I) + I + col, h);
-    }
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float gf = u2f(g[i]);
-      h[i] = p * (gf / (1.f + __expf(-gf))) * u2f(u[i]);
+      const float gf = u2f(g[c][i]);
+      h[i] = p * __fdividef(gf, 1.f + __expf(-gf)) * u2f(u[c][i]);
+    }
+    if (save) {
+      uint32_t gp[16], up[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        gp[i] = pack_bf16x2(u2f(g[c][2 * i]), u2f(g[c][2 * i + 1]));
+        up[i] = pack_bf16x2(u2f(u[c][2 * i]), u2f(u[c][2 * i + 1]));
+      }
+      uint4* gs = reinterpret_cast<uint4*>(P.gu_save + r * (2 * I) + col);
+      uint4* us = reinterpret_cast<uint4*>(P.gu_save + r * (2 * I) + I + col);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        gs[j] = make_uint4(gp[4 * j], gp[4 * j + 1], gp[4 * j + 2], gp[4 * j + 3]);
+        us[j] = make_uint4(up[4 * j], up[4 * j + 1], up[4 * j + 2], up[4 * j + 3]);
+      }
     }
     const uint32_t sb = row_quant32(h, P.q_out + r * P.q_out_ld + col);
     P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
@@ -184,29 +256,32 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& t
   }
 }
 
-// dgrad-down tile: accumulator = dH columns j0.., j0 + BN.
+// dgrad-down tile: accumulator = dH columns nt*BN.., the thread owns half hf.
+// Partial d(prob) sums go to dp_part[r][2*nt + hf].
 template <int BN>
-__device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q,
-                                            int lane) {
+__device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
+                                            int hf, uint64_t* tempty, float* xp) {
+  constexpr int COLS = BN / 2;
   const int64_t tok0 = tc.m0 + q * 32;
   const int64_t r = tok0 + lane;
   const float p = P.probs_perm[r];
   const int64_t I = P.I;
-  const int j0 = tc.nt * BN;
+  const int j0 = tc.nt * BN + hf * COLS;
   float dp = 0.f;
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = 0; c < COLS / 32; ++c) {
     uint32_t dh[32];
-    tmem_ld_32x32b_x32(tb + c * 32, dh);
+    tmem_ld_32x32b_x32(tb + hf * COLS + c * 32, dh);
     const int64_t col = j0 + c * 32;
     float g[32], u[32], dg[32];
     load_bf16_32(P.gu_save + r * (2 * I) + col, g);
     load_bf16_32(P.gu_save + r * (2 * I) + I + col, u);
     tmem_ld_wait();
+    if (c == COLS / 32 - 1) release_acc(tempty, lane);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float gf = g[i], uf = u[i];
-      const float s = 1.f / (1.f + __expf(-gf));
+      const float s = __fdividef(1.f, 1.f + __expf(-gf));
       const float sl = gf * s;
       const float a = u2f(dh[i]) * p;
       dg[i] = a * uf * s * (1.f + gf * (1.f - s));
@@ -215,18 +290,18 @@ __device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& 
     }
     uint32_t sb = row_quant32(dg, P.q_out + r * P.q_out_ld + col);
     P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-    col_quant32(dg, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
+    col_quant32_xpose(dg, xp, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
     sb = row_quant32(u, P.q_out + r * P.q_out_ld + I + col);
     P.s_out[sf_mma_offset(r, (I + col) >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-    col_quant32(u, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
+    col_quant32_xpose(u, xp, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
   }
-  P.dp_part[r * P.dp_ld + tc.nt] = dp;
+  P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp;
 }
 
 template <int BN, int EPI, bool KG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs P) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ctrl = smem + C::kStages * C::kStageBytes;
@@ -239,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* never_set = reinterpret_cast<int*>(tmem_slot + 2);
   int* s_poff = reinterpret_cast<int*>(tmem_slot + 4);
+  float* xpose = reinterpret_cast<float*>(ctrl + C::kCtrlBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = P.E;
@@ -250,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < C::kAcc; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], 8);
     }
     mbar_init(drained, 1);
     *abort_flag = 0;
@@ -292,11 +368,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto decode = [&](int64_t t) {
     TileCoord tc;
     if (KG) {
+      // The operand with the larger per-expert footprint is streamed once: its
+      // tile index varies slowest and the other operand's tiles (which stay in
+      // L2) vary fastest.
       const int64_t tpe = static_cast<int64_t>(mtn_kg) * ntn;
       tc.e = static_cast<int>(t / tpe);
       const int local = static_cast<int>(t - tc.e * tpe);
-      tc.nt = local / mtn_kg;
-      tc.m0 = (local - tc.nt * mtn_kg) * BM;
+      if (P.M >= P.N) {
+        tc.m0 = (local / ntn) * BM;
+        tc.nt = local % ntn;
+      } else {
+        tc.nt = local / mtn_kg;
+        tc.m0 = (local % mtn_kg) * BM;
+      }
       tc.kbeg = s_poff[tc.e];
       tc.num_k = (s_poff[tc.e + 1] - s_poff[tc.e]) / BK;
     } else {
@@ -317,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 1;
   };
 
+  if (warp < 4) setmaxnreg_dec<kRegsCtrl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -423,9 +508,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(drained);
       mbar_wait_bounded(drained, 0, never_set, kWaitLimitNs);
     }
-  } else {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
+    setmaxnreg_inc<kRegsEpi>();
+    // warps 4..11: TMEM lane quadrant q = warp % 4, column half hf.
     const int q = warp & 3;
+    const int hf = (warp - 4) >> 2;
+    float* my_xpose = xpose + (warp - 4) * 32 * 33;
     const int row = q * 32 + lane;
     uint32_t acc = 0, acc_phase = 0;
     for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
@@ -433,9 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tc.num_k == 0) {
         // token-grouped tile of an expert without tokens: exact zeros
         uint16_t* drow = P.d + static_cast<int64_t>(tc.e) * P.M * P.N + static_cast<int64_t>(tc.m0 + row) * P.N +
-                         tc.nt * BN;
+                         tc.nt * BN + hf * (BN / 2);
 #pragma unroll 4
-        for (int c = 0; c < BN / 8; ++c) reinterpret_cast<uint4*>(drow)[c] = make_uint4(0u, 0u, 0u, 0u);
+        for (int c = 0; c < BN / 16; ++c) reinterpret_cast<uint4*>(drow)[c] = make_uint4(0u, 0u, 0u, 0u);
         continue;
       }
       bool got = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, kWaitLimitNs);
@@ -447,15 +536,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (EPI == EPI_SWIGLU) {
-        epi_swiglu(P, tc, tb, q, lane);
+        epi_swiglu(P, tc, tb, q, lane, hf, &tempty[acc]);
       } else if (EPI == EPI_DSWIGLU) {
-        epi_dswiglu<BN>(P, tc, tb, q, lane);
+        epi_dswiglu<BN>(P, tc, tb, q, lane, hf, &tempty[acc], my_xpose);
       } else {
-        epi_bf16<BN, KG>(P, tc, tb, row);
+        epi_bf16<BN, KG>(P, tc, tb, row, hf, &tempty[acc], lane);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
       if (++acc == C::kAcc) {
         acc = 0;
         acc_phase ^= 1;
@@ -515,12 +601,18 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
   if (!encode_u8(&ta, g.a, g.a_cols, g.a_rows, BK, BM)) return cudaErrorInvalidValue;
   if (!encode_u8(&tb, g.b, g.b_cols, g.b_rows, BK, EPI == EPI_SWIGLU ? 128 : BN)) return cudaErrorInvalidValue;
   auto kern = gemm_kernel<BN, EPI, KG>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::kSmem);
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN, EPI>::kSmem);
   if (err != cudaSuccess) return err;
+  // the register split must fit in what the block is launched with, or the
+  // epilogue warps' register increase would never be granted
+  cudaFuncAttributes fa;
+  err = cudaFuncGetAttributes(&fa, kern);
+  if (err != cudaSuccess) return err;
+  if (static_cast<int64_t>(fa.numRegs) * kThreads < 128 * kRegsCtrl + 256 * kRegsEpi) return cudaErrorInvalidConfiguration;
   int64_t grid = num_sms();
   if (g.tiles_upper < grid) grid = g.tiles_upper;
   if (grid < 1) grid = 1;
-  kern<<<static_cast<unsigned>(grid), kThreads, Cfg<BN>::kSmem, s>>>(ta, tb, g);
+  kern<<<static_cast<unsigned>(grid), kThreads, Cfg<BN, EPI>::kSmem, s>>>(ta, tb, g);
   count_launch();
   return cudaGetLastError();
 }
@@ -529,14 +621,18 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
 
 int gemm_pick_bn(int epi, int N) {
   if (epi == EPI_SWIGLU) return 256;
+  // the dSwiGLU epilogue is heavier than a 128x256 mainloop: use 128-wide tiles,
+  // whose accumulators double-buffer in TMEM so the epilogue runs under the MMAs
+  if (epi == EPI_DSWIGLU) return 128;
   return N % 256 == 0 ? 256 : 128;
 }
+
+int dswiglu_partials(int I) { return 2 * (I / gemm_pick_bn(EPI_DSWIGLU, I)); }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
   const int bn = gemm_pick_bn(g.epi, g.epi == EPI_DSWIGLU ? g.I : g.N);
   if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false>(g, s);
-  if (g.epi == EPI_DSWIGLU)
-    return bn == 256 ? launch_impl<256, EPI_DSWIGLU, false>(g, s) : launch_impl<128, EPI_DSWIGLU, false>(g, s);
+  if (g.epi == EPI_DSWIGLU) return launch_impl<128, EPI_DSWIGLU, false>(g, s);
   if (g.kgroup) return bn == 256 ? launch_impl<256, EPI_BF16, true>(g, s) : launch_impl<128, EPI_BF16, true>(g, s);
   return bn == 256 ? launch_impl<256, EPI_BF16, false>(g, s) : launch_impl<128, EPI_BF16, false>(g, s);
 }

@@ -97,6 +97,7 @@ struct GemmArgs {
   int64_t tiles_upper;        // host bound on the number of tiles (grid sizing)
 };
 int gemm_pick_bn(int epi, int N);
+int dswiglu_partials(int I);   // d(prob) partial sums per row (two per column tile)
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s);
 
 }  // namespace mxg

@@ -111,16 +111,66 @@ def permute(ids: np.ndarray, E: int) -> dict:
             "src_of_row": src_of_row, "row_of_src": row_of_src}
 
 
+# ------------------------------------------------------ per-expert steps ----
+
+def scaled_swiglu(g, u, p):
+    """ScaledSwiGLU: h = p * SiLU(g) * u (p broadcast over columns)."""
+    return p * silu(g) * u
+
+
+def dscaled_swiglu(dh, g, u, p):
+    """Gradients of h = p SiLU(g) u: with s = sigmoid(g),
+    dg = dh p u s (1 + g (1 - s)), du = dh p g s, and the per-element terms of
+    d(prob) = sum_i dh g s u."""
+    s = sigmoid(g)
+    sl = g * s
+    dg = dh * p * u * s * (1.0 + g * (1.0 - s))
+    du = dh * p * sl
+    return dg, du, dh * sl * u
+
+
+def expert_weights(w_gate_up_e, w_down_e, quant: bool = True, backward: bool = True) -> dict:
+    """One expert's weights, fake-quantised along each GEMM's contraction axis:
+    wg [2I,H] along H (gate-up), wd [H,I] along I (down), and for the backward
+    wdT [I,H] along H (dgrad-down) and wguT [H,2I] along 2I (dgrad-gate-up)."""
+    wgu = np.asarray(w_gate_up_e, dtype=np.float64)
+    wd = np.asarray(w_down_e, dtype=np.float64)
+    out = {"wg": _fq(wgu, quant), "wd": _fq(wd, quant)}
+    if backward:
+        out["wdT"] = _fq(wd.T, quant)
+        out["wguT"] = _fq(wgu.T, quant)
+    return out
+
+
+def expert_forward_rows(xq_rows, p_rows, w: dict, quant: bool = True):
+    """Rows of one expert: GU = Xq Wg^T; h = ScaledSwiGLU(g, u, p); Y = MX(h) Wd^T."""
+    gu = xq_rows @ w["wg"].T
+    I = gu.shape[1] // 2
+    h = scaled_swiglu(gu[:, :I], gu[:, I:], p_rows[:, None])
+    y = _fq(h, quant) @ w["wd"].T
+    return gu, h, y
+
+
+def expert_backward_rows(dyq_rows, gu, p_rows, w: dict, quant: bool = True):
+    """Activation gradients for rows of one expert: dH = dYq WdT^T; dGU from
+    dScaledSwiGLU; dX = MX(dGU) WguT^T; per-row d(prob)."""
+    I = gu.shape[1] // 2
+    dh = dyq_rows @ w["wdT"].T
+    dg, du, dpt = dscaled_swiglu(dh, gu[:, :I], gu[:, I:], p_rows[:, None])
+    dgu = np.concatenate([dg, du], axis=1)
+    dx = _fq(dgu, quant) @ w["wguT"].T
+    return dh, dgu, dpt.sum(axis=1), dx
+
+
+def expert_weight_grads(dy_perm_e, h_e, dgu_e, x_perm_e, quant: bool = True):
+    """dW_down = colMX(dY)^T colMX(h) and dW_gate_up = colMX(dGU)^T colMX(X) over
+    the expert's tokens (column-wise blocks of 32 tokens from its first row)."""
+    dw_d = _fqc(dy_perm_e, quant).T @ _fqc(h_e, quant)
+    dw_gu = _fqc(dgu_e, quant).T @ _fqc(x_perm_e, quant)
+    return dw_d, dw_gu
+
+
 # ---------------------------------------------------------------- forward ----
-
-def expert_gate_up_rows(xq_rows, p_rows, wg_q, I):
-    """One expert's rows: GU = Xq Wgu^T and h = p SiLU(g) u, with
-    ``xq_rows``/``wg_q`` already (fake-)quantised fp64."""
-    gu = xq_rows @ wg_q.T
-    g, u = gu[:, :I], gu[:, I:]
-    h = p_rows[:, None] * silu(g) * u
-    return gu, h
-
 
 def mlp_fwd(x, ids, probs, w_gate_up, w_down, quant: bool = True) -> dict:
     """Forward of the grouped expert MLP.  Shapes: x [T,H], ids/probs [T,k],
@@ -145,12 +195,10 @@ def mlp_fwd(x, ids, probs, w_gate_up, w_down, quant: bool = True) -> dict:
     off = perm["offsets"]
     for e in range(E):
         a, b = off[e], off[e + 1]
-        wg = _fq(np.asarray(w_gate_up[e], dtype=np.float64), quant)     # along H
-        wd = _fq(np.asarray(w_down[e], dtype=np.float64), quant)        # along I
         if b == a:
             continue
-        gu[a:b], h[a:b] = expert_gate_up_rows(xq[a:b], p_perm[a:b], wg, I)
-        y_perm[a:b] = _fq(h[a:b], quant) @ wd.T
+        w = expert_weights(w_gate_up[e], w_down[e], quant, backward=False)
+        gu[a:b], h[a:b], y_perm[a:b] = expert_forward_rows(xq[a:b], p_perm[a:b], w, quant)
     y = np.zeros((T, H))
     row = perm["row_of_src"].reshape(T, k)
     for j in range(k):
@@ -187,19 +235,9 @@ def mlp_bwd(ctx: dict, dy) -> dict:
         a, b = off[e], off[e + 1]
         if b == a:
             continue                                  # empty expert: dW stays 0
-        wdT = _fq(np.asarray(ctx["w_down"][e], dtype=np.float64).T, quant)      # [I,H] along H
-        wguT = _fq(np.asarray(ctx["w_gate_up"][e], dtype=np.float64).T, quant)  # [H,2I] along 2I
-        dh[a:b] = dyq[a:b] @ wdT.T
-        g, u = gu[a:b, :I], gu[a:b, I:]
-        s = sigmoid(g)
-        sl = g * s
-        p = p_perm[a:b, None]
-        dgu[a:b, :I] = dh[a:b] * p * u * s * (1.0 + g * (1.0 - s))
-        dgu[a:b, I:] = dh[a:b] * p * sl
-        dp[a:b] = np.sum(dh[a:b] * sl * u, axis=1)
-        dx_perm[a:b] = _fq(dgu[a:b], quant) @ wguT.T                 # dGU along 2I
-        dw_d[e] = _fqc(dy_perm[a:b], quant).T @ _fqc(h[a:b], quant)
-        dw_gu[e] = _fqc(dgu[a:b], quant).T @ _fqc(x_perm[a:b], quant)
+        w = expert_weights(ctx["w_gate_up"][e], ctx["w_down"][e], quant)
+        dh[a:b], dgu[a:b], dp[a:b], dx_perm[a:b] = expert_backward_rows(dyq[a:b], gu[a:b], p_perm[a:b], w, quant)
+        dw_d[e], dw_gu[e] = expert_weight_grads(dy_perm[a:b], h[a:b], dgu[a:b], x_perm[a:b], quant)
     row = perm["row_of_src"].reshape(T, k)
     dx = np.zeros((T, H))
     for j in range(k):

@@ -118,10 +118,25 @@ def dequantize_blocks(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return (vals * e8m0_decode(scales)[..., None]).reshape(codes.shape)
 
 
-def fake_quant(v: np.ndarray) -> np.ndarray:
-    """Quantise then dequantise along the last axis."""
-    c, s = quantize_blocks(v)
-    return dequantize_blocks(c, s)
+def fake_quant(v: np.ndarray, chunk_rows: int | None = None) -> np.ndarray:
+    """Quantise then dequantise along the last axis, without materialising the
+    bit patterns: the dequantised value is the E4M3-rounded scaled value times
+    2^e (encode followed by decode is the identity on the E4M3 grid).  Same
+    steps as quantize_blocks: block max, shared exponent, exact scaling, RNE
+    with saturation.  Processed in row chunks to bound memory."""
+    v = np.asarray(v, dtype=np.float64)
+    K = v.shape[-1]
+    assert K % BLOCK == 0
+    flat = v.reshape(-1, K)
+    out = np.empty_like(flat)
+    if chunk_rows is None:                      # ~64K elements: temporaries stay in cache
+        chunk_rows = max(1, 65536 // K)
+    for r0 in range(0, flat.shape[0], chunk_rows):
+        b = flat[r0:r0 + chunk_rows].reshape(-1, K // BLOCK, BLOCK)
+        e = block_scale_exponent(np.max(np.abs(b), axis=-1))
+        scale = np.ldexp(1.0, e)[..., None]
+        out[r0:r0 + chunk_rows] = (e4m3_round(b / scale) * scale).reshape(-1, K)
+    return out.reshape(v.shape)
 
 
 def quantize_group_columns(a: np.ndarray) -> tuple:

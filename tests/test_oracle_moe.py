@@ -223,3 +223,49 @@ def test_backward_quantised_uses_mx_operands():
         np.testing.assert_allclose(g["dh"][a:b], dh, rtol=1e-12, atol=1e-12)
         dwd = mx.fake_quant_group_columns(dyp).T @ mx.fake_quant_group_columns(ctx["h"][a:b])
         np.testing.assert_allclose(g["dw_down"][e], dwd, rtol=1e-12, atol=1e-14)
+
+
+def test_sampled_evaluation_equals_full_oracle():
+    """The sampled evaluation used at full sizes reproduces the full oracle on
+    the sampled tokens and weight-gradient slices."""
+    from oracle import sampled
+    T, H, I, E, k = 96, 64, 96, 4, 2
+    c = _case(T, H, I, E, k, 91, empty_experts=(2,))
+    ids, probs = moe.route_topk(c["logits"], k)
+    ctx = moe.mlp_fwd(c["x"], ids, probs, c["w_gate_up"], c["w_down"])
+    g = moe.mlp_bwd(ctx, c["dy"])
+    perm = ctx["perm"]
+    expert_of_row = np.repeat(np.arange(E), perm["split_sizes"])
+    W = {e: moe.expert_weights(c["w_gate_up"][e], c["w_down"][e]) for e in range(E)}
+    tokens = [0, 5, 17, 95]
+    s = sampled.rows_forward_backward(tokens, c["x"], c["dy"], probs, perm["row_of_src"], expert_of_row, k, W)
+    np.testing.assert_allclose(s["y"], ctx["y"][tokens], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(s["dx"], g["dx"][tokens], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(s["dprobs"], g["dprobs"][tokens], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(s["gu"], ctx["gu"][s["rows"]], rtol=1e-11, atol=1e-13)
+    tok = perm["src_of_row"] // k
+    for e in (0, 3):
+        a, b = perm["offsets"][e], perm["offsets"][e + 1]
+        xe, dye, pe = c["x"][tok[a:b]], c["dy"][tok[a:b]], ctx["p_perm"][a:b]
+        cols = np.array([0, 7, 50, 95])
+        got = sampled.dw_down_columns(xe, dye, pe, c["w_gate_up"][e], cols)
+        np.testing.assert_allclose(got, g["dw_down"][e][:, cols], rtol=1e-11, atol=1e-13)
+        rows = np.array([1, 60, 96, 150, 191])
+        got = sampled.dw_gate_up_rows(xe, dye, pe, c["w_gate_up"][e], c["w_down"][e], rows)
+        np.testing.assert_allclose(got, g["dw_gate_up"][e][rows], rtol=1e-11, atol=1e-13)
+
+
+def test_weight_quant_pool_equals_oracle():
+    """The multi-process weight quantisation used by the full-size tests gives
+    exactly oracle.moe.expert_weights."""
+    from oracle_pool import WeightQuantPool
+    wgu = synthetic.random_bf16((2 * 96, 128), 5, std=0.02)
+    wd = synthetic.random_bf16((128, 96), 6, std=0.02)
+    ref = moe.expert_weights(wgu.double().numpy(), wd.double().numpy())
+    pool = WeightQuantPool(workers=3)
+    try:
+        got = pool.expert_weights(wgu, wd)
+    finally:
+        pool.close()
+    for n in ("wg", "wd", "wdT", "wguT"):
+        assert np.array_equal(got[n], ref[n]), n

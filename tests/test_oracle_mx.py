@@ -186,3 +186,19 @@ def test_group_columns_blocks_restart_at_group_start():
     back = mx.fake_quant_group_columns(a)
     assert back.shape == a.shape
     np.testing.assert_array_equal(back[:32], mx.fake_quant(a[:32].T).T)
+
+
+def test_fake_quant_equals_quantize_then_dequantize():
+    """The direct fake-quantiser is the quantise -> encode -> decode -> dequantise
+    round trip, bit for bit."""
+    rng = np.random.default_rng(21)
+    v = rng.standard_normal((300, 256)) * np.exp2(rng.integers(-50, 50, size=(300, 1)))
+    v[0] = 0.0
+    v[1, :32] = 448.0 * 2.0 ** 5
+    v[2, 7] = 464.0
+    v[3, 40:64] = 1e-300
+    c, s = mx.quantize_blocks(v)
+    ref = mx.dequantize_blocks(c, s)
+    got = mx.fake_quant(v, chunk_rows=37)
+    assert np.array_equal(got, ref)
+    assert np.array_equal(np.signbit(got), np.signbit(ref))
