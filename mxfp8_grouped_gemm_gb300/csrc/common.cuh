@@ -6,7 +6,7 @@
 
 #include <cstdint>
 
-#include "../../include/mxg.h"
+#include "mxg.h"
 
 namespace mxg {
 
