@@ -249,6 +249,11 @@ enum {
 int mxg_grouped_mlp_fwd_stage(const mxg_mlp_fwd_args* args, int stage, void* stream);
 int mxg_grouped_mlp_bwd_stage(const mxg_mlp_bwd_args* args, int stage, void* stream);
 
+/* The MLP keeps each expert's rows in a padded layout whose groups start on a
+ * multiple of mxg_mlp_group_align() rows (256: one CTA-pair GEMM tile);
+ * mxg_mlp_row_capacity() is the number of padded rows it reserves. */
+int mxg_mlp_group_align(void);
+size_t mxg_mlp_row_capacity(int T, int k, int E);
 size_t mxg_mlp_saved_bytes(int T, int H, int I, int E, int k);
 size_t mxg_mlp_workspace_bytes(int T, int H, int I, int E, int k);
 int mxg_grouped_mlp_fwd(const mxg_mlp_fwd_args* args, void* stream);
@@ -256,8 +261,9 @@ int mxg_grouped_mlp_bwd(const mxg_mlp_bwd_args* args, void* stream);
 
 /* Debug views into `saved` (device pointers; NULL on bad arguments) used by the
  * tests to compare intermediates: 0 = GU (bf16 [m_cap][2I], the gate-up GEMM
- * output before the activation), 1 = padded_offsets (int32 [E+1]),
- * 2 = row_of_src in the padded layout (int32 [T*k]). */
+ * output before the activation; m_cap = mxg_mlp_row_capacity), 1 =
+ * padded_offsets (int32 [E+1], multiples of mxg_mlp_group_align()), 2 =
+ * row_of_src in the padded layout (int32 [T*k]). */
 const void* mxg_mlp_saved_view(const void* saved, int T, int H, int I, int E, int k, int which);
 
 #ifdef __cplusplus

@@ -28,7 +28,8 @@ EXPORTS = [
     "mxg_route_permute_workspace_bytes", "mxg_route_permute", "mxg_mxfp8_quantize", "mxg_grouped_gemm",
     "mxg_grouped_gemm_wgrad", "mxg_mlp_saved_bytes", "mxg_mlp_workspace_bytes", "mxg_grouped_mlp_fwd",
     "mxg_grouped_mlp_bwd", "mxg_mlp_saved_view", "mxg_grouped_mlp_fwd_stage", "mxg_grouped_mlp_bwd_stage",
-    "mxg_route_permute_noalloc_max_entries", "mxg_route_permute_noalloc",
+    "mxg_route_permute_noalloc_max_entries", "mxg_route_permute_noalloc", "mxg_mlp_group_align",
+    "mxg_mlp_row_capacity",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -82,6 +83,8 @@ def lib() -> ctypes.CDLL:
         "mxg_grouped_gemm": (I32, [P, P, P, P, P, I32, I32, I32, I32, P, P, P]),
         "mxg_grouped_gemm_wgrad": (I32, [P, P, P, P, P, I32, I32, I32, I32, P, P, P]),
         "mxg_mlp_saved_bytes": (SZ, [I32, I32, I32, I32, I32]),
+        "mxg_mlp_group_align": (I32, []),
+        "mxg_mlp_row_capacity": (SZ, [I32, I32, I32]),
         "mxg_mlp_workspace_bytes": (SZ, [I32, I32, I32, I32, I32]),
         "mxg_grouped_mlp_fwd": (I32, [ctypes.POINTER(MlpFwdArgs), P]),
         "mxg_grouped_mlp_bwd": (I32, [ctypes.POINTER(MlpBwdArgs), P]),
@@ -209,6 +212,14 @@ def mxg_grouped_gemm_wgrad(a, sa, b, sb, padded_offsets, E: int, dev_status, d=N
         _ptr(padded_offsets, torch.int32, "padded_offsets"), E, M, N, t_cap, _ptr(_bits(d)),
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
     return d
+
+
+def mxg_mlp_group_align() -> int:
+    return int(lib().mxg_mlp_group_align())
+
+
+def mxg_mlp_row_capacity(T, k, E) -> int:
+    return int(lib().mxg_mlp_row_capacity(T, k, E))
 
 
 def mxg_mlp_saved_bytes(T, H, I, E, k) -> int:

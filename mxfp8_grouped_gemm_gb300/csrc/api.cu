@@ -20,9 +20,15 @@ constexpr int64_t kAlign = 256;
 inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Row capacity of the per-expert padded layout: every group starts on a
-// multiple of 128 rows, so sum_e roundup(m_e, 128) <= roundup(T*k, 128) + 128*E.
-inline int64_t row_cap(int64_t T, int64_t k, int64_t E) { return align_up(T * k, 128) + 128 * E; }
+// CTA-pair GEMM tiles (256 x 128 over two SMs) for the MLP.  Off: measured on
+// GB300, a 128-column slice per SM keeps the tensor pipe only ~35% busy, below
+// the single-CTA 128 x 256 tiles.
+constexpr bool kUsePairTiles = false;
+// The MLP's per-expert row layout: every group starts on a multiple of the
+// GEMM tile height (256 rows with CTA pairs, else 128), so
+// sum_e roundup(m_e, A) <= roundup(T*k, A) + A*E.
+constexpr int kMlpAlign = kUsePairTiles ? 256 : 128;
+inline int64_t row_cap(int64_t T, int64_t k, int64_t E) { return align_up(T * k, kMlpAlign) + kMlpAlign * E; }
 
 struct Carver {
   int64_t off = 0;
@@ -187,6 +193,7 @@ int mxg_route_permute(const int32_t* ids, int T, int k, int E, int32_t* split_si
   p.bases = at<int32_t>(ws, align_up(4 * nblk * E, kAlign));
   p.offsets = at<int32_t>(ws, 2 * align_up(4 * nblk * E, kAlign));
   p.padded_offsets = padded_offsets;
+  p.pad = 128;
   p.split_sizes = split_sizes;
   p.src_of_row = src_of_row;
   p.row_of_src = row_of_src;
@@ -287,6 +294,13 @@ int mxg_grouped_gemm_wgrad(const uint8_t* a, const uint8_t* sa, const uint8_t* b
   return cuda_status(launch_gemm(g, static_cast<cudaStream_t>(stream)));
 }
 
+int mxg_mlp_group_align(void) { return kMlpAlign; }
+
+size_t mxg_mlp_row_capacity(int T, int k, int E) {
+  if (T <= 0 || k <= 0 || E <= 0) return 0;
+  return static_cast<size_t>(row_cap(T, k, E));
+}
+
 size_t mxg_mlp_saved_bytes(int T, int H, int I, int E, int k) {
   if (!mlp_shape_ok(T, H, I, E, k)) return 0;
   return static_cast<size_t>(Plan(T, H, I, E, k).saved_bytes);
@@ -343,6 +357,7 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   pp.bases = at<int32_t>(ws, pl.bases);
   pp.offsets = at<int32_t>(ws, pl.offsets);
   pp.padded_offsets = at<int32_t>(sv, pl.poff);
+  pp.pad = kMlpAlign;
   pp.split_sizes = A->split_sizes;
   pp.prow_src = at<int32_t>(sv, pl.prow_src);
   pp.prow_of_src = at<int32_t>(sv, pl.prow_of_src);
@@ -363,6 +378,7 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   wq.q_row = at<uint8_t>(ws, pl.wgu);
   wq.s_row = at<uint8_t>(ws, pl.swgu);
   wq.sf_row_rows = pl.E * 2 * I;
+  wq.sf_row_interleave = kUsePairTiles ? I : 0;   // gate/up scale rows interleaved for CTA-pair tiles
   if (save) {
     wq.q_col = at<uint8_t>(sv, pl.wguT);
     wq.s_col = at<uint8_t>(sv, pl.swguT);
@@ -372,6 +388,7 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   wq.layout = MXG_LAYOUT_MMA;
   MXG_TRY(launch_quant(wq, s));
   QuantParams dq = wq;
+  dq.sf_row_interleave = 0;
   dq.x = A->w_down;
   dq.ld_x = I;
   dq.x_batch_stride = pl.H * I;
@@ -420,6 +437,7 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   if (run(MXG_FWD_GATE_UP)) {
   GemmArgs g{};
   g.epi = EPI_SWIGLU;
+  g.pair = kUsePairTiles;
   g.a = at<uint8_t>(ws, pl.xq);
   g.sa = at<uint8_t>(ws, pl.sxq);
   g.a_rows = pl.Rc;
@@ -448,7 +466,7 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
     g.sc_rows = I;
   }
   g.status = st;
-  g.tiles_upper = (pl.Rc / 128) * (I / 128);
+  g.tiles_upper = kUsePairTiles ? (pl.Rc / 256) * (I / 64) : (pl.Rc / 128) * (I / 128);
   MXG_TRY(launch_gemm(g, s));
   }
 
@@ -456,6 +474,7 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   if (run(MXG_FWD_DOWN)) {
   GemmArgs d{};
   d.epi = EPI_BF16;
+  d.pair = kUsePairTiles;
   d.a = at<uint8_t>(ws, pl.hq);
   d.sa = at<uint8_t>(ws, pl.shq);
   d.a_rows = pl.Rc;
@@ -473,7 +492,7 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   d.d = at<uint16_t>(ws, pl.yperm);
   d.ldd = H;
   d.status = st;
-  d.tiles_upper = (pl.Rc / 128) * (H / gemm_pick_bn(EPI_BF16, H));
+  d.tiles_upper = kUsePairTiles ? (pl.Rc / 256) * (H / 128) : (pl.Rc / 128) * (H / gemm_pick_bn(EPI_BF16, H));
   MXG_TRY(launch_gemm(d, s));
   }
 
@@ -538,6 +557,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   if (run(MXG_BWD_DGRAD_DOWN)) {
   GemmArgs g{};
   g.epi = EPI_DSWIGLU;
+  g.pair = kUsePairTiles;
   g.a = at<uint8_t>(ws, pl.dyq);
   g.sa = at<uint8_t>(ws, pl.sdyq);
   g.a_rows = pl.Rc;
@@ -566,7 +586,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   g.dp_part = at<float>(ws, pl.dp);
   g.dp_ld = static_cast<int32_t>(pl.dp_ld);
   g.status = st;
-  g.tiles_upper = (pl.Rc / 128) * (I / gemm_pick_bn(EPI_DSWIGLU, I));
+  g.tiles_upper = (pl.Rc / (kUsePairTiles ? 256 : 128)) * (I / 128);
   MXG_TRY(launch_gemm(g, s));
   }
 
@@ -575,6 +595,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   GemmArgs w{};
   w.epi = EPI_BF16;
   w.kgroup = true;
+  w.pair = kUsePairTiles && H % 256 == 0;   // CTA-pair tiles need 256 output rows
   w.a = at<uint8_t>(ws, pl.dyc);
   w.sa = at<uint8_t>(ws, pl.sdyc);
   w.a_rows = H;
@@ -590,7 +611,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   w.d = A->dw_down;
   w.ldd = I;
   w.status = st;
-  w.tiles_upper = pl.E * (H / 128) * (I / gemm_pick_bn(EPI_BF16, I));
+  w.tiles_upper = w.pair ? pl.E * (H / 256) * (I / 128) : pl.E * (H / 128) * (I / gemm_pick_bn(EPI_BF16, I));
   MXG_TRY(launch_gemm(w, s));
   }
 
@@ -598,6 +619,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   if (run(MXG_BWD_DGRAD_GATE_UP)) {
   GemmArgs x{};
   x.epi = EPI_BF16;
+  x.pair = kUsePairTiles;
   x.a = at<uint8_t>(ws, pl.dguq);
   x.sa = at<uint8_t>(ws, pl.sdguq);
   x.a_rows = pl.Rc;
@@ -615,7 +637,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   x.d = at<uint16_t>(ws, pl.dxperm);
   x.ldd = H;
   x.status = st;
-  x.tiles_upper = (pl.Rc / 128) * (H / gemm_pick_bn(EPI_BF16, H));
+  x.tiles_upper = kUsePairTiles ? (pl.Rc / 256) * (H / 128) : (pl.Rc / 128) * (H / gemm_pick_bn(EPI_BF16, H));
   MXG_TRY(launch_gemm(x, s));
   }
 
@@ -624,6 +646,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   GemmArgs v{};
   v.epi = EPI_BF16;
   v.kgroup = true;
+  v.pair = kUsePairTiles;     // 2I is a multiple of 256
   v.a = at<uint8_t>(ws, pl.dguc);
   v.sa = at<uint8_t>(ws, pl.sdguc);
   v.a_rows = 2 * I;
@@ -639,7 +662,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   v.d = A->dw_gate_up;
   v.ldd = H;
   v.status = st;
-  v.tiles_upper = pl.E * (2 * I / 128) * (H / gemm_pick_bn(EPI_BF16, H));
+  v.tiles_upper = kUsePairTiles ? pl.E * (2 * I / 256) * (H / 128) : pl.E * (2 * I / 128) * (H / gemm_pick_bn(EPI_BF16, H));
   MXG_TRY(launch_gemm(v, s));
   }
 

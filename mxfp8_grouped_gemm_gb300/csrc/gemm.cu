@@ -46,24 +46,30 @@ constexpr int BK = 128;
 // lane quadrant; measured faster than packing the epilogue into warps 2-9)
 constexpr int kThreads = 384;
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 struct Cfg {
-  static constexpr int kStages = BN == 256 ? 4 : (EPI == 2 ? 5 : 6);
-  // per epilogue warp: a 32 x 33 fp32 tile for the column-wise quantiser (dSwiGLU)
-  static constexpr int kXposeBytes = EPI == 2 ? 8 * 32 * 33 * 4 : 0;
-  static constexpr int kAcc = BN == 256 ? 1 : 2;
+  static constexpr int CG = PAIR ? 2 : 1;
+  static constexpr int kTileM = PAIR ? 2 * BM : BM;         // rows of one tile (both CTAs)
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;         // rows of B held by one CTA
+  static constexpr int kAcc = (PAIR || BN == 128) ? 2 : 1;  // accumulator buffers in TMEM
   static constexpr int kABytes = BM * BK;
-  static constexpr int kBBytes = BN * BK;
-  static constexpr int kSfaBytes = BM * 4;  // 128 rows x 4 blocks of 32
-  static constexpr int kSfbBytes = BN * 4;
+  static constexpr int kBBytes = kBRows * BK;
+  static constexpr int kSfaBytes = BM * 4;                  // 128 rows x 4 blocks of 32
+  static constexpr int kSfbBytes = BN * 4;                  // every CTA holds the tile's full SFB
   static constexpr uint32_t kTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStageBytes = (kTx + 1023) / 1024 * 1024;
-  static constexpr uint32_t kSfaCol = kAcc * BN;      // TMEM columns of the scale factors
-  static constexpr uint32_t kSfbCol = kSfaCol + 4;
+  // per epilogue warp: a 32 x 33 fp32 tile for the column-wise quantiser (dSwiGLU)
+  static constexpr int kXposeBytes = EPI == 2 ? 8 * 32 * 33 * 4 : 0;
   static constexpr int kCtrlBytes = 2048;
+  static constexpr int kStages = (232448 - 1024 - kCtrlBytes - kXposeBytes) / kStageBytes > 8
+                                     ? 8
+                                     : (232448 - 1024 - kCtrlBytes - kXposeBytes) / kStageBytes;
+  static constexpr uint32_t kSfaCol = kAcc * BN;            // TMEM columns of the scale factors
+  static constexpr uint32_t kSfbCol = kSfaCol + 4;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kCtrlBytes + kXposeBytes;
   static_assert(kSfbCol + BN / 32 <= 512, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(!PAIR || BN == 128, "CTA-pair tiles are 256 x 128");
 };
 
 struct TileCoord {
@@ -76,14 +82,6 @@ struct TileCoord {
 
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
-
-__device__ __forceinline__ void store_bf16_32(uint16_t* dst, const float (&v)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    d[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-}
 
 __device__ __forceinline__ void load_bf16_32(const uint16_t* src, float (&v)[32]) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
@@ -165,11 +163,12 @@ __device__ __forceinline__ void col_quant32_xpose(const float (&h)[32], float* x
 }
 
 // Hand the accumulator buffer back to the MMA warp (all of this warp's TMEM
-// loads have completed).
-__device__ __forceinline__ void release_acc(uint64_t* bar, int lane) {
+// loads have completed).  `bar` is the cluster address of the MMA CTA's
+// barrier (this CTA's own barrier outside CTA pairs).
+__device__ __forceinline__ void release_acc(uint32_t bar, int lane) {
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
+  if (lane == 0) mbar_arrive_remote(bar);
 }
 
 // bf16 store.  The thread owns half of its row's BN columns; it drains them
@@ -177,7 +176,7 @@ __device__ __forceinline__ void release_acc(uint64_t* bar, int lane) {
 // so the next tile's MMAs overlap the global stores.
 template <int BN, bool KG>
 __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int row, int hf,
-                                         uint64_t* tempty, int lane) {
+                                         uint32_t tempty, int lane) {
   constexpr int COLS = BN / 2;
   uint32_t packed[COLS / 2];
 #pragma unroll
@@ -202,28 +201,31 @@ __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc,
     d[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
 }
 
-// Gate-up tile: accumulator columns [0,128) = gate j0.., [128,256) = up j0..
-// The thread owns 64 h columns (half hf).  It drains its 128 accumulator
-// columns into registers, releases the accumulator, then computes h in fp32 and
-// quantises and stores while the next tile's MMAs run.
+// Gate-up tile: accumulator columns [0, BN/2) = gate j0.., [BN/2, BN) = up j0..
+// (j0 = nt * BN/2).  The thread owns BN/4 h columns (half hf).  It drains its
+// accumulator columns into registers, releases the accumulator, then computes
+// h in fp32 and quantises and stores while the next tile's MMAs run.
+template <int BN>
 __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
-                                           int hf, uint64_t* tempty) {
+                                           int hf, uint32_t tempty) {
+  constexpr int HC = BN / 2;          // h columns per tile
+  constexpr int CH = HC / 64;         // 32-column chunks per thread
   const int64_t tok0 = tc.m0 + q * 32;
   const int64_t r = tok0 + lane;
   const float p = P.probs_perm[r];
   const int64_t I = P.I;
-  const int j0 = tc.nt * 128 + hf * 64;
+  const int j0 = tc.nt * HC + hf * (HC / 2);
   const bool save = P.gu_save != nullptr;
-  uint32_t g[2][32], u[2][32];
+  uint32_t g[CH][32], u[CH][32];
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    tmem_ld_32x32b_x32(tb + hf * 64 + c * 32, g[c]);
-    tmem_ld_32x32b_x32(tb + 128 + hf * 64 + c * 32, u[c]);
+  for (int c = 0; c < CH; ++c) {
+    tmem_ld_32x32b_x32(tb + hf * (HC / 2) + c * 32, g[c]);
+    tmem_ld_32x32b_x32(tb + HC + hf * (HC / 2) + c * 32, u[c]);
   }
   tmem_ld_wait();
   release_acc(tempty, lane);
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
+  for (int c = 0; c < CH; ++c) {
     const int64_t col = j0 + c * 32;
     float h[32];
 #pragma unroll
@@ -256,7 +258,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& t
 // Partial d(prob) sums go to dp_part[r][2*nt + hf].
 template <int BN>
 __device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
-                                            int hf, uint64_t* tempty, float* xp) {
+                                            int hf, uint32_t tempty, float* xp) {
   constexpr int COLS = BN / 2;
   const int64_t tok0 = tc.m0 + q * 32;
   const int64_t r = tok0 + lane;
@@ -294,10 +296,12 @@ __device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& 
   P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp;
 }
 
-template <int BN, int EPI, bool KG>
+template <int BN, int EPI, bool KG, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs P) {
-  using C = Cfg<BN, EPI>;
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, const GemmArgs P) {
+  using C = Cfg<BN, EPI, PAIR>;
+  constexpr int CG = C::CG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ctrl = smem + C::kStages * C::kStageBytes;
@@ -313,16 +317,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* xpose = reinterpret_cast<float*>(ctrl + C::kCtrlBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // In a CTA pair, rank 0 issues the MMAs for both CTAs; rank 1 feeds its half.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const int E = P.E;
   for (int i = threadIdx.x; i <= E; i += kThreads) s_poff[i] = P.poff[i];
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
+      // in a pair, rank 0's full barrier also counts the bytes rank 1's copies
+      // complete on it (rank 1's own full barriers are unused)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < C::kAcc; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 8);
+      mbar_init(&tempty[a], PAIR ? 16 : 8);
     }
     mbar_init(drained, 1);
     *abort_flag = 0;
@@ -332,35 +340,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (PAIR) {
+      tma_prefetch_desc(&tmSA);
+      tma_prefetch_desc(&tmSB);
+    }
   }
   __syncthreads();
 
-  // Group offsets must be 128-aligned, monotone and inside the capacity.
+  // Group offsets must be aligned to the tile height, monotone, inside capacity.
   bool ok = true;
   const int64_t cap = KG ? P.a_cols : P.M;
+  const int align = KG ? BK : C::kTileM;
   for (int e = 0; e < E; ++e) {
     const int a = s_poff[e], b = s_poff[e + 1];
-    if (a < 0 || (a & 127) || b < a) ok = false;
+    if (a < 0 || (a % align) || b < a) ok = false;
   }
-  if ((s_poff[E] & 127) || s_poff[E] > cap) ok = false;
+  if ((s_poff[E] % align) || s_poff[E] > cap) ok = false;
   if (!ok) {
     if (threadIdx.x == 0) report(P.status, MXG_ERR_OFFSETS);
     return;
   }
 
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+    tmem_alloc<CG>(tmem_slot, 512);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // both CTAs' barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int ntn = (KG || EPI != EPI_SWIGLU) ? P.N / BN : P.I / 128;
-  const int mtn_kg = P.M / BM;
-  const int64_t total = KG ? static_cast<int64_t>(E) * mtn_kg * ntn : static_cast<int64_t>(s_poff[E] >> 7) * ntn;
+  const int ntn = KG ? P.N / BN : (EPI == EPI_SWIGLU ? P.I / (BN / 2) : P.N / BN);
+  const int mtn_kg = P.M / C::kTileM;
+  const int64_t total = KG ? static_cast<int64_t>(E) * mtn_kg * ntn
+                           : static_cast<int64_t>(s_poff[E] / C::kTileM) * ntn;
+  const int64_t tile0 = PAIR ? blockIdx.x / 2 : blockIdx.x;
+  const int64_t tstep = PAIR ? gridDim.x / 2 : gridDim.x;
 
+  // Tile t -> expert, this CTA's first row (m0), column tile, contraction range.
   auto decode = [&](int64_t t) {
     TileCoord tc;
     if (KG) {
@@ -370,23 +388,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t tpe = static_cast<int64_t>(mtn_kg) * ntn;
       tc.e = static_cast<int>(t / tpe);
       const int local = static_cast<int>(t - tc.e * tpe);
+      int mt;
       if (P.M >= P.N) {
-        tc.m0 = (local / ntn) * BM;
+        mt = local / ntn;
         tc.nt = local % ntn;
       } else {
         tc.nt = local / mtn_kg;
-        tc.m0 = (local % mtn_kg) * BM;
+        mt = local % mtn_kg;
       }
+      tc.m0 = mt * C::kTileM + static_cast<int>(rank) * BM;
       tc.kbeg = s_poff[tc.e];
       tc.num_k = (s_poff[tc.e + 1] - s_poff[tc.e]) / BK;
     } else {
       int e = 0;
-      while (e + 1 < E && static_cast<int64_t>(s_poff[e + 1] >> 7) * ntn <= t) ++e;
-      const int local = static_cast<int>(t - static_cast<int64_t>(s_poff[e] >> 7) * ntn);
-      const int mcount = (s_poff[e + 1] - s_poff[e]) >> 7;
+      while (e + 1 < E && static_cast<int64_t>(s_poff[e + 1] / C::kTileM) * ntn <= t) ++e;
+      const int local = static_cast<int>(t - static_cast<int64_t>(s_poff[e] / C::kTileM) * ntn);
+      const int mcount = (s_poff[e + 1] - s_poff[e]) / C::kTileM;
       tc.e = e;
       tc.nt = local / mcount;
-      tc.m0 = s_poff[e] + (local - tc.nt * mcount) * BM;
+      tc.m0 = s_poff[e] + (local - tc.nt * mcount) * C::kTileM + static_cast<int>(rank) * BM;
       tc.kbeg = 0;
       tc.num_k = P.K / BK;
     }
@@ -396,23 +416,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     report(P.status, MXG_ERR_TIMEOUT);
     *abort_flag = 1;
   };
+  // the barrier the epilogue releases accumulators on (rank 0's, in a pair)
+  const uint32_t tempty_base = PAIR ? map_to_rank(smem_u32(tempty), 0) : smem_u32(tempty);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool aborted = false;
-      for (int64_t t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
+      const uint32_t full0 = PAIR ? map_to_rank(smem_u32(full), 0) : 0u;   // rank 0's full barriers
+      for (int64_t t = tile0; t < total && !aborted; t += tstep) {
         const TileCoord tc = decode(t);
         const int a_row = tc.m0;
-        int b_row0, b_row1 = 0;
+        // b_row0: first B row this CTA loads; sfb_row: first row of the tile's
+        // scale-factor atoms (every CTA loads the whole tile's SFB)
+        int b_row0, b_row1 = 0, sfb_row;
         if (KG) {
-          b_row0 = tc.nt * BN;
+          sfb_row = tc.nt * BN;
+          b_row0 = sfb_row + static_cast<int>(rank) * C::kBRows;
         } else if (EPI == EPI_SWIGLU) {
-          b_row0 = tc.e * P.b_rows_per_expert + tc.nt * 128;
-          b_row1 = b_row0 + P.I;
+          const int hc = BN / 2;
+          b_row0 = tc.e * P.b_rows_per_expert + tc.nt * hc;      // gate rows
+          b_row1 = b_row0 + P.I;                                 // up rows
+          if (PAIR && rank == 1) b_row0 = b_row1;                // rank 1 holds the up half
+          // pairs: W_gate_up's scales are stored gate/up-interleaved per 64 rows,
+          // so the tile's 64 gate + 64 up rows form one 128-row scale atom
+          sfb_row = PAIR ? tc.e * P.b_rows_per_expert + tc.nt * BN : b_row0;
         } else {
-          b_row0 = tc.e * P.b_rows_per_expert + tc.nt * BN;
+          sfb_row = tc.e * P.b_rows_per_expert + tc.nt * BN;
+          b_row0 = sfb_row + static_cast<int>(rank) * C::kBRows;
         }
         for (int kb = 0; kb < tc.num_k; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, kWaitLimitNs)) {
@@ -426,17 +458,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sSfb = sSfa + C::kSfaBytes;
           const int kx = tc.kbeg + kb * BK;
           const int64_t kc = kx >> 7;
-          mbar_arrive_expect_tx(&full[stage], C::kTx);
-          tma_load_2d(sA, &tmA, kx, a_row, &full[stage]);
-          bulk_load(sSfa, P.sa + (kc * (P.a_rows >> 7) + (a_row >> 7)) * 512, 512, &full[stage]);
-          if (EPI == EPI_SWIGLU) {
-            tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
-            tma_load_2d(sB + 128 * BK, &tmB, kx, b_row1, &full[stage]);
-            bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (b_row0 >> 7)) * 512, 512, &full[stage]);
-            bulk_load(sSfb + 512, P.sb + (kc * (P.b_rows >> 7) + (b_row1 >> 7)) * 512, 512, &full[stage]);
+          if (PAIR) {
+            // scale atoms are rows of the scale tensors' maps (128 x u32 = 512 B)
+            const int sa_atom = static_cast<int>(kc * (P.a_rows >> 7) + (a_row >> 7));
+            const int sb_atom = static_cast<int>(kc * (P.b_rows >> 7) + (sfb_row >> 7));
+            if (rank == 0) {
+              mbar_arrive_expect_tx(&full[stage], 2 * C::kTx);   // both CTAs' bytes
+              tma_load_2d(sA, &tmA, kx, a_row, &full[stage]);
+              tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
+              tma_load_2d(sSfa, &tmSA, 0, sa_atom, &full[stage]);
+              tma_load_2d(sSfb, &tmSB, 0, sb_atom, &full[stage]);
+            } else {
+              const uint32_t bar0 = full0 + stage * 8;
+              tma_load_2d_pair(sA, &tmA, kx, a_row, bar0);
+              tma_load_2d_pair(sB, &tmB, kx, b_row0, bar0);
+              tma_load_2d_pair(sSfa, &tmSA, 0, sa_atom, bar0);
+              tma_load_2d_pair(sSfb, &tmSB, 0, sb_atom, bar0);
+            }
           } else {
-            tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
-            bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (b_row0 >> 7)) * 512, BN * 4, &full[stage]);
+            mbar_arrive_expect_tx(&full[stage], C::kTx);
+            tma_load_2d(sA, &tmA, kx, a_row, &full[stage]);
+            bulk_load(sSfa, P.sa + (kc * (P.a_rows >> 7) + (a_row >> 7)) * 512, 512, &full[stage]);
+            if (EPI == EPI_SWIGLU) {
+              tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
+              tma_load_2d(sB + 128 * BK, &tmB, kx, b_row1, &full[stage]);
+              bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (b_row0 >> 7)) * 512, 512, &full[stage]);
+              bulk_load(sSfb + 512, P.sb + (kc * (P.b_rows >> 7) + (b_row1 >> 7)) * 512, 512, &full[stage]);
+            } else {
+              tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
+              bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (sfb_row >> 7)) * 512, BN * 4, &full[stage]);
+            }
           }
           if (++stage == C::kStages) {
             stage = 0;
@@ -451,22 +502,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       const uint32_t sfa_t = tmem + C::kSfaCol;
       const uint32_t sfb_t = tmem + C::kSfbCol;
       bool aborted = false;
-      for (int64_t t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
+      for (int64_t t = tile0; t < total && !aborted; t += tstep) {
         const TileCoord tc = decode(t);
         if (tc.num_k == 0) continue;
-        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, kWaitLimitNs)) {
+        const bool got = PAIR ? mbar_wait_bounded_cluster(&tempty[acc], acc_phase ^ 1, abort_flag, kWaitLimitNs)
+                              : mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, kWaitLimitNs);
+        if (!got) {
           fail();
           break;
         }
         tc_fence_after();
         const uint32_t d_t = tmem + acc * BN;
         for (int kb = 0; kb < tc.num_k; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+          const bool in = PAIR ? mbar_wait_bounded_cluster(&full[stage], phase, abort_flag, kWaitLimitNs)
+                               : mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitLimitNs);
+          if (!in) {
             fail();
             aborted = true;
             break;
@@ -476,31 +531,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sB = sA + C::kABytes;
           uint8_t* sSfa = sB + C::kBBytes;
           uint8_t* sSfb = sSfa + C::kSfaBytes;
-          tmem_cp_32x128b_warpx4(sfa_t, smem_desc(smem_u32(sSfa), 0, 128, kLayoutNone));
+          tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc(smem_u32(sSfa), 0, 128, kLayoutNone));
 #pragma unroll
           for (int i = 0; i < BN / 128; ++i)
-            tmem_cp_32x128b_warpx4(sfb_t + 4 * i, smem_desc(smem_u32(sSfb + 512 * i), 0, 128, kLayoutNone));
+            tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * i, smem_desc(smem_u32(sSfb + 512 * i), 0, 128, kLayoutNone));
           const uint64_t adesc = smem_desc(smem_u32(sA), 0, 1024, kLayoutSwizzle128B);
           const uint64_t bdesc = smem_desc(smem_u32(sB), 0, 1024, kLayoutSwizzle128B);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
-            mma_mxf8(d_t, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8_e4m3(BM, BN, k, k), sfa_t, sfb_t,
-                     (kb | k) != 0 ? 1u : 0u);
-          mma_commit(&empty[stage]);
+            mma_mxf8<CG>(d_t, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8_e4m3(C::kTileM, BN, k, k), sfa_t, sfb_t,
+                         (kb | k) != 0 ? 1u : 0u);
+          mma_commit<CG>(&empty[stage]);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (aborted) break;
-        mma_commit(&tfull[acc]);
+        mma_commit<CG>(&tfull[acc]);
         if (++acc == C::kAcc) {
           acc = 0;
           acc_phase ^= 1;
         }
       }
       // all MMAs issued by this thread are complete before TMEM is released
-      mma_commit(drained);
+      mma_commit<CG>(drained);
       mbar_wait_bounded(drained, 0, never_set, kWaitLimitNs);
     }
   } else if (warp >= 4) {
@@ -508,10 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warps 4..11: TMEM lane quadrant q = warp % 4, column half hf.
     const int q = warp & 3;
     const int hf = (warp - 4) >> 2;
-    float* my_xpose = xpose + (warp - 4) * 32 * 33;
     const int row = q * 32 + lane;
+    float* my_xpose = xpose + (warp - 4) * 32 * 33;
     uint32_t acc = 0, acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int64_t t = tile0; t < total; t += tstep) {
       const TileCoord tc = decode(t);
       if (tc.num_k == 0) {
         // token-grouped tile of an expert without tokens: exact zeros
@@ -529,12 +584,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const uint32_t rel = tempty_base + acc * 8;
       if (EPI == EPI_SWIGLU) {
-        epi_swiglu(P, tc, tb, q, lane, hf, &tempty[acc]);
+        epi_swiglu<BN>(P, tc, tb, q, lane, hf, rel);
       } else if (EPI == EPI_DSWIGLU) {
-        epi_dswiglu<BN>(P, tc, tb, q, lane, hf, &tempty[acc], my_xpose);
+        epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
       } else {
-        epi_bf16<BN, KG>(P, tc, tb, row, hf, &tempty[acc], lane);
+        epi_bf16<BN, KG>(P, tc, tb, row, hf, rel, lane);
       }
       if (++acc == C::kAcc) {
         acc = 0;
@@ -545,8 +601,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer is done with the pair's TMEM too
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1) tmem_dealloc<CG>(tmem, 512);
 }
 
 // ------------------------------------------------------------------- host
@@ -582,6 +639,19 @@ bool encode_u8(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, uin
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [atoms][128] uint32 view of a tensor-core scale buffer (512-byte atoms).
+bool encode_atoms(CUtensorMap* m, const void* base, int64_t atoms) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(atoms)};
+  const cuuint64_t strides[1] = {512};
+  const cuuint32_t box[2] = {128, 1};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -589,19 +659,42 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int BN, int EPI, bool KG>
+template <int BN, int EPI, bool KG, bool PAIR>
 cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
+  using C = Cfg<BN, EPI, PAIR>;
   CUtensorMap ta, tb;
+  const int b_box = (EPI == EPI_SWIGLU && !PAIR) ? 128 : C::kBRows;
   if (!encode_u8(&ta, g.a, g.a_cols, g.a_rows, BK, BM)) return cudaErrorInvalidValue;
-  if (!encode_u8(&tb, g.b, g.b_cols, g.b_rows, BK, EPI == EPI_SWIGLU ? 128 : BN)) return cudaErrorInvalidValue;
-  auto kern = gemm_kernel<BN, EPI, KG>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN, EPI>::kSmem);
+  if (!encode_u8(&tb, g.b, g.b_cols, g.b_rows, BK, b_box)) return cudaErrorInvalidValue;
+  auto kern = gemm_kernel<BN, EPI, KG, PAIR>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (err != cudaSuccess) return err;
-  int64_t grid = num_sms();
-  if (g.tiles_upper < grid) grid = g.tiles_upper;
-  if (grid < 1) grid = 1;
-  kern<<<static_cast<unsigned>(grid), kThreads, Cfg<BN, EPI>::kSmem, s>>>(ta, tb, g);
+  const int64_t units = PAIR ? num_sms() / 2 : num_sms();     // CTAs, or CTA pairs
+  int64_t n = g.tiles_upper < units ? g.tiles_upper : units;
+  if (n < 1) n = 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? 2 * n : n));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  // scale tensors as rows of 512-byte atoms, for the CTA pair's TMA loads
+  CUtensorMap tsa = ta, tsb = tb;
+  if (PAIR) {
+    if (!encode_atoms(&tsa, g.sa, (g.a_rows / 128) * (g.a_cols / 128))) return cudaErrorInvalidValue;
+    if (!encode_atoms(&tsb, g.sb, (g.b_rows / 128) * (g.b_cols / 128))) return cudaErrorInvalidValue;
+  }
+  err = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, g);
   count_launch();
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -618,11 +711,18 @@ int gemm_pick_bn(int epi, int N) {
 int dswiglu_partials(int I) { return 2 * (I / gemm_pick_bn(EPI_DSWIGLU, I)); }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
+  if (g.pair) {  // CTA-pair tiles, 256 x 128
+    if (g.epi == EPI_SWIGLU) return launch_impl<128, EPI_SWIGLU, false, true>(g, s);
+    if (g.epi == EPI_DSWIGLU) return launch_impl<128, EPI_DSWIGLU, false, true>(g, s);
+    if (g.kgroup) return launch_impl<128, EPI_BF16, true, true>(g, s);
+    return launch_impl<128, EPI_BF16, false, true>(g, s);
+  }
   const int bn = gemm_pick_bn(g.epi, g.epi == EPI_DSWIGLU ? g.I : g.N);
-  if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false>(g, s);
-  if (g.epi == EPI_DSWIGLU) return launch_impl<128, EPI_DSWIGLU, false>(g, s);
-  if (g.kgroup) return bn == 256 ? launch_impl<256, EPI_BF16, true>(g, s) : launch_impl<128, EPI_BF16, true>(g, s);
-  return bn == 256 ? launch_impl<256, EPI_BF16, false>(g, s) : launch_impl<128, EPI_BF16, false>(g, s);
+  if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, false>(g, s);
+  if (g.epi == EPI_DSWIGLU) return launch_impl<128, EPI_DSWIGLU, false, false>(g, s);
+  if (g.kgroup)
+    return bn == 256 ? launch_impl<256, EPI_BF16, true, false>(g, s) : launch_impl<128, EPI_BF16, true, false>(g, s);
+  return bn == 256 ? launch_impl<256, EPI_BF16, false, false>(g, s) : launch_impl<128, EPI_BF16, false, false>(g, s);
 }
 
 }  // namespace mxg

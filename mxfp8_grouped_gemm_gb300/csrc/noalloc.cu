@@ -79,6 +79,7 @@ extern "C" int mxg_route_permute_noalloc(const int32_t* ids, int T, int k, int E
   p.bases = scratch + static_cast<int64_t>(nblk) * E;
   p.offsets = scratch + 2 * static_cast<int64_t>(nblk) * E;
   p.padded_offsets = padded_offsets;
+  p.pad = 128;
   p.split_sizes = split_sizes;
   p.src_of_row = src_of_row;
   p.row_of_src = row_of_src;

@@ -72,7 +72,14 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
     uint4* dst = reinterpret_cast<uint4*>(P.q_row + grow * P.cols + c0 + j * 32);
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    P.s_row[sf_offset(P.layout, grow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5)] = static_cast<uint8_t>(sb);
+    int64_t srow = grow;
+    if (P.sf_row_interleave > 0) {
+      const int half = P.sf_row_interleave;
+      const int lr = p0 + r;
+      const int jj = lr % half;
+      srow = static_cast<int64_t>(b) * P.rows + (jj / 64) * 128 + (lr / half) * 64 + (jj % 64);
+    }
+    P.s_row[sf_offset(P.layout, srow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5)] = static_cast<uint8_t>(sb);
   }
 
   if (P.q_col != nullptr) {

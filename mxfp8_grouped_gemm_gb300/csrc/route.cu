@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kThreads) count_kernel(const PermuteParams P) 
   for (int e = threadIdx.x; e < P.E; e += kThreads) P.counts[blockIdx.x * P.E + e] = hist[e];
 }
 
-// One CTA: per-expert totals, exclusive scans (plain and 128-padded) and the
+// One CTA: per-expert totals, exclusive scans (plain and padded) and the
 // per-(chunk, expert) starting rows.
 __global__ void __launch_bounds__(kThreads) scan_kernel(const PermuteParams P, int nblk) {
   __shared__ int tot[kMaxE];
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const PermuteParams P, i
     poff[0] = 0;
     for (int e = 0; e < P.E; ++e) {
       off[e + 1] = off[e] + tot[e];
-      poff[e + 1] = poff[e] + ((tot[e] + 127) & ~127);
+      poff[e + 1] = poff[e] + (tot[e] + P.pad - 1) / P.pad * P.pad;
     }
   }
   __syncthreads();

@@ -63,5 +63,4 @@ class GroupedMLP:
         return self.saved[off:off + 4 * (self.E + 1)].view(torch.int32)
 
     def padded_rows_capacity(self) -> int:
-        R = self.T * self.k
-        return (R + 127) // 128 * 128 + 128 * self.E
+        return _lib.mxg_mlp_row_capacity(self.T, self.k, self.E)

@@ -82,12 +82,13 @@ def route_topk(logits: np.ndarray, k: int):
     return ids, probs
 
 
-def permute(ids: np.ndarray, E: int) -> dict:
+def permute(ids: np.ndarray, E: int, pad: int = PAD) -> dict:
     """Counting sort of flat index f = t*k + j by expert id, stable in f.
 
     Returns split_sizes[E], offsets[E+1] (exclusive scan), padded_offsets[E+1]
-    (each group rounded up to a multiple of 128 rows), src_of_row[R] (flat index
-    feeding permuted row r) and row_of_src[R] (its inverse).
+    (each group rounded up to a multiple of ``pad`` rows: a layout of the
+    grouped kernels, not part of the method), src_of_row[R] (flat index feeding
+    permuted row r) and row_of_src[R] (its inverse).
     """
     flat = np.asarray(ids, dtype=np.int64).reshape(-1)
     R = flat.size
@@ -98,7 +99,7 @@ def permute(ids: np.ndarray, E: int) -> dict:
     padded = np.zeros(E + 1, dtype=np.int64)
     for e in range(E):                     # exclusive scans
         offsets[e + 1] = offsets[e] + split[e]
-        padded[e + 1] = padded[e] + (split[e] + PAD - 1) // PAD * PAD
+        padded[e + 1] = padded[e] + (split[e] + pad - 1) // pad * pad
     cursor = offsets[:E].copy()
     src_of_row = np.empty(R, dtype=np.int64)
     row_of_src = np.empty(R, dtype=np.int64)

@@ -113,6 +113,9 @@ def test_mlp_sizes_and_validation(L):
     assert m.mxg_mlp_saved_bytes(256, 100, 256, 4, 2) == 0          # H % 128
     assert m.mxg_mlp_saved_bytes(256, 128, 256, 4, 5) == 0          # k > E
     assert m.mxg_mlp_saved_bytes(512, 128, 256, 4, 2) > m.mxg_mlp_saved_bytes(256, 128, 256, 4, 2)
+    align = m.mxg_mlp_group_align()
+    assert align in (128, 256)
+    assert m.mxg_mlp_row_capacity(300, 2, 6) == (600 + align - 1) // align * align + align * 6
     args = m.MlpFwdArgs(256, 128, 256, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, FAKE,
                         1 << 40, 1, FAKE)
     bad = m.MlpFwdArgs.from_buffer_copy(args)

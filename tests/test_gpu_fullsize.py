@@ -64,7 +64,7 @@ def test_fullsize_sampled(name, pool):
     # --- integer outputs, in full
     ids, probs = moe.route_topk(inp["logits"].numpy(), k)
     assert np.array_equal(np_(ids_g), ids)
-    perm = moe.permute(ids, E)
+    perm = moe.permute(ids, E, pad=m.mxg_mlp_group_align())
     split = perm["split_sizes"]
     assert np.array_equal(np_(layer.split_sizes), split)
     assert np.array_equal(np_(poff_g), perm["padded_offsets"])

@@ -65,11 +65,12 @@ def test_mlp_fwd_bwd_matches_oracle(name):
 
     assert np.array_equal(got["ids"], ids)
     assert np.array_equal(got["split"], perm["split_sizes"])
-    assert np.array_equal(got["poff"], perm["padded_offsets"])
+    poff = moe.permute(ids, E, pad=m.mxg_mlp_group_align())["padded_offsets"]
+    assert np.array_equal(got["poff"], poff)
 
     # gate-up output (before the activation), in the padded row layout
     e_of_row = np.repeat(np.arange(E), perm["split_sizes"])
-    prow = perm["padded_offsets"][e_of_row] + (np.arange(T * k) - perm["offsets"][e_of_row])
+    prow = poff[e_of_row] + (np.arange(T * k) - perm["offsets"][e_of_row])
     assert_rel_close(got["gu"][prow], ctx["gu"], tol=1e-2, floor=1.0, name="gate-up")
 
     report = {}

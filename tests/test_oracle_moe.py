@@ -59,6 +59,11 @@ def test_permute_matches_stable_argsort(E, k):
     assert np.all(p["padded_offsets"] % 128 == 0)
     pads = np.diff(p["padded_offsets"])
     assert np.all((pads >= p["split_sizes"]) & (pads < p["split_sizes"] + 128))
+    p256 = moe.permute(ids, E, pad=256)
+    pads = np.diff(p256["padded_offsets"])
+    assert np.all(p256["padded_offsets"] % 256 == 0)
+    assert np.all((pads >= p["split_sizes"]) & (pads < p["split_sizes"] + 256))
+    np.testing.assert_array_equal(p256["src_of_row"], p["src_of_row"])
 
 
 def _exact_dot(qa, sa, qb, sb):
