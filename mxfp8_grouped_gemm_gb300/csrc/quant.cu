@@ -17,98 +17,128 @@ namespace {
 
 constexpr int kRows = 32;    // rows per CTA tile (one column-wise block)
 constexpr int kCols = 128;   // columns per CTA tile (four row-wise blocks)
-constexpr int kPad = 8;      // smem row padding (bf16 elements)
 
-__global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
-  __shared__ __align__(16) uint16_t tile[kRows][kCols + kPad];
-  const int p0 = blockIdx.x * kRows;
-  const int c0 = blockIdx.y * kCols;
-  const int b = blockIdx.z;
-  const int tid = threadIdx.x;
-  if (P.rows_valid != nullptr && p0 >= *P.rows_valid) return;
+__device__ __forceinline__ void quant_store32(float (&v)[32], uint8_t* dst, uint8_t* sdst) {
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
+  const uint32_t sb = mx_scale_byte(amax);
+  const float inv = mx_inv_scale(sb);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] *= inv;
+  uint32_t w[8];
+  encode32(v, w);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  *sdst = static_cast<uint8_t>(sb);
+}
 
-  const uint16_t* xb = P.x + static_cast<int64_t>(b) * P.x_batch_stride;
-  // 32 rows x 128 bf16 = 512 vectors of 16 bytes
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gsrc)
+               : "memory");
+}
+
+constexpr int kTilesPerCta = 4;      // 32-row tiles walked by one CTA
+constexpr int kStride = kCols + 8;   // bf16 per smem row (272 bytes: 16-byte aligned, spreads banks)
+
+// Stage one 32 x 128 tile (gathered rows) into shared memory asynchronously.
+__device__ __forceinline__ void stage_tile(const QuantParams& P, const uint16_t* xb, int p0, int c0, uint16_t* buf,
+                                           int tid) {
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const int i = tid + it * 128;
-    const int r = i >> 4, v = i & 15;
-    const int p = p0 + r;
-    int64_t srow = p;
+    const int rr = i >> 4, vv = i & 15;
+    const int pp = p0 + rr;
+    int64_t srow = pp;
     bool zero = false;
     if (P.src_rows != nullptr) {
-      const int f = P.src_rows[p];
+      const int f = P.src_rows[pp];
       if (f < 0) zero = true;
       else srow = f / P.src_div;
     }
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (!zero) val = *reinterpret_cast<const uint4*>(xb + srow * P.ld_x + c0 + v * 8);
-    *reinterpret_cast<uint4*>(&tile[r][v * 8]) = val;
+    uint16_t* dst = buf + rr * kStride + vv * 8;
+    if (zero) *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    else cp_async16(dst, xb + srow * P.ld_x + c0 + vv * 8);
   }
-  if (P.probs_perm != nullptr && blockIdx.y == 0 && b == 0 && tid < kRows) {
-    const int p = p0 + tid;
-    const int f = P.src_rows != nullptr ? P.src_rows[p] : p;
-    P.probs_perm[p] = f < 0 ? 0.f : P.probs[f];
-  }
-  __syncthreads();
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
 
-  if (P.q_row != nullptr) {
-    // thread -> (row r, 32-column block j)
-    const int r = tid >> 2, j = tid & 3;
-    float v[32];
-    uint32_t amax = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      v[i] = bf16_bits_to_float(tile[r][j * 32 + i]);
-      amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
-    }
-    const uint32_t sb = mx_scale_byte(amax);
-    const float inv = mx_inv_scale(sb);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= inv;
-    uint32_t w[8];
-    encode32(v, w);
-    const int64_t grow = static_cast<int64_t>(b) * P.rows + p0 + r;
-    uint4* dst = reinterpret_cast<uint4*>(P.q_row + grow * P.cols + c0 + j * 32);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    int64_t srow = grow;
-    if (P.sf_row_interleave > 0) {
-      const int half = P.sf_row_interleave;
-      const int lr = p0 + r;
-      const int jj = lr % half;
-      srow = static_cast<int64_t>(b) * P.rows + (jj / 64) * 128 + (lr / half) * 64 + (jj % 64);
-    }
-    P.s_row[sf_offset(P.layout, srow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5)] = static_cast<uint8_t>(sb);
-  }
+// One CTA walks kTilesPerCta tiles of 32 rows x 128 columns, loading tile t+1
+// (asynchronous 16-byte copies into the other shared buffer) while it
+// quantises tile t.  Row-wise: thread t quantises the 32-value block (row t/4,
+// columns 32*(t%4)..) read back with 16-byte loads.  Column-wise: thread t
+// quantises column t over the tile's 32 rows.
+__global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
+  __shared__ __align__(16) uint16_t tile[2][kRows * kStride];
+  const int c0 = blockIdx.y * kCols;
+  const int b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int first = blockIdx.x * kTilesPerCta * kRows;
+  int limit = P.rows;
+  if (P.rows_valid != nullptr) limit = min(limit, *P.rows_valid);
+  const int ntiles = min(kTilesPerCta, (limit - first + kRows - 1) / kRows);
+  if (ntiles <= 0) return;
+  const uint16_t* xb = P.x + static_cast<int64_t>(b) * P.x_batch_stride;
 
-  if (P.q_col != nullptr) {
-    // thread -> column c0 + tid, the 32 rows of this tile form one block
-    float v[32];
-    uint32_t amax = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      v[i] = bf16_bits_to_float(tile[i][tid]);
-      amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
+  stage_tile(P, xb, first, c0, tile[0], tid);
+  for (int t = 0; t < ntiles; ++t) {
+    const int p0 = first + t * kRows;
+    if (t + 1 < ntiles) {
+      stage_tile(P, xb, p0 + kRows, c0, tile[(t + 1) & 1], tid);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
-    const uint32_t sb = mx_scale_byte(amax);
-    const float inv = mx_inv_scale(sb);
+    __syncthreads();
+    const uint16_t* buf = tile[t & 1];
+    if (P.probs_perm != nullptr && blockIdx.y == 0 && b == 0 && tid < kRows) {
+      const int pp = p0 + tid;
+      const int f = P.src_rows != nullptr ? P.src_rows[pp] : pp;
+      P.probs_perm[pp] = f < 0 ? 0.f : P.probs[f];
+    }
+    if (P.q_row != nullptr) {
+      const int r = tid >> 2, j = tid & 3;
+      const int p = p0 + r;
+      float v[32];
+      const uint4* s4 = reinterpret_cast<const uint4*>(buf + r * kStride + j * 32);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= inv;
-    uint32_t w[8];
-    encode32(v, w);
-    const int64_t gcol = static_cast<int64_t>(b) * P.cols + c0 + tid;
-    uint4* dst = reinterpret_cast<uint4*>(P.q_col + gcol * P.ld_col + p0);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    P.s_col[sf_offset(P.layout, gcol, p0 >> 5, P.sf_col_rows, P.ld_col >> 5)] = static_cast<uint8_t>(sb);
+      for (int i = 0; i < 4; ++i) {
+        const uint4 q = s4[i];
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          v[8 * i + 2 * h] = __uint_as_float(w[h] << 16);
+          v[8 * i + 2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
+        }
+      }
+      const int64_t grow = static_cast<int64_t>(b) * P.rows + p;
+      int64_t sfrow = grow;
+      if (P.sf_row_interleave > 0) {
+        const int half = P.sf_row_interleave;
+        const int jj = p % half;
+        sfrow = static_cast<int64_t>(b) * P.rows + (jj / 64) * 128 + (p / half) * 64 + (jj % 64);
+      }
+      quant_store32(v, P.q_row + grow * P.cols + c0 + j * 32,
+                    P.s_row + sf_offset(P.layout, sfrow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5));
+    }
+    if (P.q_col != nullptr) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = bf16_bits_to_float(buf[i * kStride + tid]);
+      const int64_t gcol = static_cast<int64_t>(b) * P.cols + c0 + tid;
+      quant_store32(v, P.q_col + gcol * P.ld_col + p0,
+                    P.s_col + sf_offset(P.layout, gcol, p0 >> 5, P.sf_col_rows, P.ld_col >> 5));
+    }
+    __syncthreads();   // buffer t&1 is refilled two tiles later
   }
 }
 
 }  // namespace
 
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s) {
-  dim3 grid(p.rows / kRows, p.cols / kCols, p.batch);
+  dim3 grid((p.rows / kRows + kTilesPerCta - 1) / kTilesPerCta, p.cols / kCols, p.batch);
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
   quant_kernel<<<grid, 128, 0, s>>>(p);
   count_launch();

@@ -29,17 +29,19 @@ class GroupedMLP:
         self.dprobs = torch.empty((T, k), dtype=torch.float32, device=self.device)
 
     def route(self, logits, stream=None):
+        """Top-k routing into this object's ids/probs buffers."""
         return _lib.mxg_route_topk(logits, self.k, self.ids, self.probs, stream=stream)
 
-    def forward(self, x, ids, probs, w_gate_up, w_down, save_for_backward=True, stream=None, stage=None):
+    def forward(self, x, ids, probs, w_gate_up, w_down, save_for_backward=True, stream=None, stage=None, y=None):
         return _lib.mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, self.saved, self.workspace,
-                                        self.dev_status, y=self.y, split_sizes=self.split_sizes,
-                                        save_for_backward=save_for_backward, stream=stream, stage=stage)
+                                        self.dev_status, y=self.y if y is None else y,
+                                        split_sizes=self.split_sizes, save_for_backward=save_for_backward,
+                                        stream=stream, stage=stage)
 
-    def backward(self, dy, stream=None, stage=None):
+    def backward(self, dy, stream=None, stage=None, dx=None):
         return _lib.mxg_grouped_mlp_bwd(dy, self.saved, self.workspace, self.dev_status, self.E, self.I, self.k,
-                                        dx=self.dx, dw_gate_up=self.dw_gate_up, dw_down=self.dw_down,
-                                        dprobs=self.dprobs, stream=stream, stage=stage)
+                                        dx=self.dx if dx is None else dx, dw_gate_up=self.dw_gate_up,
+                                        dw_down=self.dw_down, dprobs=self.dprobs, stream=stream, stage=stage)
 
     def step(self, logits, x, w_gate_up, w_down, dy, stream=None):
         """One pass of the whole path: route, forward (saving for backward), backward."""
