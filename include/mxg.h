@@ -163,6 +163,17 @@ int mxg_grouped_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, cons
                      const int32_t* padded_offsets, int E, int m_cap, int N, int K, uint16_t* d,
                      int32_t* dev_status, void* stream);
 
+/* Test hook for failure detection (no counterpart in the paper): runs
+ * mxg_grouped_gemm with every kernel wait bounded by `wait_limit_ns` and a
+ * producer that never issues its copies, so the first wait of the MMA warp
+ * runs out.  The kernel then records MXG_ERR_TIMEOUT in dev_status, stops,
+ * waits for its own work, frees its tensor memory and returns; the CUDA
+ * context stays usable.  `d` is left unwritten.  Same argument rules as
+ * mxg_grouped_gemm; wait_limit_ns must be non-zero. */
+int mxg_debug_grouped_gemm_stall(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                                 const int32_t* padded_offsets, int E, int m_cap, int N, int K, uint16_t* d,
+                                 uint64_t wait_limit_ns, int32_t* dev_status, void* stream);
+
 /* Grouped MXFP8 GEMM, contraction-grouped (the weight-gradient shape): for
  * each expert e, D_e[m][n] = sum over tokens t in [padded_offsets[e],
  * padded_offsets[e+1]) of deq(A)[m][t] * deq(B)[n][t].  A and B are stored

@@ -29,7 +29,7 @@ EXPORTS = [
     "mxg_grouped_gemm_wgrad", "mxg_mlp_saved_bytes", "mxg_mlp_workspace_bytes", "mxg_grouped_mlp_fwd",
     "mxg_grouped_mlp_bwd", "mxg_mlp_saved_view", "mxg_grouped_mlp_fwd_stage", "mxg_grouped_mlp_bwd_stage",
     "mxg_route_permute_noalloc_max_entries", "mxg_route_permute_noalloc", "mxg_mlp_group_align",
-    "mxg_mlp_row_capacity",
+    "mxg_mlp_row_capacity", "mxg_debug_grouped_gemm_stall",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
         "mxg_mxfp8_quantize": (I32, [P, I32, I32, P, P, P, P, I32, P]),
         "mxg_grouped_gemm": (I32, [P, P, P, P, P, I32, I32, I32, I32, P, P, P]),
         "mxg_grouped_gemm_wgrad": (I32, [P, P, P, P, P, I32, I32, I32, I32, P, P, P]),
+        "mxg_debug_grouped_gemm_stall": (I32, [P, P, P, P, P, I32, I32, I32, I32, P, U64, P, P]),
         "mxg_mlp_saved_bytes": (SZ, [I32, I32, I32, I32, I32]),
         "mxg_mlp_group_align": (I32, []),
         "mxg_mlp_row_capacity": (SZ, [I32, I32, I32]),

@@ -263,6 +263,40 @@ int mxg_grouped_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, cons
   return cuda_status(launch_gemm(g, static_cast<cudaStream_t>(stream)));
 }
 
+int mxg_debug_grouped_gemm_stall(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                                  const int32_t* padded_offsets, int E, int m_cap, int N, int K, uint16_t* d,
+                                  uint64_t wait_limit_ns, int32_t* dev_status, void* stream) {
+  if (!a || !sa || !b || !sb || !padded_offsets || !d || !dev_status) return MXG_ERR_ARG;
+  if (E <= 0 || m_cap <= 0 || N <= 0 || K <= 0 || wait_limit_ns == 0) return MXG_ERR_ARG;
+  if (E > 256 || K % 128 || N % 128 || m_cap % 128) return MXG_ERR_SHAPE;
+  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(d) ||
+      !aligned16(padded_offsets))
+    return MXG_ERR_ALIGN;
+  GemmArgs g{};
+  g.epi = EPI_BF16;
+  g.a = a;
+  g.sa = sa;
+  g.a_rows = m_cap;
+  g.a_cols = K;
+  g.b = b;
+  g.sb = sb;
+  g.b_rows = static_cast<int64_t>(E) * N;
+  g.b_cols = K;
+  g.poff = padded_offsets;
+  g.E = E;
+  g.M = m_cap;
+  g.N = N;
+  g.K = K;
+  g.b_rows_per_expert = N;
+  g.d = d;
+  g.ldd = N;
+  g.status = dev_status;
+  g.tiles_upper = static_cast<int64_t>(m_cap / 128) * (N / gemm_pick_bn(EPI_BF16, N));
+  g.wait_limit_ns = wait_limit_ns;
+  g.debug_stall = 1;
+  return cuda_status(launch_gemm(g, static_cast<cudaStream_t>(stream)));
+}
+
 int mxg_grouped_gemm_wgrad(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                            const int32_t* padded_offsets, int E, int M, int N, int t_cap, uint16_t* d,
                            int32_t* dev_status, void* stream) {

@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* xpose = reinterpret_cast<float*>(ctrl + C::kCtrlBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t limit_ns = P.wait_limit_ns != 0 ? P.wait_limit_ns : kWaitLimitNs;
   // In a CTA pair, rank 0 issues the MMAs for both CTAs; rank 1 feeds its half.
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const int E = P.E;
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && P.debug_stall == 0) {
       uint32_t stage = 0, phase = 0;
       bool aborted = false;
       const uint32_t full0 = PAIR ? map_to_rank(smem_u32(full), 0) : 0u;   // rank 0's full barriers
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           b_row0 = sfb_row + static_cast<int>(rank) * C::kBRows;
         }
         for (int kb = 0; kb < tc.num_k; ++kb) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, kWaitLimitNs)) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, limit_ns)) {
             fail();
             aborted = true;
             break;
@@ -510,8 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t t = tile0; t < total && !aborted; t += tstep) {
         const TileCoord tc = decode(t);
         if (tc.num_k == 0) continue;
-        const bool got = PAIR ? mbar_wait_bounded_cluster(&tempty[acc], acc_phase ^ 1, abort_flag, kWaitLimitNs)
-                              : mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, kWaitLimitNs);
+        const bool got = PAIR ? mbar_wait_bounded_cluster(&tempty[acc], acc_phase ^ 1, abort_flag, limit_ns)
+                              : mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, limit_ns);
         if (!got) {
           fail();
           break;
@@ -519,8 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_t = tmem + acc * BN;
         for (int kb = 0; kb < tc.num_k; ++kb) {
-          const bool in = PAIR ? mbar_wait_bounded_cluster(&full[stage], phase, abort_flag, kWaitLimitNs)
-                               : mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitLimitNs);
+          const bool in = PAIR ? mbar_wait_bounded_cluster(&full[stage], phase, abort_flag, limit_ns)
+                               : mbar_wait_bounded(&full[stage], phase, abort_flag, limit_ns);
           if (!in) {
             fail();
             aborted = true;
@@ -556,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // all MMAs issued by this thread are complete before TMEM is released
       mma_commit<CG>(drained);
-      mbar_wait_bounded(drained, 0, never_set, kWaitLimitNs);
+      mbar_wait_bounded(drained, 0, never_set, limit_ns);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
@@ -576,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN / 16; ++c) reinterpret_cast<uint4*>(drow)[c] = make_uint4(0u, 0u, 0u, 0u);
         continue;
       }
-      bool got = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, kWaitLimitNs);
+      bool got = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, limit_ns);
       got = __all_sync(0xffffffffu, got);
       if (!got) {
         if (lane == 0) fail();

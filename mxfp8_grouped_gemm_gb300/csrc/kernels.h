@@ -101,6 +101,8 @@ struct GemmArgs {
   int32_t dp_ld;
   int32_t* status;
   int64_t tiles_upper;        // host bound on the number of tiles (grid sizing)
+  uint64_t wait_limit_ns;     // bound on every wait inside the kernel (0: default)
+  int32_t debug_stall;        // test hook: the producer issues no copies
 };
 int gemm_pick_bn(int epi, int N);
 int dswiglu_partials(int I);   // d(prob) partial sums per row (two per column tile)

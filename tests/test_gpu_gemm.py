@@ -89,3 +89,32 @@ def test_grouped_gemm_wgrad(sizes, M, N):
             continue
         ref = A[:, t0:t1] @ B[:, t0:t1].T
         assert_rel_close(got[e], ref, tol=1e-2, floor=1.0, name=f"expert {e}")
+
+
+def test_kernel_wait_timeout_is_reported_and_context_survives():
+    """Failure detection without a fault: a producer that never issues its copies
+    makes the MMA warp's bounded wait run out; the kernel reports
+    MXG_ERR_TIMEOUT, frees its tensor memory and returns, and a normal GEMM
+    afterwards still gives correct results."""
+    m = require_gpu()
+    L = m.lib()
+    E, N, K = 1, 128, 256
+    poff = torch.tensor([0, 256], dtype=torch.int32, device="cuda")
+    a = synthetic.random_bf16((256, K), 11)
+    b = synthetic.random_bf16((N, K), 12)
+    qa, sa = _quant_mma(m, a)
+    qb, sb = _quant_mma(m, b)
+    d = torch.zeros((256, N), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = L.mxg_debug_grouped_gemm_stall(qa.data_ptr(), sa.data_ptr(), qb.data_ptr(), sb.data_ptr(), poff.data_ptr(),
+                                        E, 256, N, K, d.data_ptr(), 20_000_000, st.data_ptr(),
+                                        torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) == 18                                          # MXG_ERR_TIMEOUT
+    st.zero_()
+    m.mxg_grouped_gemm(qa, sa, qb, sb, poff, E, N, K, st, d=d)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = mx.fake_quant(a.double().numpy()) @ mx.fake_quant(b.double().numpy()).T
+    assert_rel_close(np_(d), ref, tol=1e-2, floor=1.0, name="after timeout")
