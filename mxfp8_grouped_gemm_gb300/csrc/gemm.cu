@@ -22,6 +22,9 @@
 //   EPI_DSWIGLU : dH tile -> dg = dH p u s (1 + g (1-s)), du = dH p g s
 //                 (s = sigmoid(g)), d(prob) partial sum_i dH g s u; dGU
 //                 quantised row-wise (dgrad A) and token-column-wise (wgrad A).
+//                 With BN = 256 the accumulator is single-buffered, so dH is
+//                 first drained to shared memory as bf16 and the accumulator
+//                 released; the math then overlaps the next tile's MMAs.
 //
 // CTA = 12 warps: warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs,
 // warps 4-11 run the epilogue (warp w reads TMEM lanes 32*(w%4)..+31, half of
@@ -59,7 +62,10 @@ struct Cfg {
   static constexpr uint32_t kTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStageBytes = (kTx + 1023) / 1024 * 1024;
   // per epilogue warp: a 32 x 33 fp32 tile for the column-wise quantiser (dSwiGLU)
-  static constexpr int kXposeBytes = EPI == 2 ? 8 * 32 * 33 * 4 : 0;
+  // dSwiGLU: BN = 256 stages the tile's dH as bf16 rows (padded to 264) so the
+  // accumulator is released before the epilogue math; BN = 128 keeps a 32 x 33
+  // fp32 transpose tile per epilogue warp for the column-wise quantiser
+  static constexpr int kXposeBytes = EPI == 2 ? (BN == 256 ? 128 * (256 + 8) * 2 : 8 * 32 * 33 * 4) : 0;
   static constexpr int kCtrlBytes = 2048;
   static constexpr int kStages = (232448 - 1024 - kCtrlBytes - kXposeBytes) / kStageBytes > 8
                                      ? 8
@@ -88,6 +94,19 @@ __device__ __forceinline__ void load_bf16_32(const uint16_t* src, float (&v)[32]
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint4 q = s[i];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = u2f(w[j] << 16);
+      v[8 * i + 2 * j + 1] = u2f(w[j] & 0xffff0000u);
+    }
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16_32(const uint4* src, float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 q = src[i];
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -292,6 +311,64 @@ __device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& 
     sb = row_quant32(u, P.q_out + r * P.q_out_ld + I + col);
     P.s_out[sf_mma_offset(r, (I + col) >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
     col_quant32_xpose(u, xp, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
+  }
+  P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp;
+}
+
+
+// BN = 256: drain the thread's 128 dH columns to a bf16 staging row in shared
+// memory, release the accumulator, then run the dSwiGLU epilogue from there.
+__device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q,
+                                                   int lane, int hf, uint32_t tempty, uint16_t* stage_base) {
+  constexpr int COLS = 128;
+  constexpr int STRIDE = 256 + 8;                 // bf16 per staging row
+  const int64_t tok0 = tc.m0 + q * 32;
+  const int64_t r = tok0 + lane;
+  uint16_t* srow = stage_base + (q * 32 + lane) * STRIDE + hf * COLS;
+#pragma unroll
+  for (int c = 0; c < COLS / 32; c += 2) {
+    uint32_t a0[32], a1[32];
+    tmem_ld_32x32b_x32(tb + hf * COLS + c * 32, a0);
+    tmem_ld_32x32b_x32(tb + hf * COLS + (c + 1) * 32, a1);
+    tmem_ld_wait();
+    uint4* d0 = reinterpret_cast<uint4*>(srow + c * 32);
+    uint4* d1 = reinterpret_cast<uint4*>(srow + (c + 1) * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      d0[i] = make_uint4(pack_bf16x2(u2f(a0[8 * i]), u2f(a0[8 * i + 1])), pack_bf16x2(u2f(a0[8 * i + 2]), u2f(a0[8 * i + 3])),
+                         pack_bf16x2(u2f(a0[8 * i + 4]), u2f(a0[8 * i + 5])), pack_bf16x2(u2f(a0[8 * i + 6]), u2f(a0[8 * i + 7])));
+      d1[i] = make_uint4(pack_bf16x2(u2f(a1[8 * i]), u2f(a1[8 * i + 1])), pack_bf16x2(u2f(a1[8 * i + 2]), u2f(a1[8 * i + 3])),
+                         pack_bf16x2(u2f(a1[8 * i + 4]), u2f(a1[8 * i + 5])), pack_bf16x2(u2f(a1[8 * i + 6]), u2f(a1[8 * i + 7])));
+    }
+  }
+  release_acc(tempty, lane);
+  const float p = P.probs_perm[r];
+  const int64_t I = P.I;
+  const int j0 = tc.nt * 256 + hf * COLS;
+  float dp = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < COLS / 32; ++c) {
+    const int64_t col = j0 + c * 32;
+    float dh[32], g[32], u[32], dg[32];
+    unpack_bf16_32(reinterpret_cast<const uint4*>(srow + c * 32), dh);
+    unpack_bf16_32(reinterpret_cast<const uint4*>(P.gu_save + r * (2 * I) + col), g);
+    unpack_bf16_32(reinterpret_cast<const uint4*>(P.gu_save + r * (2 * I) + I + col), u);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float gf = g[i], uf = u[i];
+      const float s = __fdividef(1.f, 1.f + __expf(-gf));
+      const float sl = gf * s;
+      const float a = dh[i] * p;
+      dg[i] = a * uf * s * (1.f + gf * (1.f - s));
+      u[i] = a * sl;
+      dp += dh[i] * sl * uf;
+    }
+    uint32_t sb = row_quant32(dg, P.q_out + r * P.q_out_ld + col);
+    P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
+    col_quant32(dg, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
+    sb = row_quant32(u, P.q_out + r * P.q_out_ld + I + col);
+    P.s_out[sf_mma_offset(r, (I + col) >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
+    col_quant32(u, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
   }
   P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp;
 }
@@ -589,7 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (EPI == EPI_SWIGLU) {
         epi_swiglu<BN>(P, tc, tb, q, lane, hf, rel);
       } else if (EPI == EPI_DSWIGLU) {
-        epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
+        if (BN == 256) epi_dswiglu_staged(P, tc, tb, q, lane, hf, rel, reinterpret_cast<uint16_t*>(xpose));
+        else epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
       } else {
         epi_bf16<BN, KG>(P, tc, tb, row, hf, rel, lane);
       }
@@ -703,9 +781,6 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
 
 int gemm_pick_bn(int epi, int N) {
   if (epi == EPI_SWIGLU) return 256;
-  // the dSwiGLU epilogue is heavier than a 128x256 mainloop: use 128-wide tiles,
-  // whose accumulators double-buffer in TMEM so the epilogue runs under the MMAs
-  if (epi == EPI_DSWIGLU) return 128;
   return N % 256 == 0 ? 256 : 128;
 }
 
@@ -720,7 +795,8 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
   }
   const int bn = gemm_pick_bn(g.epi, g.epi == EPI_DSWIGLU ? g.I : g.N);
   if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, false>(g, s);
-  if (g.epi == EPI_DSWIGLU) return launch_impl<128, EPI_DSWIGLU, false, false>(g, s);
+  if (g.epi == EPI_DSWIGLU)
+    return bn == 256 ? launch_impl<256, EPI_DSWIGLU, false, false>(g, s) : launch_impl<128, EPI_DSWIGLU, false, false>(g, s);
   if (g.kgroup)
     return bn == 256 ? launch_impl<256, EPI_BF16, true, false>(g, s) : launch_impl<128, EPI_BF16, true, false>(g, s);
   return bn == 256 ? launch_impl<256, EPI_BF16, false, false>(g, s) : launch_impl<128, EPI_BF16, false, false>(g, s);
