@@ -29,7 +29,9 @@
 // CTA = 12 warps: warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs,
 // warps 4-11 run the epilogue (warp w reads TMEM lanes 32*(w%4)..+31, half of
 // the tile's columns each).
-// Tile 128 x BN x 128 (BN = 256 or 128); 4/6-stage smem ring; the
+// Tile 128 x BN x 128 (BN = 256 or 128) on one SM, or 256 x 256 x 128 on a
+// CTA pair (cta_group::2: each SM holds its 128 rows of A and half of B, so
+// the operand bytes per MMA flop drop by a third); 4-8-stage smem ring; the
 // accumulator is double-buffered in TMEM when it fits next to the scale
 // factors (BN = 128).  Every wait is bounded; a wait that gives up records
 // MXG_ERR_TIMEOUT, stops the CTA's pipeline and still frees TMEM.
@@ -54,14 +56,13 @@ struct Cfg {
   static constexpr int CG = PAIR ? 2 : 1;
   static constexpr int kTileM = PAIR ? 2 * BM : BM;         // rows of one tile (both CTAs)
   static constexpr int kBRows = PAIR ? BN / 2 : BN;         // rows of B held by one CTA
-  static constexpr int kAcc = (PAIR || BN == 128) ? 2 : 1;  // accumulator buffers in TMEM
+  static constexpr int kAcc = BN == 128 ? 2 : 1;            // accumulator buffers in TMEM
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = kBRows * BK;
   static constexpr int kSfaBytes = BM * 4;                  // 128 rows x 4 blocks of 32
   static constexpr int kSfbBytes = BN * 4;                  // every CTA holds the tile's full SFB
   static constexpr uint32_t kTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStageBytes = (kTx + 1023) / 1024 * 1024;
-  // per epilogue warp: a 32 x 33 fp32 tile for the column-wise quantiser (dSwiGLU)
   // dSwiGLU: BN = 256 stages the tile's dH as bf16 rows (padded to 264) so the
   // accumulator is released before the epilogue math; BN = 128 keeps a 32 x 33
   // fp32 transpose tile per epilogue warp for the column-wise quantiser
@@ -75,7 +76,7 @@ struct Cfg {
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kCtrlBytes + kXposeBytes;
   static_assert(kSfbCol + BN / 32 <= 512, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
-  static_assert(!PAIR || BN == 128, "CTA-pair tiles are 256 x 128");
+  static_assert(!PAIR || BN == 256, "CTA-pair tiles are 256 x 256");
 };
 
 struct TileCoord {
@@ -506,23 +507,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t t = tile0; t < total && !aborted; t += tstep) {
         const TileCoord tc = decode(t);
         const int a_row = tc.m0;
-        // b_row0: first B row this CTA loads; sfb_row: first row of the tile's
-        // scale-factor atoms (every CTA loads the whole tile's SFB)
-        int b_row0, b_row1 = 0, sfb_row;
+        // b_row0: first B row this CTA loads (b_row1: the up rows of a gate-up
+        // tile); sfb0/sfb1: first rows of the tile's two 128-row scale atoms
+        // (BN = 256; every CTA of a pair loads both)
+        int b_row0, b_row1 = 0, sfb0, sfb1;
         if (KG) {
-          sfb_row = tc.nt * BN;
-          b_row0 = sfb_row + static_cast<int>(rank) * C::kBRows;
+          sfb0 = tc.nt * BN;
+          sfb1 = sfb0 + 128;
+          b_row0 = sfb0 + static_cast<int>(rank) * C::kBRows;
         } else if (EPI == EPI_SWIGLU) {
-          const int hc = BN / 2;
-          b_row0 = tc.e * P.b_rows_per_expert + tc.nt * hc;      // gate rows
-          b_row1 = b_row0 + P.I;                                 // up rows
-          if (PAIR && rank == 1) b_row0 = b_row1;                // rank 1 holds the up half
-          // pairs: W_gate_up's scales are stored gate/up-interleaved per 64 rows,
-          // so the tile's 64 gate + 64 up rows form one 128-row scale atom
-          sfb_row = PAIR ? tc.e * P.b_rows_per_expert + tc.nt * BN : b_row0;
+          sfb0 = tc.e * P.b_rows_per_expert + tc.nt * (BN / 2);  // gate rows
+          sfb1 = sfb0 + P.I;                                     // up rows
+          b_row0 = (PAIR && rank == 1) ? sfb1 : sfb0;             // in a pair, rank 1 holds the up half
+          b_row1 = sfb1;
         } else {
-          sfb_row = tc.e * P.b_rows_per_expert + tc.nt * BN;
-          b_row0 = sfb_row + static_cast<int>(rank) * C::kBRows;
+          sfb0 = tc.e * P.b_rows_per_expert + tc.nt * BN;
+          sfb1 = sfb0 + 128;
+          b_row0 = sfb0 + static_cast<int>(rank) * C::kBRows;
         }
         for (int kb = 0; kb < tc.num_k; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, limit_ns)) {
@@ -539,19 +540,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (PAIR) {
             // scale atoms are rows of the scale tensors' maps (128 x u32 = 512 B)
             const int sa_atom = static_cast<int>(kc * (P.a_rows >> 7) + (a_row >> 7));
-            const int sb_atom = static_cast<int>(kc * (P.b_rows >> 7) + (sfb_row >> 7));
+            const int sb_atom0 = static_cast<int>(kc * (P.b_rows >> 7) + (sfb0 >> 7));
+            const int sb_atom1 = static_cast<int>(kc * (P.b_rows >> 7) + (sfb1 >> 7));
             if (rank == 0) {
               mbar_arrive_expect_tx(&full[stage], 2 * C::kTx);   // both CTAs' bytes
               tma_load_2d(sA, &tmA, kx, a_row, &full[stage]);
               tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
               tma_load_2d(sSfa, &tmSA, 0, sa_atom, &full[stage]);
-              tma_load_2d(sSfb, &tmSB, 0, sb_atom, &full[stage]);
+              tma_load_2d(sSfb, &tmSB, 0, sb_atom0, &full[stage]);
+              tma_load_2d(sSfb + 512, &tmSB, 0, sb_atom1, &full[stage]);
             } else {
               const uint32_t bar0 = full0 + stage * 8;
               tma_load_2d_pair(sA, &tmA, kx, a_row, bar0);
               tma_load_2d_pair(sB, &tmB, kx, b_row0, bar0);
               tma_load_2d_pair(sSfa, &tmSA, 0, sa_atom, bar0);
-              tma_load_2d_pair(sSfb, &tmSB, 0, sb_atom, bar0);
+              tma_load_2d_pair(sSfb, &tmSB, 0, sb_atom0, bar0);
+              tma_load_2d_pair(sSfb + 512, &tmSB, 0, sb_atom1, bar0);
             }
           } else {
             mbar_arrive_expect_tx(&full[stage], C::kTx);
@@ -564,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               bulk_load(sSfb + 512, P.sb + (kc * (P.b_rows >> 7) + (b_row1 >> 7)) * 512, 512, &full[stage]);
             } else {
               tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
-              bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (sfb_row >> 7)) * 512, BN * 4, &full[stage]);
+              bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (sfb0 >> 7)) * 512, BN * 4, &full[stage]);
             }
           }
           if (++stage == C::kStages) {
@@ -787,11 +791,11 @@ int gemm_pick_bn(int epi, int N) {
 int dswiglu_partials(int I) { return 2 * (I / gemm_pick_bn(EPI_DSWIGLU, I)); }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
-  if (g.pair) {  // CTA-pair tiles, 256 x 128
-    if (g.epi == EPI_SWIGLU) return launch_impl<128, EPI_SWIGLU, false, true>(g, s);
-    if (g.epi == EPI_DSWIGLU) return launch_impl<128, EPI_DSWIGLU, false, true>(g, s);
-    if (g.kgroup) return launch_impl<128, EPI_BF16, true, true>(g, s);
-    return launch_impl<128, EPI_BF16, false, true>(g, s);
+  if (g.pair) {  // CTA-pair tiles, 256 x 256
+    if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, true>(g, s);
+    if (g.epi == EPI_DSWIGLU) return launch_impl<256, EPI_DSWIGLU, false, true>(g, s);
+    if (g.kgroup) return launch_impl<256, EPI_BF16, true, true>(g, s);
+    return launch_impl<256, EPI_BF16, false, true>(g, s);
   }
   const int bn = gemm_pick_bn(g.epi, g.epi == EPI_DSWIGLU ? g.I : g.N);
   if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, false>(g, s);

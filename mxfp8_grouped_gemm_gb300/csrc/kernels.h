@@ -29,10 +29,6 @@ struct QuantParams {
   int64_t ld_col;
   int64_t sf_col_rows;        // rows of the column-wise matrix (MMA layout)
   int32_t layout;             // MXG_LAYOUT_*
-  // >0: the row-wise scales of a gate/up weight ([2I][K] per batch, I = this
-  // value) are stored with gate and up rows interleaved in 64-row chunks, so a
-  // CTA-pair tile's 64 gate + 64 up rows share one 128-row scale atom
-  int32_t sf_row_interleave;
 };
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
 
@@ -69,7 +65,7 @@ enum Epi { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
 struct GemmArgs {
   int epi;
   bool kgroup;
-  bool pair;                  // CTA-pair 256 x 128 tiles (row groups 256-aligned)
+  bool pair;                  // CTA-pair 256 x 256 tiles (row groups 256-aligned)
   const uint8_t* a;           // codes
   const uint8_t* sa;
   int64_t a_rows;             // rows of the A matrix (SF layout, tensor map)

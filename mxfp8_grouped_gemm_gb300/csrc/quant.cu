@@ -114,14 +114,8 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
         }
       }
       const int64_t grow = static_cast<int64_t>(b) * P.rows + p;
-      int64_t sfrow = grow;
-      if (P.sf_row_interleave > 0) {
-        const int half = P.sf_row_interleave;
-        const int jj = p % half;
-        sfrow = static_cast<int64_t>(b) * P.rows + (jj / 64) * 128 + (p / half) * 64 + (jj % 64);
-      }
       quant_store32(v, P.q_row + grow * P.cols + c0 + j * 32,
-                    P.s_row + sf_offset(P.layout, sfrow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5));
+                    P.s_row + sf_offset(P.layout, grow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5));
     }
     if (P.q_col != nullptr) {
       float v[32];
