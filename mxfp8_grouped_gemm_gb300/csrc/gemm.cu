@@ -27,13 +27,14 @@
 //                 released; the math then overlaps the next tile's MMAs.
 //
 // CTA = 12 warps: warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs,
-// warps 4-11 run the epilogue (warp w reads TMEM lanes 32*(w%4)..+31, half of
-// the tile's columns each).
+// warp 2 copies each stage's scale factors into TMEM, warps 4-11 run the
+// epilogue (warp w reads TMEM lanes 32*(w%4)..+31, half of the tile's columns
+// each).
 // Tile 128 x BN x 128 (BN = 256 or 128) on one SM, or 256 x 256 x 128 on a
 // CTA pair (cta_group::2: each SM holds its 128 rows of A and half of B, so
-// the operand bytes per MMA flop drop by a third); 4-8-stage smem ring; the
-// accumulator is double-buffered in TMEM when it fits next to the scale
-// factors (BN = 128).  Every wait is bounded; a wait that gives up records
+// the operand bytes per MMA flop drop by a third); 4-8-stage smem ring with a
+// matching ring of scale-factor slots in TMEM; the accumulator is
+// double-buffered in TMEM when it fits next to them (BN = 128).  Every wait is bounded; a wait that gives up records
 // MXG_ERR_TIMEOUT, stops the CTA's pipeline and still frees TMEM.
 #include <mutex>
 
@@ -47,8 +48,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 128;
-// warp 0 TMA, warp 1 MMA, warps 2-3 idle, warps 4-11 epilogue (two per TMEM
-// lane quadrant; measured faster than packing the epilogue into warps 2-9)
+// warp 0 TMA, warp 1 MMA, warp 2 scale-factor copies, warp 3 idle, warps 4-11
+// epilogue (two per TMEM lane quadrant)
 constexpr int kThreads = 384;
 
 template <int BN, int EPI, bool PAIR>
@@ -71,10 +72,13 @@ struct Cfg {
   static constexpr int kStages = (232448 - 1024 - kCtrlBytes - kXposeBytes) / kStageBytes > 8
                                      ? 8
                                      : (232448 - 1024 - kCtrlBytes - kXposeBytes) / kStageBytes;
-  static constexpr uint32_t kSfaCol = kAcc * BN;            // TMEM columns of the scale factors
-  static constexpr uint32_t kSfbCol = kSfaCol + 4;
+  // Scale factors in TMEM: one slot per smem stage (SFA 4 columns, then SFB
+  // 4 per 128 rows), so the copy for the next K step never overwrites scales
+  // that MMAs still in the tensor pipe are reading.
+  static constexpr uint32_t kSfCol = kAcc * BN;             // first TMEM column of the slots
+  static constexpr uint32_t kSfSlot = 4 + BN / 32;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kCtrlBytes + kXposeBytes;
-  static_assert(kSfbCol + BN / 32 <= 512, "TMEM budget");
+  static_assert(kSfCol + kStages * kSfSlot <= 512, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(!PAIR || BN == 256, "CTA-pair tiles are 256 x 256");
 };
@@ -388,7 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + C::kStages;
   uint64_t* tempty = tfull + C::kAcc;
   uint64_t* drained = tempty + C::kAcc;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drained + 1);
+  uint64_t* sfready = drained + 1;                  // scale factors of a stage are in TMEM
+  uint64_t* cdrained = sfready + C::kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cdrained + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* never_set = reinterpret_cast<int*>(tmem_slot + 2);
   int* s_poff = reinterpret_cast<int*>(tmem_slot + 4);
@@ -412,6 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[a], PAIR ? 16 : 8);
     }
     mbar_init(drained, 1);
+    for (int st = 0; st < C::kStages; ++st) mbar_init(&sfready[st], 1);
+    mbar_init(cdrained, 1);
     *abort_flag = 0;
     *never_set = 0;
     fence_barrier_init();
@@ -586,8 +594,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------------- MMA
     if (lane == 0 && rank == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-      const uint32_t sfa_t = tmem + C::kSfaCol;
-      const uint32_t sfb_t = tmem + C::kSfbCol;
       bool aborted = false;
       for (int64_t t = tile0; t < total && !aborted; t += tstep) {
         const TileCoord tc = decode(t);
@@ -601,9 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_t = tmem + acc * BN;
         for (int kb = 0; kb < tc.num_k; ++kb) {
-          const bool in = PAIR ? mbar_wait_bounded_cluster(&full[stage], phase, abort_flag, limit_ns)
-                               : mbar_wait_bounded(&full[stage], phase, abort_flag, limit_ns);
-          if (!in) {
+          // the copier thread has seen the stage's data land and its scale
+          // factors are in TMEM slot `stage`
+          if (!mbar_wait_bounded(&sfready[stage], phase, abort_flag, limit_ns)) {
             fail();
             aborted = true;
             break;
@@ -611,12 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           uint8_t* sA = smem + stage * C::kStageBytes;
           uint8_t* sB = sA + C::kABytes;
-          uint8_t* sSfa = sB + C::kBBytes;
-          uint8_t* sSfb = sSfa + C::kSfaBytes;
-          tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc(smem_u32(sSfa), 0, 128, kLayoutNone));
-#pragma unroll
-          for (int i = 0; i < BN / 128; ++i)
-            tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * i, smem_desc(smem_u32(sSfb + 512 * i), 0, 128, kLayoutNone));
+          const uint32_t sfa_t = tmem + C::kSfCol + stage * C::kSfSlot;
+          const uint32_t sfb_t = sfa_t + 4;
           const uint64_t adesc = smem_desc(smem_u32(sA), 0, 1024, kLayoutSwizzle128B);
           const uint64_t bdesc = smem_desc(smem_u32(sB), 0, 1024, kLayoutSwizzle128B);
 #pragma unroll
@@ -639,6 +641,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       // all MMAs issued by this thread are complete before TMEM is released
       mma_commit<CG>(drained);
       mbar_wait_bounded(drained, 0, never_set, limit_ns);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------- scale-factor copier
+    // Waits for each stage's data and copies its scale factors into the
+    // stage's TMEM slot.  Kept off the MMA thread: a barrier wait followed by
+    // a shared->TMEM copy on the issuing thread starves the tensor pipe.
+    if (lane == 0 && rank == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool aborted = false;
+      for (int64_t t = tile0; t < total && !aborted; t += tstep) {
+        const TileCoord tc = decode(t);
+        for (int kb = 0; kb < tc.num_k; ++kb) {
+          const bool in = PAIR ? mbar_wait_bounded_cluster(&full[stage], phase, abort_flag, limit_ns)
+                               : mbar_wait_bounded(&full[stage], phase, abort_flag, limit_ns);
+          if (!in) {
+            fail();
+            aborted = true;
+            break;
+          }
+          uint8_t* sSfa = smem + stage * C::kStageBytes + C::kABytes + C::kBBytes;
+          uint8_t* sSfb = sSfa + C::kSfaBytes;
+          const uint32_t sfa_t = tmem + C::kSfCol + stage * C::kSfSlot;
+          tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc(smem_u32(sSfa), 0, 128, kLayoutNone));
+#pragma unroll
+          for (int i = 0; i < BN / 128; ++i)
+            tmem_cp_32x128b_warpx4<CG>(sfa_t + 4 + 4 * i, smem_desc(smem_u32(sSfb + 512 * i), 0, 128, kLayoutNone));
+          mma_commit<CG>(&sfready[stage]);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // every copy issued by this thread has landed before TMEM is released
+      mma_commit<CG>(cdrained);
+      mbar_wait_bounded(cdrained, 0, never_set, limit_ns);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
