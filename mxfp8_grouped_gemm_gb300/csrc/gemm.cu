@@ -187,12 +187,25 @@ __device__ __forceinline__ void col_quant32_xpose(const float (&h)[32], float* x
 }
 
 // Hand the accumulator buffer back to the MMA warp (all of this warp's TMEM
-// loads have completed).  `bar` is the cluster address of the MMA CTA's
-// barrier (this CTA's own barrier outside CTA pairs).
-__device__ __forceinline__ void release_acc(uint32_t bar, int lane) {
+// loads have completed).  A single CTA, or rank 0 of a pair, arrives on its own
+// barrier.  Rank 1 of a pair signals rank 0 with a 4-byte asynchronous store
+// into rank 0's shared memory that completes transaction bytes on rank 0's
+// barrier: measured on GB300, an mbarrier arrive through the cluster window
+// became visible to the waiting MMA thread only 2-4k cycles later, against a
+// few hundred for these two paths.
+struct AccRelease {
+  uint32_t bar;   // rank 0 / single CTA: own barrier (shared window); rank 1: rank 0's barrier (cluster window)
+  uint32_t land;  // rank 1: this warp's 4-byte slot in rank 0's shared memory (cluster window)
+  bool peer;      // rank 1 of a CTA pair
+};
+
+__device__ __forceinline__ void release_acc(const AccRelease& rl, int lane) {
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive_remote(bar);
+  if (lane == 0) {
+    if (rl.peer) st_async_complete_tx(rl.land, 1u, rl.bar);
+    else mbar_arrive_u32(rl.bar);
+  }
 }
 
 // bf16 store.  The thread owns half of its row's BN columns; it drains them
@@ -200,7 +213,7 @@ __device__ __forceinline__ void release_acc(uint32_t bar, int lane) {
 // so the next tile's MMAs overlap the global stores.
 template <int BN, bool KG>
 __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int row, int hf,
-                                         uint32_t tempty, int lane) {
+                                         const AccRelease& tempty, int lane) {
   constexpr int COLS = BN / 2;
   uint32_t packed[COLS / 2];
 #pragma unroll
@@ -231,7 +244,7 @@ __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc,
 // h in fp32 and quantises and stores while the next tile's MMAs run.
 template <int BN>
 __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
-                                           int hf, uint32_t tempty) {
+                                           int hf, const AccRelease& tempty) {
   constexpr int HC = BN / 2;          // h columns per tile
   constexpr int CH = HC / 64;         // 32-column chunks per thread
   const int64_t tok0 = tc.m0 + q * 32;
@@ -282,7 +295,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& t
 // Partial d(prob) sums go to dp_part[r][2*nt + hf].
 template <int BN>
 __device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
-                                            int hf, uint32_t tempty, float* xp) {
+                                            int hf, const AccRelease& tempty, float* xp) {
   constexpr int COLS = BN / 2;
   const int64_t tok0 = tc.m0 + q * 32;
   const int64_t r = tok0 + lane;
@@ -324,7 +337,7 @@ __device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& 
 // BN = 256: drain the thread's 128 dH columns to a bf16 staging row in shared
 // memory, release the accumulator, then run the dSwiGLU epilogue from there.
 __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q,
-                                                   int lane, int hf, uint32_t tempty, uint16_t* stage_base) {
+                                                   int lane, int hf, const AccRelease& tempty, uint16_t* stage_base) {
   constexpr int COLS = 128;
   constexpr int STRIDE = 256 + 8;                 // bf16 per staging row
   const int64_t tok0 = tc.m0 + q * 32;
@@ -415,7 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < C::kAcc; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], PAIR ? 16 : 8);
+      // the epilogue warps' arrivals (8) + in a pair the MMA thread's arrive.expect_tx
+      // for the 8 x 4 bytes rank 1's warps store
+      mbar_init(&tempty[a], PAIR ? 9 : 8);
     }
     mbar_init(drained, 1);
     for (int st = 0; st < C::kStages; ++st) mbar_init(&sfready[st], 1);
@@ -504,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 1;
   };
   // the barrier the epilogue releases accumulators on (rank 0's, in a pair)
-  const uint32_t tempty_base = PAIR ? map_to_rank(smem_u32(tempty), 0) : smem_u32(tempty);
+  uint32_t* landing = reinterpret_cast<uint32_t*>(tmem_slot + 4) + 264;   // after s_poff (E <= 256)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -594,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------------- MMA
     if (lane == 0 && rank == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-      bool aborted = false;
+      bool aborted = false, committed = false;
       for (int64_t t = tile0; t < total && !aborted; t += tstep) {
         const TileCoord tc = decode(t);
         if (tc.num_k == 0) continue;
@@ -633,11 +648,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (aborted) break;
         mma_commit<CG>(&tfull[acc]);
+        if (PAIR) mbar_arrive_expect_tx(&tempty[acc], 8 * 4);
+        committed = true;
         if (++acc == C::kAcc) {
           acc = 0;
           acc_phase ^= 1;
         }
       }
+      // rank 1's release stores for the last tile have landed in this CTA's
+      // shared memory before the CTA exits
+      if (PAIR && committed) mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, never_set, limit_ns);
       // all MMAs issued by this thread are complete before TMEM is released
       mma_commit<CG>(drained);
       mbar_wait_bounded(drained, 0, never_set, limit_ns);
@@ -704,7 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      const uint32_t rel = tempty_base + acc * 8;
+      AccRelease rel;
+      rel.peer = PAIR && rank == 1;
+      rel.bar = rel.peer ? map_to_rank(smem_u32(&tempty[acc]), 0) : smem_u32(&tempty[acc]);
+      rel.land = rel.peer ? map_to_rank(smem_u32(&landing[warp - 4]), 0) : 0u;
       if (EPI == EPI_SWIGLU) {
         epi_swiglu<BN>(P, tc, tb, q, lane, hf, rel);
       } else if (EPI == EPI_DSWIGLU) {

@@ -118,6 +118,17 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
+// 4-byte store into another CTA's shared memory that completes 4 bytes of
+// transaction count on that CTA's mbarrier (both cluster addresses).
+__device__ __forceinline__ void st_async_complete_tx(uint32_t cluster_addr, uint32_t value, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(cluster_addr),
+               "r"(value), "r"(cluster_bar)
+               : "memory");
+}
+// Plain arrive on this CTA's mbarrier, given as a shared-window address.
+__device__ __forceinline__ void mbar_arrive_u32(uint32_t saddr) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr) : "memory");
+}
 // Arrive on an mbarrier in another CTA of the cluster (release at cluster scope).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
