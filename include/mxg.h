@@ -90,6 +90,46 @@ uint64_t mxg_launch_count(void);
 int mxg_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* probs, void* stream);
 
 /* ----------------------------------------------------------------------------
+ * Router front end: logits = x W_r^T (one linear layer H -> E, no bias) and the
+ * top-k route of mxg_route_topk on them, in one kernel.  [Grouped] Fig. 1 (a
+ * router picks two of eight experts per token); the page does not spell the
+ * router out, the single bias-free linear layer is the reading taken.
+ *   x         bf16 [T][H] (device)
+ *   w_router  bf16 [E][H] (device)
+ *   logits    fp32 [T][E] out, accumulated in fp32 from the bf16 products
+ *   ids, probs  as mxg_route_topk
+ * Requires H % 128 == 0, 1 <= k <= E <= 256, k <= 32.  x, w_router 16-byte
+ * aligned.
+ */
+int mxg_router_fwd(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, float* logits,
+                   int32_t* ids, float* probs, void* stream);
+
+/* Scratch for mxg_router_bwd (bytes). */
+size_t mxg_router_bwd_workspace_bytes(int T, int H, int E, int k);
+
+/* ----------------------------------------------------------------------------
+ * Router backward.  The choice of experts carries no gradient; the
+ * probabilities are a softmax over the chosen logits, so
+ *   dlogit[t, ids[t,j]] = probs[t,j] * (dprobs[t,j] - sum_i probs[t,i] dprobs[t,i])
+ * (0 for experts not chosen), then
+ *   dx[t]     += sum_j dlogit[t, ids[t,j]] * W_r[ids[t,j]]   (in place, bf16)
+ *   dw_router  = sum_t dlogits[t]^T x[t]                     (fp32, overwritten)
+ *   x, w_router  bf16 as in mxg_router_fwd
+ *   ids, probs   the route of mxg_router_fwd; dprobs fp32 [T][k] (the MLP's
+ *                d(probs) output)
+ *   dx           bf16 [T][H] in/out: the router's term is added to it (pass the
+ *                MLP's dx to get the layer's input gradient)
+ *   dw_router    fp32 [E][H] out
+ *   workspace    >= mxg_router_bwd_workspace_bytes(T, H, E, k) bytes
+ * dw_router is a fixed-order sum (deterministic).  Expert ids outside [0, E)
+ * are skipped and reported as MXG_ERR_EXPERT_ID through dev_status.
+ * Requires H % 128 == 0, 1 <= k <= E <= 256, k <= 32.
+ */
+int mxg_router_bwd(const uint16_t* x, const uint16_t* w_router, const int32_t* ids, const float* probs,
+                   const float* dprobs, int T, int H, int E, int k, uint16_t* dx, float* dw_router, void* workspace,
+                   size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* ----------------------------------------------------------------------------
  * Permute index: counting sort of the flat index f = t*k + j by expert id,
  * stable in f (bit-exact, deterministic).  [Grouped] "Grouping fragmented
  * expert workloads" (split_sizes: one token count per expert); [Overhead]

@@ -29,7 +29,8 @@ EXPORTS = [
     "mxg_grouped_gemm_wgrad", "mxg_mlp_saved_bytes", "mxg_mlp_workspace_bytes", "mxg_grouped_mlp_fwd",
     "mxg_grouped_mlp_bwd", "mxg_mlp_saved_view", "mxg_grouped_mlp_fwd_stage", "mxg_grouped_mlp_bwd_stage",
     "mxg_route_permute_noalloc_max_entries", "mxg_route_permute_noalloc", "mxg_mlp_group_align",
-    "mxg_mlp_row_capacity", "mxg_debug_grouped_gemm_stall",
+    "mxg_mlp_row_capacity", "mxg_debug_grouped_gemm_stall", "mxg_router_fwd", "mxg_router_bwd_workspace_bytes",
+    "mxg_router_bwd",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -94,6 +95,9 @@ def lib() -> ctypes.CDLL:
         "mxg_route_permute_noalloc_max_entries": (SZ, [I32]),
         "mxg_route_permute_noalloc": (I32, [P, I32, I32, I32, P, P, P, P, P, P]),
         "mxg_grouped_mlp_bwd_stage": (I32, [ctypes.POINTER(MlpBwdArgs), I32, P]),
+        "mxg_router_fwd": (I32, [P, P, I32, I32, I32, I32, P, P, P, P]),
+        "mxg_router_bwd_workspace_bytes": (SZ, [I32, I32, I32, I32]),
+        "mxg_router_bwd": (I32, [P, P, P, P, P, I32, I32, I32, I32, P, P, P, SZ, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -154,6 +158,42 @@ def mxg_route_topk(logits: torch.Tensor, k: int, ids=None, probs=None, stream=No
                                                   _ptr(ids, torch.int32, "ids"), _ptr(probs, torch.float32, "probs"),
                                                   _stream(stream)))
     return ids, probs
+
+
+def mxg_router_fwd(x: torch.Tensor, w_router: torch.Tensor, k: int, logits=None, ids=None, probs=None, stream=None):
+    """logits = x W_r^T (fp32 out) and the top-k route on them."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev) if logits is None else logits
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev) if ids is None else ids
+    probs = torch.empty((T, k), dtype=torch.float32, device=dev) if probs is None else probs
+    _check("mxg_router_fwd", lib().mxg_router_fwd(_ptr(x, torch.bfloat16, "x"), _ptr(w_router, torch.bfloat16, "w_router"),
+                                                  T, H, E, k, _ptr(logits, torch.float32, "logits"),
+                                                  _ptr(ids, torch.int32, "ids"), _ptr(probs, torch.float32, "probs"),
+                                                  _stream(stream)))
+    return logits, ids, probs
+
+
+def mxg_router_bwd_workspace_bytes(T, H, E, k) -> int:
+    return int(lib().mxg_router_bwd_workspace_bytes(T, H, E, k))
+
+
+def mxg_router_bwd(x, w_router, ids, probs, dprobs, dx, dev_status, dw_router=None, workspace=None, stream=None):
+    """Adds the router's term to dx (in place) and returns dW_r (fp32)."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    k = ids.shape[1]
+    dev = x.device
+    dw_router = torch.empty((E, H), dtype=torch.float32, device=dev) if dw_router is None else dw_router
+    nbytes = mxg_router_bwd_workspace_bytes(T, H, E, k)
+    workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev) if workspace is None else workspace
+    _check("mxg_router_bwd", lib().mxg_router_bwd(
+        _ptr(x, torch.bfloat16, "x"), _ptr(w_router, torch.bfloat16, "w_router"), _ptr(ids, torch.int32, "ids"),
+        _ptr(probs, torch.float32, "probs"), _ptr(dprobs, torch.float32, "dprobs"), T, H, E, k,
+        _ptr(dx, torch.bfloat16, "dx"), _ptr(dw_router, torch.float32, "dw_router"), _ptr(workspace), workspace.numel(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+    return dw_router
 
 
 def mxg_route_permute(ids: torch.Tensor, E: int, dev_status: torch.Tensor, stream=None) -> dict:

@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cfloat>
 #include <cstdint>
 
 #include "mxg.h"
@@ -59,6 +60,59 @@ __device__ __forceinline__ void encode32(const float (&v)[32], uint32_t (&w)[8])
     const uint32_t lo = cvt_e4m3x2(v[4 * i + 0], v[4 * i + 1]);
     const uint32_t hi = cvt_e4m3x2(v[4 * i + 2], v[4 * i + 3]);
     w[i] = lo | (hi << 16);
+  }
+}
+
+// ----------------------------------------------------------------- top-k
+// One warp routes one token: lane l holds logits l, l+32, ... (E <= 256); k
+// rounds of a warp argmax (ties to the lower id) pick the experts in
+// descending order, then softmax over the chosen logits.  `row` may be global
+// or shared memory.
+__device__ __forceinline__ void warp_topk_softmax(const float* row, int E, int k, int lane, int32_t* ids_out,
+                                                  float* probs_out) {
+  float v[8];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int e = lane + 32 * q;
+    v[q] = e < E ? row[e] : -FLT_MAX;
+    if (e >= E) taken |= 1u << q;
+  }
+  float my_val = 0.f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -FLT_MAX;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (!(taken >> q & 1u) && (bi == 0x7fffffff || v[q] > bv)) {   // first max within the lane = lowest id
+        bv = v[q];
+        bi = lane + 32 * q;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_val = bv;
+      my_id = bi;
+    }
+  }
+  const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
+  const float w = lane < k ? expf(my_val - vmax) : 0.f;
+  float sum = w;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    ids_out[lane] = my_id;
+    probs_out[lane] = w / sum;
   }
 }
 

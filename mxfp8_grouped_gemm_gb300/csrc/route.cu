@@ -16,57 +16,14 @@ namespace mxg {
 namespace {
 
 // ----------------------------------------------------------------- top-k ----
-// One warp per token; lane l holds logits l, l+32, ... (E <= 256).
+// One warp per token (see warp_topk_softmax).
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                    int32_t* __restrict__ ids, float* __restrict__ probs) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
-  const float* row = logits + static_cast<int64_t>(warp) * E;
-  float v[8];
-  uint32_t taken = 0;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int e = lane + 32 * q;
-    v[q] = e < E ? row[e] : -FLT_MAX;
-    if (e >= E) taken |= 1u << q;
-  }
-  float my_val = 0.f;
-  int my_id = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = -FLT_MAX;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (!(taken >> q & 1u) && (bi == 0x7fffffff || v[q] > bv)) {   // first max within the lane = lowest id
-        bv = v[q];
-        bi = lane + 32 * q;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == j) {
-      my_val = bv;
-      my_id = bi;
-    }
-  }
-  const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
-  const float w = lane < k ? expf(my_val - vmax) : 0.f;
-  float sum = w;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-  if (lane < k) {
-    ids[static_cast<int64_t>(warp) * k + lane] = my_id;
-    probs[static_cast<int64_t>(warp) * k + lane] = w / sum;
-  }
+  warp_topk_softmax(logits + static_cast<int64_t>(warp) * E, E, k, lane, ids + static_cast<int64_t>(warp) * k,
+                    probs + static_cast<int64_t>(warp) * k);
 }
 
 // --------------------------------------------------------------- permute ----

@@ -106,6 +106,29 @@ def test_gemm_validation(L):
     assert L.mxg_grouped_gemm_wgrad(*a) == 2
 
 
+def test_router_validation(L):
+    f = [FAKE, FAKE, 64, 256, 8, 2, FAKE, FAKE, FAKE, None]
+    a = list(f); a[0] = None
+    assert L.mxg_router_fwd(*a) == 1
+    a = list(f); a[3] = 200                    # H not a multiple of 128
+    assert L.mxg_router_fwd(*a) == 2
+    a = list(f); a[5] = 9                      # k > E
+    assert L.mxg_router_fwd(*a) == 2
+    a = list(f); a[1] = MISALIGNED
+    assert L.mxg_router_fwd(*a) == 3
+    ws = L.mxg_router_bwd_workspace_bytes(64, 256, 8, 2)
+    assert ws >= 64 * 2 * 4
+    b = [FAKE, FAKE, FAKE, FAKE, FAKE, 64, 256, 8, 2, FAKE, FAKE, FAKE, ws, FAKE, None]
+    a = list(b); a[9] = None
+    assert L.mxg_router_bwd(*a) == 1
+    a = list(b); a[6] = 192
+    assert L.mxg_router_bwd(*a) == 2
+    a = list(b); a[9] = MISALIGNED
+    assert L.mxg_router_bwd(*a) == 3
+    a = list(b); a[12] = ws - 1
+    assert L.mxg_router_bwd(*a) == 5
+
+
 def test_mlp_sizes_and_validation(L):
     import mxfp8_grouped_gemm_gb300 as m
     assert m.mxg_mlp_saved_bytes(256, 128, 256, 4, 2) > 0
