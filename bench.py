@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--workload", default="mixtral")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-router", action="store_true", help="skip timing the router front end")
     return ap.parse_args()
 
 
@@ -278,6 +279,41 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize(dev)
         e2e_ms = ea.elapsed_time(eb) / args.steps
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
+    # ---- router front end (logits GEMM H -> E + route, and its backward), on
+    # the same tokens, outside the MLP step: reported beside it ----
+    router = None
+    if not args.no_router and H % 128 == 0:
+        w_r = synthetic.random_bf16((E, H), 4242, std=0.02).to(dev)
+        dprobs = torch.randn(T, k, device=dev, generator=torch.Generator(device=dev).manual_seed(5))
+        dx_r = torch.zeros((T, H), dtype=torch.bfloat16, device=dev)
+        st_r = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws_r = torch.empty(m.mxg_router_bwd_workspace_bytes(T, H, E, k), dtype=torch.uint8, device=dev)
+        dw_r = torch.empty((E, H), dtype=torch.float32, device=dev)
+        lo, ri, rp = m.mxg_router_fwd(d["x"], w_r, k)
+        reps = 20
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for _ in range(3):
+            m.mxg_router_fwd(d["x"], w_r, k, logits=lo, ids=ri, probs=rp)
+            m.mxg_router_bwd(d["x"], w_r, ri, rp, dprobs, dx_r, st_r, dw_router=dw_r, workspace=ws_r)
+        torch.cuda.synchronize(dev)
+        ev[0].record(stream)
+        for _ in range(reps):
+            m.mxg_router_fwd(d["x"], w_r, k, logits=lo, ids=ri, probs=rp)
+        ev[1].record(stream)
+        for _ in range(reps):
+            m.mxg_router_bwd(d["x"], w_r, ri, rp, dprobs, dx_r, st_r, dw_router=dw_r, workspace=ws_r)
+        ev[2].record(stream)
+        torch.cuda.synchronize(dev)
+        if int(st_r.item()) != 0:
+            raise SystemExit(f"bench: router status {m.status_string(int(st_r.item()))}")
+        f_ms, b_ms = ev[0].elapsed_time(ev[1]) / reps, ev[1].elapsed_time(ev[2]) / reps
+        # algorithmic bytes: fwd reads x, writes logits, ids, probs; bwd reads
+        # probs, dprobs, ids, x, reads and writes dx, writes dW_r
+        fb = T * H * 2 + T * E * 4 + T * k * 8
+        bb = T * k * 12 + T * H * 2 + 2 * T * H * 2 + E * H * 4
+        router = {"fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4),
+                  "fwd_gbs": round(fb / (f_ms * 1e-3) / 1e9, 1), "bwd_gbs": round(bb / (b_ms * 1e-3) / 1e9, 1),
+                  "note": "not part of the MLP step above"}
     clk = clocks.stop()
     if layer.status() != 0:
         raise SystemExit(f"bench: device status {m.status_string(layer.status())}")
@@ -328,6 +364,8 @@ def run_ours(args, rank, world):
         "gpu_launches": int(round(launches)),
         "clocks": clk,
     }
+    if router:
+        res["router"] = router
     if e2e:
         res["e2e"] = {"value": round(world * flops / (e2e["ms"] * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                       "ms_per_step": round(e2e["ms"], 4), "h2d_bytes_per_step": e2e["h2d"],
