@@ -17,6 +17,13 @@ namespace {
 
 constexpr int kRows = 32;    // rows per CTA tile (one column-wise block)
 constexpr int kCols = 128;   // columns per CTA tile (four row-wise blocks)
+constexpr int kStride = kCols + 8;   // bf16 per smem row (272 bytes: 16-byte aligned, spreads banks)
+
+// Shared-memory position of 16-byte chunk c of staged row r: chunks are
+// permuted by XOR with 2*((r/8)%4), so that the eight rows of one transposed
+// 8x8 load (rows 2m + {0,1,8,9,16,17,24,25}) fall in eight different bank
+// groups.
+__device__ __forceinline__ int chunk_pos(int r, int c) { return c ^ (((r >> 3) & 3) << 1); }
 
 __device__ __forceinline__ void quant_store32(float (&v)[32], uint8_t* dst, uint8_t* sdst) {
   uint32_t amax = 0;
@@ -40,8 +47,55 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
                : "memory");
 }
 
+// Four 8x8 bf16 matrices from shared memory, transposed: thread t receives,
+// for matrix m, the two elements (rows 2(t%4), 2(t%4)+1; column t/4) of that
+// matrix as one packed word.  Threads 8m..8m+7 give the row addresses of m.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+
+// Column-wise MX of one warp's 32-row x 32-column block (columns col0..+31 of
+// the staged tile): ldmatrix.trans hands each quad of lanes one column with
+// lane j of the quad holding rows 8j..8j+7 in order (the row addresses are
+// permuted so that matrix m's fragment rows 2j, 2j+1 are tile rows 8j+2m,
+// 8j+2m+1); the quad reduces the block maximum with two shuffles and each lane
+// writes its 8 codes as one 8-byte store.
+__device__ __forceinline__ void quant_col_block(const QuantParams& P, const uint16_t* buf, int col0, int64_t gcol0,
+                                                int p0, int lane) {
+  const int m = lane >> 3, i = lane & 7;
+  const int srow = 8 * (i >> 1) + 2 * m + (i & 1);
+  const uint16_t* rowp = buf + srow * kStride;
+  const int j = lane & 3;
+#pragma unroll
+  for (int ct = 0; ct < 4; ++ct) {
+    uint32_t r[4];
+    ldsm_x4_trans(static_cast<uint32_t>(__cvta_generic_to_shared(rowp + chunk_pos(srow, (col0 >> 3) + ct) * 8)), r);
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[2 * q] = __uint_as_float(r[q] << 16);
+      v[2 * q + 1] = __uint_as_float(r[q] & 0xffff0000u);
+    }
+    uint32_t amax = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) amax = max(amax, __float_as_uint(v[q]) & 0x7fffffffu);
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const uint32_t sb = mx_scale_byte(amax);
+    const float inv = mx_inv_scale(sb);
+    uint32_t w[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
+    const int64_t gcol = gcol0 + ct * 8 + (lane >> 2);
+    *reinterpret_cast<uint2*>(P.q_col + gcol * P.ld_col + p0 + 8 * j) = make_uint2(w[0], w[1]);
+    if (j == 0) P.s_col[sf_offset(P.layout, gcol, p0 >> 5, P.sf_col_rows, P.ld_col >> 5)] = static_cast<uint8_t>(sb);
+  }
+}
+
 constexpr int kTilesPerCta = 4;      // 32-row tiles walked by one CTA
-constexpr int kStride = kCols + 8;   // bf16 per smem row (272 bytes: 16-byte aligned, spreads banks)
 
 // Stage one 32 x 128 tile (gathered rows) into shared memory asynchronously.
 __device__ __forceinline__ void stage_tile(const QuantParams& P, const uint16_t* xb, int p0, int c0, uint16_t* buf,
@@ -58,7 +112,7 @@ __device__ __forceinline__ void stage_tile(const QuantParams& P, const uint16_t*
       if (f < 0) zero = true;
       else srow = f / P.src_div;
     }
-    uint16_t* dst = buf + rr * kStride + vv * 8;
+    uint16_t* dst = buf + rr * kStride + chunk_pos(rr, vv) * 8;
     if (zero) *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     else cp_async16(dst, xb + srow * P.ld_x + c0 + vv * 8);
   }
@@ -68,8 +122,9 @@ __device__ __forceinline__ void stage_tile(const QuantParams& P, const uint16_t*
 // One CTA walks kTilesPerCta tiles of 32 rows x 128 columns, loading tile t+1
 // (asynchronous 16-byte copies into the other shared buffer) while it
 // quantises tile t.  Row-wise: thread t quantises the 32-value block (row t/4,
-// columns 32*(t%4)..) read back with 16-byte loads.  Column-wise: thread t
-// quantises column t over the tile's 32 rows.
+// columns 32*(t%4)..) read back with 16-byte loads.  Column-wise: warp w
+// quantises columns 32w..32w+31 over the tile's 32 rows from transposed
+// matrix loads (quant_col_block).
 __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
   __shared__ __align__(16) uint16_t tile[2][kRows * kStride];
   const int c0 = blockIdx.y * kCols;
@@ -102,10 +157,10 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
       const int r = tid >> 2, j = tid & 3;
       const int p = p0 + r;
       float v[32];
-      const uint4* s4 = reinterpret_cast<const uint4*>(buf + r * kStride + j * 32);
+      const uint4* s4 = reinterpret_cast<const uint4*>(buf + r * kStride);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint4 q = s4[i];
+        const uint4 q = s4[chunk_pos(r, 4 * j + i)];
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -118,12 +173,8 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
                     P.s_row + sf_offset(P.layout, grow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5));
     }
     if (P.q_col != nullptr) {
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = bf16_bits_to_float(buf[i * kStride + tid]);
-      const int64_t gcol = static_cast<int64_t>(b) * P.cols + c0 + tid;
-      quant_store32(v, P.q_col + gcol * P.ld_col + p0,
-                    P.s_col + sf_offset(P.layout, gcol, p0 >> 5, P.sf_col_rows, P.ld_col >> 5));
+      const int warp = tid >> 5;
+      quant_col_block(P, buf, warp * 32, static_cast<int64_t>(b) * P.cols + c0 + warp * 32, p0, tid & 31);
     }
     __syncthreads();   // buffer t&1 is refilled two tiles later
   }
