@@ -345,6 +345,20 @@ def run_ours(args, rank, world):
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                 "frac": None, "traffic": None}
     gemm_ms = sum(stage_ms[s_] for s_ in stage_flops)
+    # memory-bound kernels against the measured copy bandwidth: algorithmic
+    # bytes (each input read once, each output written once) / CUDA-event time
+    Rc = m.mxg_mlp_row_capacity(T, k, E)
+    mx = lambda n: n + n // 32                                  # E4M3 codes + E8M0 scales
+    hbm_bytes = {
+        "fwd.quant_weights": 2 * E * 3 * H * I + 2 * mx(E * 3 * H * I),   # bf16 in, two orientations out
+        "fwd.quant_x": 2 * R * H + 2 * mx(Rc * H),                          # gathered rows in, row + column MX out
+        "bwd.quant_dy": 2 * R * H + 2 * mx(Rc * H),
+        "fwd.combine": 2 * R * H + 2 * T * H,                              # k rows in, one row out
+        "bwd.combine_dx": 2 * R * H + 2 * T * H,
+    }
+    hbm = {s_: {"gbs": round(b / (stage_ms[s_] * 1e-3) / 1e9, 1),
+                "frac": round(b / (stage_ms[s_] * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 3)}
+           for s_, b in hbm_bytes.items()}
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -361,6 +375,7 @@ def run_ours(args, rank, world):
         "split_sizes": {"min": int(split.min()), "max": int(split.max()), "mean": float(split.mean()),
                         "zeros": int((split == 0).sum())},
         "roofline": roof,
+        "hbm_kernels": {"peak_gbs": float(peaks["hbm_gbs"]), "peak_source": f"{peaks_kind} copy", **hbm},
         "gpu_launches": int(round(launches)),
         "clocks": clk,
     }
