@@ -167,6 +167,22 @@ def traffic_for(stage: str, workload: str) -> int | None:
     return int(e["bytes_per_launch"])
 
 
+def max_over_ranks(times_ms, world, device=None):
+    """Per-rank step times -> the slowest rank's (replicas run in lock step from
+    the barrier, so the job's time is the maximum)."""
+    if world == 1:
+        return [float(t) for t in times_ms]
+    import torch
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_throughput(flops_per_replica_step, ms, world):
+    """Whole-job TFLOP/s: every replica does a full step of work per step time."""
+    return world * flops_per_replica_step / (ms * 1e-3) / 1e12
+
+
 def run_ours(args, rank, world):
     import numpy as np
     import torch
@@ -318,15 +334,11 @@ def run_ours(args, rank, world):
     if layer.status() != 0:
         raise SystemExit(f"bench: device status {m.status_string(layer.status())}")
 
-    ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms, e2e["ms"] if e2e else 0.0], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_max = float(t[0]), float(t[1])
-        if e2e:
-            e2e["ms"] = e2e_max
+    ms, e2e_ms = max_over_ranks([total_ms / args.steps, e2e["ms"] if e2e else 0.0], world, dev)
+    if e2e:
+        e2e["ms"] = e2e_ms
     flops = wl.gemm_flops(True)
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_throughput(flops, ms, world)
     split = layer.split_sizes.cpu().numpy()
 
     peaks, peaks_kind = load_peaks()
