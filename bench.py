@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-router", action="store_true", help="skip timing the router front end")
+    ap.add_argument("--precision", choices=["mxfp8", "bf16"], default="mxfp8",
+                    help="bf16: the like-for-like BF16 grouped MLP instead of the MXFP8 path")
     return ap.parse_args()
 
 
@@ -123,10 +125,10 @@ def cpu_sample_inputs(inp, wl, i_cut=CPU_SAMPLE_I):
             "dy": inp["dy"][:T_s].double().numpy(), "T": T_s, "I": I_s}
 
 
-def cpu_sample_run(s, k):
+def cpu_sample_run(s, k, quant=True):
     from oracle import moe
     ids, probs = moe.route_topk(s["logits"], k)
-    ctx = moe.mlp_fwd(s["x"], ids, probs, s["w_gate_up"], s["w_down"])
+    ctx = moe.mlp_fwd(s["x"], ids, probs, s["w_gate_up"], s["w_down"], quant=quant)
     moe.mlp_bwd(ctx, s["dy"])
 
 
@@ -137,12 +139,12 @@ def cpu_threads() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(inp, wl, reps: int = 1) -> dict:
+def cpu_baseline(inp, wl, reps: int = 1, quant: bool = True) -> dict:
     s = cpu_sample_inputs(inp, wl)
     flops = 18.0 * s["T"] * wl.k * wl.H * s["I"]
     t0 = time.perf_counter()
     for _ in range(reps):
-        cpu_sample_run(s, wl.k)
+        cpu_sample_run(s, wl.k, quant)
     dt = (time.perf_counter() - t0) / reps
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
             "sample": f"fwd+bwd of the first {s['T']} tokens, all {wl.E} experts, H={wl.H}, intermediate cut to "
@@ -201,7 +203,7 @@ def run_ours(args, rank, world):
     if "dy" not in inp:
         inp["dy"] = synthetic.random_bf16((wl.T, wl.H), 77)
     T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
-    layer = m.GroupedMLP(T, H, I, E, k, device=dev)
+    layer = m.GroupedMLP(T, H, I, E, k, device=dev, precision=args.precision)
     d = {n: v.to(dev) for n, v in inp.items() if isinstance(v, torch.Tensor)}
     stream = torch.cuda.current_stream(dev)
 
@@ -342,7 +344,10 @@ def run_ours(args, rank, world):
     split = layer.split_sizes.cpu().numpy()
 
     peaks, peaks_kind = load_peaks()
-    p_mx = 2.0 * float(peaks["bf16_tflops_sustained"])
+    # the tensor roofline of the computing dtype: 2 x measured bf16 for MXFP8
+    # (the nominal fp8/bf16 ratio), the measured bf16 itself for the BF16 path
+    ratio = 2.0 if args.precision == "mxfp8" else 1.0
+    p_mx = ratio * float(peaks["bf16_tflops_sustained"])
     R = T * k
     stage_flops = {"fwd.gate_up": 4.0 * R * H * I, "fwd.down": 2.0 * R * H * I, "bwd.dgrad_down": 2.0 * R * H * I,
                    "bwd.wgrad_down": 2.0 * R * H * I, "bwd.dgrad_gate_up": 4.0 * R * H * I,
@@ -352,7 +357,8 @@ def run_ours(args, rank, world):
         ach = stage_flops[dom] / (stage_ms[dom] * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": round(p_mx, 1),
                 "unit": "TFLOP/s", "frac": round(ach / p_mx, 4), "traffic": traffic_for(dom, args.workload),
-                "peak_source": f"2 x {peaks_kind} sustained dense bf16 ({peaks['bf16_tflops_sustained']} TFLOP/s)"}
+                "peak_source": (f"2 x " if ratio == 2.0 else "") +
+                               f"{peaks_kind} sustained dense bf16 ({peaks['bf16_tflops_sustained']} TFLOP/s)"}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                 "frac": None, "traffic": None}
@@ -374,15 +380,15 @@ def run_ours(args, rank, world):
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3" if args.precision == "mxfp8" else "bf16", "data": "synthetic",
         "config": {"workload": f"{wl.name}: Mixtral-8x7B MoE layer T={T} H={H} I={I} E={E} top-{k}"
                    if wl.name == "mixtral" else f"{wl.name}: T={T} H={H} I={I} E={E} top-{k}",
-                   "tokens_per_step": T, "gemm_flops_per_step": flops,
+                   "precision": args.precision, "tokens_per_step": T, "gemm_flops_per_step": flops,
                    "l2": "no flush: every step streams > 10 GB (weights 2.8 GB) through HBM, inputs > L2",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": round(world * T / (ms * 1e-3), 1),
         "gemm_tflops": round(world * flops / (gemm_ms * 1e-3) / 1e12, 2),
-        "frac_of_mxfp8_peak": round(value / world / p_mx, 4),
+        ("frac_of_mxfp8_peak" if args.precision == "mxfp8" else "frac_of_bf16_peak"): round(value / world / p_mx, 4),
         "stages_ms": {s_: round(v, 4) for s_, v in stage_ms.items()},
         "split_sizes": {"min": int(split.min()), "max": int(split.max()), "mean": float(split.mean()),
                         "zeros": int((split == 0).sum())},
@@ -398,7 +404,7 @@ def run_ours(args, rank, world):
                       "ms_per_step": round(e2e["ms"], 4), "h2d_bytes_per_step": e2e["h2d"],
                       "d2h_bytes_per_step": e2e["d2h"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(inp, wl)
+        res["cpu_baseline"] = cpu_baseline(inp, wl, quant=args.precision == "mxfp8")
     return res
 
 

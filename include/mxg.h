@@ -310,6 +310,24 @@ size_t mxg_mlp_workspace_bytes(int T, int H, int I, int E, int k);
 int mxg_grouped_mlp_fwd(const mxg_mlp_fwd_args* args, void* stream);
 int mxg_grouped_mlp_bwd(const mxg_mlp_bwd_args* args, void* stream);
 
+/* ----------------------------------------------------------------------------
+ * The same grouped expert MLP in BF16: bf16 operands on the tensor cores with
+ * fp32 accumulation, no quantisation; h and dGU are kept in bf16.  The like-
+ * for-like reference of the MXFP8 path ([Grouped] "Training benchmark", Fig.
+ * 5, compares the recipe's BF16 and MXFP8 runs).  Arguments, stages, outputs,
+ * ownership and errors as mxg_grouped_mlp_fwd / _bwd, with `saved` and
+ * `workspace` sized by the two _bf16_ queries (a saved buffer of one precision
+ * cannot be passed to the other's backward).  Requires H % 256 == 0 and
+ * I % 256 == 0 (every GEMM runs as 256 x 256 CTA-pair tiles; expert groups
+ * start on multiples of 256 padded rows).
+ */
+size_t mxg_mlp_bf16_saved_bytes(int T, int H, int I, int E, int k);
+size_t mxg_mlp_bf16_workspace_bytes(int T, int H, int I, int E, int k);
+int mxg_grouped_mlp_bf16_fwd(const mxg_mlp_fwd_args* args, void* stream);
+int mxg_grouped_mlp_bf16_bwd(const mxg_mlp_bwd_args* args, void* stream);
+int mxg_grouped_mlp_bf16_fwd_stage(const mxg_mlp_fwd_args* args, int stage, void* stream);
+int mxg_grouped_mlp_bf16_bwd_stage(const mxg_mlp_bwd_args* args, int stage, void* stream);
+
 /* Debug views into `saved` (device pointers; NULL on bad arguments) used by the
  * tests to compare intermediates: 0 = GU (bf16 [m_cap][2I], the gate-up GEMM
  * output before the activation; m_cap = mxg_mlp_row_capacity), 1 =

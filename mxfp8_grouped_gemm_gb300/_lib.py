@@ -30,7 +30,8 @@ EXPORTS = [
     "mxg_grouped_mlp_bwd", "mxg_mlp_saved_view", "mxg_grouped_mlp_fwd_stage", "mxg_grouped_mlp_bwd_stage",
     "mxg_route_permute_noalloc_max_entries", "mxg_route_permute_noalloc", "mxg_mlp_group_align",
     "mxg_mlp_row_capacity", "mxg_debug_grouped_gemm_stall", "mxg_router_fwd", "mxg_router_bwd_workspace_bytes",
-    "mxg_router_bwd",
+    "mxg_router_bwd", "mxg_mlp_bf16_saved_bytes", "mxg_mlp_bf16_workspace_bytes", "mxg_grouped_mlp_bf16_fwd",
+    "mxg_grouped_mlp_bf16_bwd", "mxg_grouped_mlp_bf16_fwd_stage", "mxg_grouped_mlp_bf16_bwd_stage",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -96,6 +97,12 @@ def lib() -> ctypes.CDLL:
         "mxg_route_permute_noalloc": (I32, [P, I32, I32, I32, P, P, P, P, P, P]),
         "mxg_grouped_mlp_bwd_stage": (I32, [ctypes.POINTER(MlpBwdArgs), I32, P]),
         "mxg_router_fwd": (I32, [P, P, I32, I32, I32, I32, P, P, P, P]),
+        "mxg_mlp_bf16_saved_bytes": (SZ, [I32, I32, I32, I32, I32]),
+        "mxg_mlp_bf16_workspace_bytes": (SZ, [I32, I32, I32, I32, I32]),
+        "mxg_grouped_mlp_bf16_fwd": (I32, [ctypes.POINTER(MlpFwdArgs), P]),
+        "mxg_grouped_mlp_bf16_bwd": (I32, [ctypes.POINTER(MlpBwdArgs), P]),
+        "mxg_grouped_mlp_bf16_fwd_stage": (I32, [ctypes.POINTER(MlpFwdArgs), I32, P]),
+        "mxg_grouped_mlp_bf16_bwd_stage": (I32, [ctypes.POINTER(MlpBwdArgs), I32, P]),
         "mxg_router_bwd_workspace_bytes": (SZ, [I32, I32, I32, I32]),
         "mxg_router_bwd": (I32, [P, P, P, P, P, I32, I32, I32, I32, P, P, P, SZ, P, P]),
     }
@@ -271,13 +278,22 @@ def mxg_mlp_workspace_bytes(T, H, I, E, k) -> int:
     return int(lib().mxg_mlp_workspace_bytes(T, H, I, E, k))
 
 
+def mxg_mlp_bf16_saved_bytes(T, H, I, E, k) -> int:
+    return int(lib().mxg_mlp_bf16_saved_bytes(T, H, I, E, k))
+
+
+def mxg_mlp_bf16_workspace_bytes(T, H, I, E, k) -> int:
+    return int(lib().mxg_mlp_bf16_workspace_bytes(T, H, I, E, k))
+
+
 def mxg_mlp_saved_view(saved: torch.Tensor, T, H, I, E, k, which: int) -> int:
     return int(lib().mxg_mlp_saved_view(_ptr(saved), T, H, I, E, k, which) or 0)
 
 
 def mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, saved, workspace, dev_status, y=None, split_sizes=None,
-                        save_for_backward: bool = True, stream=None, stage: int | None = None):
-    """Full forward, or one stage of it (FWD_STAGES index) when ``stage`` is given."""
+                        save_for_backward: bool = True, stream=None, stage: int | None = None, bf16: bool = False):
+    """Full forward, or one stage of it (FWD_STAGES index) when ``stage`` is given
+    (``bf16``: the BF16 path, mxg_grouped_mlp_bf16_fwd)."""
     T, H = x.shape
     k = ids.shape[1]
     E, N2, _ = w_gate_up.shape
@@ -289,16 +305,18 @@ def mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, saved, workspace, dev_
                    _ptr(_bits(w_down), torch.int16, "w_down"), _ptr(_bits(y)), _ptr(split_sizes, torch.int32),
                    _ptr(saved, torch.uint8, "saved"), saved.numel(), _ptr(workspace, torch.uint8, "workspace"),
                    workspace.numel(), 1 if save_for_backward else 0, _ptr(dev_status, torch.int32, "dev_status"))
+    name = "mxg_grouped_mlp_bf16_fwd" if bf16 else "mxg_grouped_mlp_fwd"
     if stage is None:
-        _check("mxg_grouped_mlp_fwd", lib().mxg_grouped_mlp_fwd(ctypes.byref(a), _stream(stream)))
+        _check(name, getattr(lib(), name)(ctypes.byref(a), _stream(stream)))
     else:
-        _check("mxg_grouped_mlp_fwd_stage", lib().mxg_grouped_mlp_fwd_stage(ctypes.byref(a), stage, _stream(stream)))
+        _check(name + "_stage", getattr(lib(), name + "_stage")(ctypes.byref(a), stage, _stream(stream)))
     return y, split_sizes
 
 
 def mxg_grouped_mlp_bwd(dy, saved, workspace, dev_status, E: int, I: int, k: int, dx=None, dw_gate_up=None,
-                        dw_down=None, dprobs=None, stream=None, stage: int | None = None):
-    """Full backward, or one stage of it (BWD_STAGES index) when ``stage`` is given."""
+                        dw_down=None, dprobs=None, stream=None, stage: int | None = None, bf16: bool = False):
+    """Full backward, or one stage of it (BWD_STAGES index) when ``stage`` is given
+    (``bf16``: the BF16 path, mxg_grouped_mlp_bf16_bwd)."""
     T, H = dy.shape
     dev = dy.device
     dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if dx is None else dx
@@ -309,8 +327,9 @@ def mxg_grouped_mlp_bwd(dy, saved, workspace, dev_status, E: int, I: int, k: int
                    saved.numel(), _ptr(_bits(dx)), _ptr(_bits(dw_gate_up)), _ptr(_bits(dw_down)),
                    _ptr(dprobs, torch.float32), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                    _ptr(dev_status, torch.int32, "dev_status"))
+    name = "mxg_grouped_mlp_bf16_bwd" if bf16 else "mxg_grouped_mlp_bwd"
     if stage is None:
-        _check("mxg_grouped_mlp_bwd", lib().mxg_grouped_mlp_bwd(ctypes.byref(a), _stream(stream)))
+        _check(name, getattr(lib(), name)(ctypes.byref(a), _stream(stream)))
     else:
-        _check("mxg_grouped_mlp_bwd_stage", lib().mxg_grouped_mlp_bwd_stage(ctypes.byref(a), stage, _stream(stream)))
+        _check(name + "_stage", getattr(lib(), name + "_stage")(ctypes.byref(a), stage, _stream(stream)))
     return dx, dw_gate_up, dw_down, dprobs

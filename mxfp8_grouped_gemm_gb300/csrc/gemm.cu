@@ -52,16 +52,18 @@ constexpr int BK = 128;
 // epilogue (two per TMEM lane quadrant)
 constexpr int kThreads = 384;
 
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI, bool PAIR, bool BF = false>
 struct Cfg {
+  // contraction elements per stage: one 128-byte swizzle row of A and B
+  static constexpr int kKElems = BF ? 64 : 128;
   static constexpr int CG = PAIR ? 2 : 1;
   static constexpr int kTileM = PAIR ? 2 * BM : BM;         // rows of one tile (both CTAs)
   static constexpr int kBRows = PAIR ? BN / 2 : BN;         // rows of B held by one CTA
   static constexpr int kAcc = BN == 128 ? 2 : 1;            // accumulator buffers in TMEM
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = kBRows * BK;
-  static constexpr int kSfaBytes = BM * 4;                  // 128 rows x 4 blocks of 32
-  static constexpr int kSfbBytes = BN * 4;                  // every CTA holds the tile's full SFB
+  static constexpr int kSfaBytes = BF ? 0 : BM * 4;         // 128 rows x 4 blocks of 32
+  static constexpr int kSfbBytes = BF ? 0 : BN * 4;         // every CTA holds the tile's full SFB
   static constexpr uint32_t kTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStageBytes = (kTx + 1023) / 1024 * 1024;
   // dSwiGLU: BN = 256 stages the tile's dH as bf16 rows (padded to 264) so the
@@ -76,9 +78,10 @@ struct Cfg {
   // 4 per 128 rows), so the copy for the next K step never overwrites scales
   // that MMAs still in the tensor pipe are reading.
   static constexpr uint32_t kSfCol = kAcc * BN;             // first TMEM column of the slots
-  static constexpr uint32_t kSfSlot = 4 + BN / 32;
+  static constexpr uint32_t kSfSlot = BF ? 0 : 4 + BN / 32;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kCtrlBytes + kXposeBytes;
   static_assert(kSfCol + kStages * kSfSlot <= 512, "TMEM budget");
+  static_assert(kABytes == BM * 128, "stage rows are one 128-byte swizzle row");
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(!PAIR || BN == 256, "CTA-pair tiles are 256 x 256");
 };
@@ -186,6 +189,27 @@ __device__ __forceinline__ void col_quant32_xpose(const float (&h)[32], float* x
   sc[sf_mma_offset(col0 + lane, tok0 >> 5, sc_rows)] = static_cast<uint8_t>(sb);
 }
 
+// bf16 outputs of the fused epilogues (BF16 path): the thread's 32 values as
+// one 64-byte run of its row, and the transposed copy (column col0+i, row
+// tok0+lane: for each column the warp writes 32 consecutive bf16).
+__device__ __forceinline__ void row_store_bf16(const float (&h)[32], uint16_t* dst) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack_bf16x2(h[8 * i], h[8 * i + 1]), pack_bf16x2(h[8 * i + 2], h[8 * i + 3]),
+                      pack_bf16x2(h[8 * i + 4], h[8 * i + 5]), pack_bf16x2(h[8 * i + 6], h[8 * i + 7]));
+}
+__device__ __forceinline__ void col_store_bf16(const float (&h)[32], uint16_t* yc, int64_t ld, int64_t col0,
+                                               int64_t tok0, int lane) {
+  uint16_t* dst = yc + col0 * ld + tok0 + lane;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const __nv_bfloat16 v = __float2bfloat16_rn(h[i]);
+    *dst = *reinterpret_cast<const uint16_t*>(&v);
+    dst += ld;
+  }
+}
+
 // Hand the accumulator buffer back to the MMA warp (all of this warp's TMEM
 // loads have completed).  A single CTA, or rank 0 of a pair, arrives on its own
 // barrier.  Rank 1 of a pair signals rank 0 with a 4-byte asynchronous store
@@ -242,7 +266,7 @@ __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc,
 // (j0 = nt * BN/2).  The thread owns BN/4 h columns (half hf).  It drains its
 // accumulator columns into registers, releases the accumulator, then computes
 // h in fp32 and quantises and stores while the next tile's MMAs run.
-template <int BN>
+template <int BN, bool BF>
 __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
                                            int hf, const AccRelease& tempty) {
   constexpr int HC = BN / 2;          // h columns per tile
@@ -285,9 +309,14 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& t
         us[j] = make_uint4(up[4 * j], up[4 * j + 1], up[4 * j + 2], up[4 * j + 3]);
       }
     }
-    const uint32_t sb = row_quant32(h, P.q_out + r * P.q_out_ld + col);
-    P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-    if (P.qc_out != nullptr) col_quant32(h, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
+    if constexpr (BF) {
+      row_store_bf16(h, P.y_row + r * P.y_row_ld + col);
+      if (P.y_col != nullptr) col_store_bf16(h, P.y_col, P.y_col_ld, col, tok0, lane);
+    } else {
+      const uint32_t sb = row_quant32(h, P.q_out + r * P.q_out_ld + col);
+      P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
+      if (P.qc_out != nullptr) col_quant32(h, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
+    }
   }
 }
 
@@ -336,6 +365,7 @@ __device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& 
 
 // BN = 256: drain the thread's 128 dH columns to a bf16 staging row in shared
 // memory, release the accumulator, then run the dSwiGLU epilogue from there.
+template <bool BF>
 __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q,
                                                    int lane, int hf, const AccRelease& tempty, uint16_t* stage_base) {
   constexpr int COLS = 128;
@@ -381,21 +411,28 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
       u[i] = a * sl;
       dp += dh[i] * sl * uf;
     }
-    uint32_t sb = row_quant32(dg, P.q_out + r * P.q_out_ld + col);
-    P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-    col_quant32(dg, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
-    sb = row_quant32(u, P.q_out + r * P.q_out_ld + I + col);
-    P.s_out[sf_mma_offset(r, (I + col) >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-    col_quant32(u, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
+    if constexpr (BF) {
+      row_store_bf16(dg, P.y_row + r * P.y_row_ld + col);
+      col_store_bf16(dg, P.y_col, P.y_col_ld, col, tok0, lane);
+      row_store_bf16(u, P.y_row + r * P.y_row_ld + I + col);
+      col_store_bf16(u, P.y_col, P.y_col_ld, I + col, tok0, lane);
+    } else {
+      uint32_t sb = row_quant32(dg, P.q_out + r * P.q_out_ld + col);
+      P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
+      col_quant32(dg, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
+      sb = row_quant32(u, P.q_out + r * P.q_out_ld + I + col);
+      P.s_out[sf_mma_offset(r, (I + col) >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
+      col_quant32(u, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
+    }
   }
   P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp;
 }
 
-template <int BN, int EPI, bool KG, bool PAIR>
+template <int BN, int EPI, bool KG, bool PAIR, bool BF>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, const GemmArgs P) {
-  using C = Cfg<BN, EPI, PAIR>;
+  using C = Cfg<BN, EPI, PAIR, BF>;
   constexpr int CG = C::CG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -452,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Group offsets must be aligned to the tile height, monotone, inside capacity.
   bool ok = true;
   const int64_t cap = KG ? P.a_cols : P.M;
-  const int align = KG ? BK : C::kTileM;
+  const int align = KG ? C::kKElems : C::kTileM;
   for (int e = 0; e < E; ++e) {
     const int a = s_poff[e], b = s_poff[e + 1];
     if (a < 0 || (a % align) || b < a) ok = false;
@@ -500,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc.m0 = mt * C::kTileM + static_cast<int>(rank) * BM;
       tc.kbeg = s_poff[tc.e];
-      tc.num_k = (s_poff[tc.e + 1] - s_poff[tc.e]) / BK;
+      tc.num_k = (s_poff[tc.e + 1] - s_poff[tc.e]) / C::kKElems;
     } else {
       int e = 0;
       while (e + 1 < E && static_cast<int64_t>(s_poff[e + 1] / C::kTileM) * ntn <= t) ++e;
@@ -510,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc.nt = local / mcount;
       tc.m0 = s_poff[e] + (local - tc.nt * mcount) * C::kTileM + static_cast<int>(rank) * BM;
       tc.kbeg = 0;
-      tc.num_k = P.K / BK;
+      tc.num_k = P.K / C::kKElems;
     }
     return tc;
   };
@@ -558,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sB = sA + C::kABytes;
           uint8_t* sSfa = sB + C::kBBytes;
           uint8_t* sSfb = sSfa + C::kSfaBytes;
-          const int kx = tc.kbeg + kb * BK;
+          const int kx = tc.kbeg + kb * C::kKElems;
           const int64_t kc = kx >> 7;
           if (PAIR) {
             // scale atoms are rows of the scale tensors' maps (128 x u32 = 512 B)
@@ -569,29 +606,35 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(&full[stage], 2 * C::kTx);   // both CTAs' bytes
               tma_load_2d(sA, &tmA, kx, a_row, &full[stage]);
               tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
-              tma_load_2d(sSfa, &tmSA, 0, sa_atom, &full[stage]);
-              tma_load_2d(sSfb, &tmSB, 0, sb_atom0, &full[stage]);
-              tma_load_2d(sSfb + 512, &tmSB, 0, sb_atom1, &full[stage]);
+              if constexpr (!BF) {
+                tma_load_2d(sSfa, &tmSA, 0, sa_atom, &full[stage]);
+                tma_load_2d(sSfb, &tmSB, 0, sb_atom0, &full[stage]);
+                tma_load_2d(sSfb + 512, &tmSB, 0, sb_atom1, &full[stage]);
+              }
             } else {
               const uint32_t bar0 = full0 + stage * 8;
               tma_load_2d_pair(sA, &tmA, kx, a_row, bar0);
               tma_load_2d_pair(sB, &tmB, kx, b_row0, bar0);
-              tma_load_2d_pair(sSfa, &tmSA, 0, sa_atom, bar0);
-              tma_load_2d_pair(sSfb, &tmSB, 0, sb_atom0, bar0);
-              tma_load_2d_pair(sSfb + 512, &tmSB, 0, sb_atom1, bar0);
+              if constexpr (!BF) {
+                tma_load_2d_pair(sSfa, &tmSA, 0, sa_atom, bar0);
+                tma_load_2d_pair(sSfb, &tmSB, 0, sb_atom0, bar0);
+                tma_load_2d_pair(sSfb + 512, &tmSB, 0, sb_atom1, bar0);
+              }
             }
           } else {
             mbar_arrive_expect_tx(&full[stage], C::kTx);
             tma_load_2d(sA, &tmA, kx, a_row, &full[stage]);
-            bulk_load(sSfa, P.sa + (kc * (P.a_rows >> 7) + (a_row >> 7)) * 512, 512, &full[stage]);
+            if constexpr (!BF) bulk_load(sSfa, P.sa + (kc * (P.a_rows >> 7) + (a_row >> 7)) * 512, 512, &full[stage]);
             if (EPI == EPI_SWIGLU) {
               tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
-              tma_load_2d(sB + 128 * BK, &tmB, kx, b_row1, &full[stage]);
-              bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (b_row0 >> 7)) * 512, 512, &full[stage]);
-              bulk_load(sSfb + 512, P.sb + (kc * (P.b_rows >> 7) + (b_row1 >> 7)) * 512, 512, &full[stage]);
+              tma_load_2d(sB + 128 * 128, &tmB, kx, b_row1, &full[stage]);
+              if constexpr (!BF) {
+                bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (b_row0 >> 7)) * 512, 512, &full[stage]);
+                bulk_load(sSfb + 512, P.sb + (kc * (P.b_rows >> 7) + (b_row1 >> 7)) * 512, 512, &full[stage]);
+              }
             } else {
               tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
-              bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (sfb0 >> 7)) * 512, BN * 4, &full[stage]);
+              if constexpr (!BF) bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (sfb0 >> 7)) * 512, BN * 4, &full[stage]);
             }
           }
           if (++stage == C::kStages) {
@@ -622,9 +665,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_t = tmem + acc * BN;
         for (int kb = 0; kb < tc.num_k; ++kb) {
-          // the copier thread has seen the stage's data land and its scale
-          // factors are in TMEM slot `stage`
-          if (!mbar_wait_bounded(&sfready[stage], phase, abort_flag, limit_ns)) {
+          // MXFP8: the copier thread has seen the stage's data land and its
+          // scale factors are in TMEM slot `stage`; bf16: wait for the data
+          bool in;
+          if constexpr (BF)
+            in = PAIR ? mbar_wait_bounded_cluster(&full[stage], phase, abort_flag, limit_ns)
+                      : mbar_wait_bounded(&full[stage], phase, abort_flag, limit_ns);
+          else
+            in = mbar_wait_bounded(&sfready[stage], phase, abort_flag, limit_ns);
+          if (!in) {
             fail();
             aborted = true;
             break;
@@ -632,14 +681,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           uint8_t* sA = smem + stage * C::kStageBytes;
           uint8_t* sB = sA + C::kABytes;
-          const uint32_t sfa_t = tmem + C::kSfCol + stage * C::kSfSlot;
-          const uint32_t sfb_t = sfa_t + 4;
           const uint64_t adesc = smem_desc(smem_u32(sA), 0, 1024, kLayoutSwizzle128B);
           const uint64_t bdesc = smem_desc(smem_u32(sB), 0, 1024, kLayoutSwizzle128B);
+          if constexpr (BF) {
+            // four K = 16 steps of 32 bytes per 128-byte stage row
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k)
-            mma_mxf8<CG>(d_t, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8_e4m3(C::kTileM, BN, k, k), sfa_t, sfb_t,
-                         (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              mma_bf16<CG>(d_t, adesc + 2 * k, bdesc + 2 * k, idesc_bf16(C::kTileM, BN), (kb | k) != 0 ? 1u : 0u);
+          } else {
+            const uint32_t sfa_t = tmem + C::kSfCol + stage * C::kSfSlot;
+            const uint32_t sfb_t = sfa_t + 4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_mxf8<CG>(d_t, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8_e4m3(C::kTileM, BN, k, k), sfa_t, sfb_t,
+                           (kb | k) != 0 ? 1u : 0u);
+          }
           mma_commit<CG>(&empty[stage]);
           if (++stage == C::kStages) {
             stage = 0;
@@ -667,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Waits for each stage's data and copies its scale factors into the
     // stage's TMEM slot.  Kept off the MMA thread: a barrier wait followed by
     // a shared->TMEM copy on the issuing thread starves the tensor pipe.
-    if (lane == 0 && rank == 0) {
+    if (!BF && lane == 0 && rank == 0) {
       uint32_t stage = 0, phase = 0;
       bool aborted = false;
       for (int64_t t = tile0; t < total && !aborted; t += tstep) {
@@ -728,10 +784,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       rel.peer = PAIR && rank == 1;
       rel.bar = rel.peer ? map_to_rank(smem_u32(&tempty[acc]), 0) : smem_u32(&tempty[acc]);
       rel.land = rel.peer ? map_to_rank(smem_u32(&landing[warp - 4]), 0) : 0u;
-      if (EPI == EPI_SWIGLU) {
-        epi_swiglu<BN>(P, tc, tb, q, lane, hf, rel);
-      } else if (EPI == EPI_DSWIGLU) {
-        if (BN == 256) epi_dswiglu_staged(P, tc, tb, q, lane, hf, rel, reinterpret_cast<uint16_t*>(xpose));
+      if constexpr (EPI == EPI_SWIGLU) {
+        epi_swiglu<BN, BF>(P, tc, tb, q, lane, hf, rel);
+      } else if constexpr (EPI == EPI_DSWIGLU) {
+        if constexpr (BN == 256) epi_dswiglu_staged<BF>(P, tc, tb, q, lane, hf, rel, reinterpret_cast<uint16_t*>(xpose));
         else epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
       } else {
         epi_bf16<BN, KG>(P, tc, tb, row, hf, rel, lane);
@@ -783,6 +839,20 @@ bool encode_u8(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, uin
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 tensor map over [rows][cols] with a 64-element (128-byte) wide
+// swizzled box.
+bool encode_bf16(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [atoms][128] uint32 view of a tensor-core scale buffer (512-byte atoms).
 bool encode_atoms(CUtensorMap* m, const void* base, int64_t atoms) {
   EncodeTiledFn enc = get_encode();
@@ -803,14 +873,19 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int BN, int EPI, bool KG, bool PAIR>
+template <int BN, int EPI, bool KG, bool PAIR, bool BF = false>
 cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
-  using C = Cfg<BN, EPI, PAIR>;
+  using C = Cfg<BN, EPI, PAIR, BF>;
   CUtensorMap ta, tb;
   const int b_box = (EPI == EPI_SWIGLU && !PAIR) ? 128 : C::kBRows;
-  if (!encode_u8(&ta, g.a, g.a_cols, g.a_rows, BK, BM)) return cudaErrorInvalidValue;
-  if (!encode_u8(&tb, g.b, g.b_cols, g.b_rows, BK, b_box)) return cudaErrorInvalidValue;
-  auto kern = gemm_kernel<BN, EPI, KG, PAIR>;
+  if (BF) {
+    if (!encode_bf16(&ta, g.a, g.a_cols, g.a_rows, BM)) return cudaErrorInvalidValue;
+    if (!encode_bf16(&tb, g.b, g.b_cols, g.b_rows, b_box)) return cudaErrorInvalidValue;
+  } else {
+    if (!encode_u8(&ta, g.a, g.a_cols, g.a_rows, BK, BM)) return cudaErrorInvalidValue;
+    if (!encode_u8(&tb, g.b, g.b_cols, g.b_rows, BK, b_box)) return cudaErrorInvalidValue;
+  }
+  auto kern = gemm_kernel<BN, EPI, KG, PAIR, BF>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (err != cudaSuccess) return err;
   const int64_t units = PAIR ? num_sms() / 2 : num_sms();     // CTAs, or CTA pairs
@@ -832,7 +907,7 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
   }
   // scale tensors as rows of 512-byte atoms, for the CTA pair's TMA loads
   CUtensorMap tsa = ta, tsb = tb;
-  if (PAIR) {
+  if (PAIR && !BF) {
     if (!encode_atoms(&tsa, g.sa, (g.a_rows / 128) * (g.a_cols / 128))) return cudaErrorInvalidValue;
     if (!encode_atoms(&tsb, g.sb, (g.b_rows / 128) * (g.b_cols / 128))) return cudaErrorInvalidValue;
   }
@@ -852,6 +927,13 @@ int gemm_pick_bn(int epi, int N) {
 int dswiglu_partials(int I) { return 2 * (I / gemm_pick_bn(EPI_DSWIGLU, I)); }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
+  if (g.bf16) {  // BF16 path: CTA-pair tiles only
+    if (!g.pair) return cudaErrorInvalidValue;
+    if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, true, true>(g, s);
+    if (g.epi == EPI_DSWIGLU) return launch_impl<256, EPI_DSWIGLU, false, true, true>(g, s);
+    if (g.kgroup) return launch_impl<256, EPI_BF16, true, true, true>(g, s);
+    return launch_impl<256, EPI_BF16, false, true, true>(g, s);
+  }
   if (g.pair) {  // CTA-pair tiles, 256 x 256
     if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, true>(g, s);
     if (g.epi == EPI_DSWIGLU) return launch_impl<256, EPI_DSWIGLU, false, true>(g, s);

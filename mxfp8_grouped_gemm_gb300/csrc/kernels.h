@@ -29,6 +29,9 @@ struct QuantParams {
   int64_t ld_col;
   int64_t sf_col_rows;        // rows of the column-wise matrix (MMA layout)
   int32_t layout;             // MXG_LAYOUT_*
+  // bf16 pass-through (the BF16 path): the staged rows copied out unchanged
+  uint16_t* b_row;            // nullable: [batch*rows][cols] (gathered copy)
+  uint16_t* b_col;            // nullable: [batch*cols][ld_col] (transposed copy)
 };
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
 
@@ -96,6 +99,13 @@ struct GemmArgs {
   float* dp_part;
   int32_t dp_ld;
   int32_t* status;
+  // BF16 path: A and B hold bf16 values (a_cols / b_cols count elements), no
+  // scale factors; the fused epilogues write bf16 instead of MXFP8
+  bool bf16;
+  uint16_t* y_row;            // [rows][..] bf16 row-major output (h, or dGU)
+  int64_t y_row_ld;
+  uint16_t* y_col;            // [cols][..] bf16 transposed output (h^T, or dGU^T)
+  int64_t y_col_ld;
   int64_t tiles_upper;        // host bound on the number of tiles (grid sizing)
   uint64_t wait_limit_ns;     // bound on every wait inside the kernel (0: default)
   int32_t debug_stall;        // test hook: the producer issues no copies

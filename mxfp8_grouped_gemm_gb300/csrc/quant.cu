@@ -7,6 +7,8 @@
 //
 // Format: BioNeMo Uses Grouped Kernels and MXFP8, "Reducing memory pressure
 // with MXFP8", Fig. 3 (E4M3 values, one E8M0 scale per 32 consecutive values).
+// The same pass also serves the BF16 path: gathered and transposed bf16
+// copies (b_row / b_col) instead of codes.
 // Scale rule: OCP MX v1.0 (floor(log2 amax) - 8, clamp, RNE, saturate).
 #include "common.cuh"
 #include "kernels.h"
@@ -95,6 +97,24 @@ __device__ __forceinline__ void quant_col_block(const QuantParams& P, const uint
   }
 }
 
+// Transposed bf16 copy of one warp's 32-row x 32-column block: the same
+// transposed loads as quant_col_block, each lane writing its column's 8
+// consecutive rows as one 16-byte store.
+__device__ __forceinline__ void copy_col_block(const QuantParams& P, const uint16_t* buf, int col0, int64_t gcol0,
+                                               int p0, int lane) {
+  const int m = lane >> 3, i = lane & 7;
+  const int srow = 8 * (i >> 1) + 2 * m + (i & 1);
+  const uint16_t* rowp = buf + srow * kStride;
+  const int j = lane & 3;
+#pragma unroll
+  for (int ct = 0; ct < 4; ++ct) {
+    uint32_t r[4];
+    ldsm_x4_trans(static_cast<uint32_t>(__cvta_generic_to_shared(rowp + chunk_pos(srow, (col0 >> 3) + ct) * 8)), r);
+    const int64_t gcol = gcol0 + ct * 8 + (lane >> 2);
+    *reinterpret_cast<uint4*>(P.b_col + gcol * P.ld_col + p0 + 8 * j) = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+}
+
 constexpr int kTilesPerCta = 4;      // 32-row tiles walked by one CTA
 
 // Stage one 32 x 128 tile (gathered rows) into shared memory asynchronously.
@@ -175,6 +195,17 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
     if (P.q_col != nullptr) {
       const int warp = tid >> 5;
       quant_col_block(P, buf, warp * 32, static_cast<int64_t>(b) * P.cols + c0 + warp * 32, p0, tid & 31);
+    }
+    if (P.b_row != nullptr) {
+      const int r = tid >> 2, j = tid & 3;
+      const uint4* s4 = reinterpret_cast<const uint4*>(buf + r * kStride);
+      uint4* d = reinterpret_cast<uint4*>(P.b_row + (static_cast<int64_t>(b) * P.rows + p0 + r) * P.cols + c0 + j * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[i] = s4[chunk_pos(r, 4 * j + i)];
+    }
+    if (P.b_col != nullptr) {
+      const int warp = tid >> 5;
+      copy_col_block(P, buf, warp * 32, static_cast<int64_t>(b) * P.cols + c0 + warp * 32, p0, tid & 31);
     }
     __syncthreads();   // buffer t&1 is refilled two tiles later
   }

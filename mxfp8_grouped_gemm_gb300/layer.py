@@ -9,13 +9,24 @@ from . import _lib
 
 
 class GroupedMLP:
-    def __init__(self, T: int, H: int, I: int, E: int, k: int, device="cuda"):
+    """precision "mxfp8" (the path) or "bf16" (the like-for-like BF16 reference:
+    H and I multiples of 256)."""
+
+    def __init__(self, T: int, H: int, I: int, E: int, k: int, device="cuda", precision: str = "mxfp8"):
+        if precision not in ("mxfp8", "bf16"):
+            raise ValueError(f"precision must be 'mxfp8' or 'bf16', got {precision!r}")
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        self.bf16 = precision == "bf16"
         self.device = torch.device(device)
-        saved = _lib.mxg_mlp_saved_bytes(T, H, I, E, k)
-        ws = _lib.mxg_mlp_workspace_bytes(T, H, I, E, k)
+        if self.bf16:
+            saved = _lib.mxg_mlp_bf16_saved_bytes(T, H, I, E, k)
+            ws = _lib.mxg_mlp_bf16_workspace_bytes(T, H, I, E, k)
+        else:
+            saved = _lib.mxg_mlp_saved_bytes(T, H, I, E, k)
+            ws = _lib.mxg_mlp_workspace_bytes(T, H, I, E, k)
         if saved == 0 or ws == 0:
-            raise ValueError(f"unsupported shape T={T} H={H} I={I} E={E} k={k} (H, I multiples of 128; k <= E <= 256)")
+            raise ValueError(f"unsupported {precision} shape T={T} H={H} I={I} E={E} k={k} "
+                             f"(H, I multiples of {256 if self.bf16 else 128}; k <= E <= 256)")
         self.saved = torch.empty(saved, dtype=torch.uint8, device=self.device)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=self.device)
@@ -36,12 +47,13 @@ class GroupedMLP:
         return _lib.mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, self.saved, self.workspace,
                                         self.dev_status, y=self.y if y is None else y,
                                         split_sizes=self.split_sizes, save_for_backward=save_for_backward,
-                                        stream=stream, stage=stage)
+                                        stream=stream, stage=stage, bf16=self.bf16)
 
     def backward(self, dy, stream=None, stage=None, dx=None):
         return _lib.mxg_grouped_mlp_bwd(dy, self.saved, self.workspace, self.dev_status, self.E, self.I, self.k,
                                         dx=self.dx if dx is None else dx, dw_gate_up=self.dw_gate_up,
-                                        dw_down=self.dw_down, dprobs=self.dprobs, stream=stream, stage=stage)
+                                        dw_down=self.dw_down, dprobs=self.dprobs, stream=stream, stage=stage,
+                                        bf16=self.bf16)
 
     def step(self, logits, x, w_gate_up, w_down, dy, stream=None):
         """One pass of the whole path: route, forward (saving for backward), backward."""

@@ -106,6 +106,21 @@ def test_gemm_validation(L):
     assert L.mxg_grouped_gemm_wgrad(*a) == 2
 
 
+def test_bf16_mlp_sizes_and_validation(L):
+    assert L.mxg_mlp_bf16_saved_bytes(256, 256, 512, 4, 2) > 0
+    assert L.mxg_mlp_bf16_workspace_bytes(256, 256, 512, 4, 2) > 0
+    assert L.mxg_mlp_bf16_saved_bytes(256, 128, 512, 4, 2) == 0      # H not a multiple of 256
+    assert L.mxg_mlp_bf16_saved_bytes(256, 256, 384, 4, 2) == 0      # I not a multiple of 256
+    import mxfp8_grouped_gemm_gb300 as m
+    a = m.MlpFwdArgs(256, 128, 512, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, FAKE, 1 << 30, 1, FAKE)
+    assert L.mxg_grouped_mlp_bf16_fwd(ctypes.byref(a), None) == 2
+    a = m.MlpFwdArgs(256, 256, 512, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, FAKE, 1 << 30, 1, FAKE)
+    assert L.mxg_grouped_mlp_bf16_fwd(ctypes.byref(a), None) == 5      # saved buffer too small
+    b = m.MlpBwdArgs(256, 256, 512, 4, 2, MISALIGNED, FAKE, 1 << 30, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, FAKE)
+    assert L.mxg_grouped_mlp_bf16_bwd(ctypes.byref(b), None) == 3
+    assert L.mxg_grouped_mlp_bf16_fwd_stage(ctypes.byref(a), 99, None) == 1
+
+
 def test_router_validation(L):
     f = [FAKE, FAKE, 64, 256, 8, 2, FAKE, FAKE, FAKE, None]
     a = list(f); a[0] = None
