@@ -117,9 +117,10 @@ __device__ __forceinline__ void copy_col_block(const QuantParams& P, const uint1
 
 constexpr int kTilesPerCta = 4;      // 32-row tiles walked by one CTA
 
-// Stage one 32 x 128 tile (gathered rows) into shared memory asynchronously.
+// Stage one 32 x 128 tile (gathered rows: s_src holds the source row of each
+// of the CTA's rows, -1 for padding) into shared memory asynchronously.
 __device__ __forceinline__ void stage_tile(const QuantParams& P, const uint16_t* xb, int p0, int c0, uint16_t* buf,
-                                           int tid) {
+                                           int tid, const int* s_src, int first) {
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const int i = tid + it * 128;
@@ -128,9 +129,9 @@ __device__ __forceinline__ void stage_tile(const QuantParams& P, const uint16_t*
     int64_t srow = pp;
     bool zero = false;
     if (P.src_rows != nullptr) {
-      const int f = P.src_rows[pp];
+      const int f = s_src[pp - first];
       if (f < 0) zero = true;
-      else srow = f / P.src_div;
+      else srow = f;
     }
     uint16_t* dst = buf + rr * kStride + chunk_pos(rr, vv) * 8;
     if (zero) *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
@@ -156,12 +157,20 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
   const int ntiles = min(kTilesPerCta, (limit - first + kRows - 1) / kRows);
   if (ntiles <= 0) return;
   const uint16_t* xb = P.x + static_cast<int64_t>(b) * P.x_batch_stride;
+  // gathered rows: the CTA's 128 source rows resolved once (one load and one
+  // division per row) instead of in every staging pass
+  __shared__ int s_src[kTilesPerCta * kRows];
+  if (P.src_rows != nullptr) {
+    const int f = first + tid < P.rows ? P.src_rows[first + tid] : -1;
+    s_src[tid] = f < 0 ? -1 : f / P.src_div;
+    __syncthreads();
+  }
 
-  stage_tile(P, xb, first, c0, tile[0], tid);
+  stage_tile(P, xb, first, c0, tile[0], tid, s_src, first);
   for (int t = 0; t < ntiles; ++t) {
     const int p0 = first + t * kRows;
     if (t + 1 < ntiles) {
-      stage_tile(P, xb, p0 + kRows, c0, tile[(t + 1) & 1], tid);
+      stage_tile(P, xb, p0 + kRows, c0, tile[(t + 1) & 1], tid, s_src, first);
       asm volatile("cp.async.wait_group 1;" ::: "memory");
     } else {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
