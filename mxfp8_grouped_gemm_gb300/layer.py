@@ -65,13 +65,17 @@ class GroupedMLP:
         return int(self.dev_status.item())
 
     def gu_view(self) -> torch.Tensor:
-        """The gate-up GEMM output (bf16 [m_cap, 2I]) kept in the saved buffer."""
+        """The gate-up GEMM output (bf16 [m_cap, 2I]) kept in the saved buffer (MXFP8 path)."""
+        if self.bf16:
+            raise NotImplementedError("gu_view reads the MXFP8 path's saved layout")
         base = self.saved.data_ptr()
         off = _lib.mxg_mlp_saved_view(self.saved, self.T, self.H, self.I, self.E, self.k, 0) - base
         m_cap = self.padded_rows_capacity()
         return self.saved[off:off + m_cap * 2 * self.I * 2].view(torch.bfloat16).view(m_cap, 2 * self.I)
 
     def padded_offsets(self) -> torch.Tensor:
+        if self.bf16:
+            raise NotImplementedError("padded_offsets reads the MXFP8 path's saved layout")
         base = self.saved.data_ptr()
         off = _lib.mxg_mlp_saved_view(self.saved, self.T, self.H, self.I, self.E, self.k, 1) - base
         return self.saved[off:off + 4 * (self.E + 1)].view(torch.int32)
