@@ -30,7 +30,9 @@
  *     work instead of faulting.
  *   - bf16 tensors are passed as uint16_t bit patterns.  All matrices are
  *     row-major and dense unless stated otherwise.
- *   - Device pointers must be 16-byte aligned (MXG_ERR_ALIGN otherwise).
+ *   - Device pointers must be 32-byte aligned (MXG_ERR_ALIGN otherwise): the
+ *     GEMM epilogues read and write whole 32-byte sectors.  Allocations from
+ *     cudaMalloc and torch's caching allocator satisfy this.
  */
 #ifndef MXG_H_
 #define MXG_H_
@@ -46,7 +48,7 @@ typedef enum {
   MXG_OK = 0,
   MXG_ERR_ARG = 1,        /* null pointer, non-positive size, bad enum value        */
   MXG_ERR_SHAPE = 2,      /* a dimension violates the call's divisibility rules      */
-  MXG_ERR_ALIGN = 3,      /* a device pointer is not 16-byte aligned                 */
+  MXG_ERR_ALIGN = 3,      /* a device pointer is not 32-byte aligned                 */
   MXG_ERR_ARCH = 4,       /* current device is not sm_103 / library not built for it */
   MXG_ERR_WORKSPACE = 5,  /* caller's scratch/saved buffer is too small              */
   MXG_ERR_CUDA = 6,       /* a CUDA runtime call or kernel launch failed             */
@@ -98,7 +100,7 @@ int mxg_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float
  *   w_router  bf16 [E][H] (device)
  *   logits    fp32 [T][E] out, accumulated in fp32 from the bf16 products
  *   ids, probs  as mxg_route_topk
- * Requires H % 128 == 0, 1 <= k <= E <= 256, k <= 32.  x, w_router 16-byte
+ * Requires H % 128 == 0, 1 <= k <= E <= 256, k <= 32.  x, w_router 32-byte
  * aligned.
  */
 int mxg_router_fwd(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, float* logits,

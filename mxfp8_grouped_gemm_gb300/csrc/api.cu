@@ -18,7 +18,7 @@ namespace {
 constexpr int64_t kAlign = 256;
 
 inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // CTA-pair GEMM tiles (256 x 256 over two SMs) for the MLP's GEMMs whose
 // output width is a multiple of 256.  Measured on GB300 (Mixtral layer): the
@@ -138,7 +138,7 @@ const char* mxg_status_string(int status) {
     case MXG_OK: return "ok";
     case MXG_ERR_ARG: return "invalid argument (null pointer, non-positive size or bad enum)";
     case MXG_ERR_SHAPE: return "shape violates the call's divisibility rules";
-    case MXG_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case MXG_ERR_ALIGN: return "device pointer not 32-byte aligned";
     case MXG_ERR_ARCH: return "device is not sm_103 (GB300)";
     case MXG_ERR_WORKSPACE: return "scratch or saved buffer too small";
     case MXG_ERR_CUDA: return "CUDA runtime error or kernel launch failure";
@@ -164,7 +164,7 @@ int mxg_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float
   if (!logits || !ids || !probs) return MXG_ERR_ARG;
   if (T <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
   if (k > E || E > 256 || k > 32) return MXG_ERR_SHAPE;
-  if (!aligned16(logits) || !aligned16(ids) || !aligned16(probs)) return MXG_ERR_ALIGN;
+  if (!aligned32(logits) || !aligned32(ids) || !aligned32(probs)) return MXG_ERR_ALIGN;
   return cuda_status(launch_topk(logits, T, E, k, ids, probs, static_cast<cudaStream_t>(stream)));
 }
 
@@ -181,8 +181,8 @@ int mxg_route_permute(const int32_t* ids, int T, int k, int E, int32_t* split_si
     return MXG_ERR_ARG;
   if (T <= 0 || k <= 0 || E <= 0) return MXG_ERR_ARG;
   if (k > E || E > 256) return MXG_ERR_SHAPE;
-  if (!aligned16(ids) || !aligned16(split_sizes) || !aligned16(src_of_row) || !aligned16(row_of_src) ||
-      !aligned16(padded_offsets) || !aligned16(ws))
+  if (!aligned32(ids) || !aligned32(split_sizes) || !aligned32(src_of_row) || !aligned32(row_of_src) ||
+      !aligned32(padded_offsets) || !aligned32(ws))
     return MXG_ERR_ALIGN;
   if (ws_bytes < mxg_route_permute_workspace_bytes(T, k, E)) return MXG_ERR_WORKSPACE;
   const int64_t nblk = permute_num_blocks(T * k);
@@ -211,7 +211,7 @@ int mxg_mxfp8_quantize(const uint16_t* x, int rows, int cols, uint8_t* q_row, ui
   // the kernel tiles 32 rows x 128 columns
   if (rows % 32 || cols % 128) return MXG_ERR_SHAPE;
   if (layout == MXG_LAYOUT_MMA && rows % 128) return MXG_ERR_SHAPE;
-  if (!aligned16(x) || (q_row && !aligned16(q_row)) || (q_col && !aligned16(q_col))) return MXG_ERR_ALIGN;
+  if (!aligned32(x) || (q_row && !aligned32(q_row)) || (q_col && !aligned32(q_col))) return MXG_ERR_ALIGN;
   QuantParams p{};
   p.x = x;
   p.ld_x = cols;
@@ -237,8 +237,8 @@ int mxg_grouped_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, cons
   if (!a || !sa || !b || !sb || !padded_offsets || !d || !dev_status) return MXG_ERR_ARG;
   if (E <= 0 || m_cap <= 0 || N <= 0 || K <= 0) return MXG_ERR_ARG;
   if (E > 256 || K % 128 || N % 128 || m_cap % 128) return MXG_ERR_SHAPE;
-  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(d) ||
-      !aligned16(padded_offsets))
+  if (!aligned32(a) || !aligned32(sa) || !aligned32(b) || !aligned32(sb) || !aligned32(d) ||
+      !aligned32(padded_offsets))
     return MXG_ERR_ALIGN;
   GemmArgs g{};
   g.epi = EPI_BF16;
@@ -270,8 +270,8 @@ int mxg_debug_grouped_gemm_stall(const uint8_t* a, const uint8_t* sa, const uint
   if (!a || !sa || !b || !sb || !padded_offsets || !d || !dev_status) return MXG_ERR_ARG;
   if (E <= 0 || m_cap <= 0 || N <= 0 || K <= 0 || wait_limit_ns == 0) return MXG_ERR_ARG;
   if (E > 256 || K % 128 || N % 128 || m_cap % 128) return MXG_ERR_SHAPE;
-  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(d) ||
-      !aligned16(padded_offsets))
+  if (!aligned32(a) || !aligned32(sa) || !aligned32(b) || !aligned32(sb) || !aligned32(d) ||
+      !aligned32(padded_offsets))
     return MXG_ERR_ALIGN;
   GemmArgs g{};
   g.epi = EPI_BF16;
@@ -304,8 +304,8 @@ int mxg_grouped_gemm_wgrad(const uint8_t* a, const uint8_t* sa, const uint8_t* b
   if (!a || !sa || !b || !sb || !padded_offsets || !d || !dev_status) return MXG_ERR_ARG;
   if (E <= 0 || M <= 0 || N <= 0 || t_cap <= 0) return MXG_ERR_ARG;
   if (E > 256 || M % 128 || N % 128 || t_cap % 128) return MXG_ERR_SHAPE;
-  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(d) ||
-      !aligned16(padded_offsets))
+  if (!aligned32(a) || !aligned32(sa) || !aligned32(b) || !aligned32(sb) || !aligned32(d) ||
+      !aligned32(padded_offsets))
     return MXG_ERR_ALIGN;
   GemmArgs g{};
   g.epi = EPI_BF16;
@@ -365,9 +365,9 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   if (!A->x || !A->ids || !A->probs || !A->w_gate_up || !A->w_down || !A->y || !A->split_sizes || !A->saved ||
       !A->workspace || !A->dev_status)
     return MXG_ERR_ARG;
-  if (!aligned16(A->x) || !aligned16(A->ids) || !aligned16(A->probs) || !aligned16(A->w_gate_up) ||
-      !aligned16(A->w_down) || !aligned16(A->y) || !aligned16(A->split_sizes) || !aligned16(A->saved) ||
-      !aligned16(A->workspace))
+  if (!aligned32(A->x) || !aligned32(A->ids) || !aligned32(A->probs) || !aligned32(A->w_gate_up) ||
+      !aligned32(A->w_down) || !aligned32(A->y) || !aligned32(A->split_sizes) || !aligned32(A->saved) ||
+      !aligned32(A->workspace))
     return MXG_ERR_ALIGN;
   const Plan pl(T, H, I, E, k);
   if (A->saved_bytes < static_cast<uint64_t>(pl.saved_bytes) ||
@@ -550,8 +550,8 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   if (!A->dy || !A->saved || !A->dx || !A->dw_gate_up || !A->dw_down || !A->dprobs || !A->workspace ||
       !A->dev_status)
     return MXG_ERR_ARG;
-  if (!aligned16(A->dy) || !aligned16(A->saved) || !aligned16(A->dx) || !aligned16(A->dw_gate_up) ||
-      !aligned16(A->dw_down) || !aligned16(A->dprobs) || !aligned16(A->workspace))
+  if (!aligned32(A->dy) || !aligned32(A->saved) || !aligned32(A->dx) || !aligned32(A->dw_gate_up) ||
+      !aligned32(A->dw_down) || !aligned32(A->dprobs) || !aligned32(A->workspace))
     return MXG_ERR_ALIGN;
   const Plan pl(T, H, I, E, k);
   if (A->saved_bytes < static_cast<uint64_t>(pl.saved_bytes) ||

@@ -24,7 +24,7 @@ constexpr int64_t kAlign = 256;
 constexpr int kGroupAlign = 256;   // CTA-pair tile height
 
 inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 struct Carver {
   int64_t off = 0;
@@ -129,9 +129,9 @@ int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   if (!A->x || !A->ids || !A->probs || !A->w_gate_up || !A->w_down || !A->y || !A->split_sizes || !A->saved ||
       !A->workspace || !A->dev_status)
     return MXG_ERR_ARG;
-  if (!aligned16(A->x) || !aligned16(A->ids) || !aligned16(A->probs) || !aligned16(A->w_gate_up) ||
-      !aligned16(A->w_down) || !aligned16(A->y) || !aligned16(A->split_sizes) || !aligned16(A->saved) ||
-      !aligned16(A->workspace))
+  if (!aligned32(A->x) || !aligned32(A->ids) || !aligned32(A->probs) || !aligned32(A->w_gate_up) ||
+      !aligned32(A->w_down) || !aligned32(A->y) || !aligned32(A->split_sizes) || !aligned32(A->saved) ||
+      !aligned32(A->workspace))
     return MXG_ERR_ALIGN;
   const PlanBf pl(T, H, I, E, k);
   if (A->saved_bytes < static_cast<uint64_t>(pl.saved_bytes) ||
@@ -257,8 +257,8 @@ int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   if (!A->dy || !A->saved || !A->dx || !A->dw_gate_up || !A->dw_down || !A->dprobs || !A->workspace ||
       !A->dev_status)
     return MXG_ERR_ARG;
-  if (!aligned16(A->dy) || !aligned16(A->saved) || !aligned16(A->dx) || !aligned16(A->dw_gate_up) ||
-      !aligned16(A->dw_down) || !aligned16(A->dprobs) || !aligned16(A->workspace))
+  if (!aligned32(A->dy) || !aligned32(A->saved) || !aligned32(A->dx) || !aligned32(A->dw_gate_up) ||
+      !aligned32(A->dw_down) || !aligned32(A->dprobs) || !aligned32(A->workspace))
     return MXG_ERR_ALIGN;
   const PlanBf pl(T, H, I, E, k);
   if (A->saved_bytes < static_cast<uint64_t>(pl.saved_bytes) ||

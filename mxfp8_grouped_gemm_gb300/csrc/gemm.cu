@@ -97,17 +97,15 @@ struct TileCoord {
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
+// 32 bf16 of a read-only global row (64 bytes, 32-byte aligned) as fp32.
 __device__ __forceinline__ void load_bf16_32(const uint16_t* src, float (&v)[32]) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint32_t w[16];
+  ld_global_nc_v8(src, w);
+  ld_global_nc_v8(src + 16, w + 8);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 q = s[i];
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[8 * i + 2 * j] = u2f(w[j] << 16);
-      v[8 * i + 2 * j + 1] = u2f(w[j] & 0xffff0000u);
-    }
+  for (int j = 0; j < 16; ++j) {
+    v[2 * j] = u2f(w[j] << 16);
+    v[2 * j + 1] = u2f(w[j] & 0xffff0000u);
   }
 }
 
@@ -137,9 +135,7 @@ __device__ __forceinline__ uint32_t row_quant32(const float (&h)[32], uint8_t* d
   for (int i = 0; i < 32; ++i) v[i] = h[i] * inv;
   uint32_t w[8];
   encode32(v, w);
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  st_global_v8(dst, w);
   return sb;
 }
 
@@ -193,11 +189,11 @@ __device__ __forceinline__ void col_quant32_xpose(const float (&h)[32], float* x
 // one 64-byte run of its row, and the transposed copy (column col0+i, row
 // tok0+lane: for each column the warp writes 32 consecutive bf16).
 __device__ __forceinline__ void row_store_bf16(const float (&h)[32], uint16_t* dst) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+  uint32_t w[16];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    d[i] = make_uint4(pack_bf16x2(h[8 * i], h[8 * i + 1]), pack_bf16x2(h[8 * i + 2], h[8 * i + 3]),
-                      pack_bf16x2(h[8 * i + 4], h[8 * i + 5]), pack_bf16x2(h[8 * i + 6], h[8 * i + 7]));
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(h[2 * i], h[2 * i + 1]);
+  st_global_v8(dst, w);
+  st_global_v8(dst + 16, w + 8);
 }
 __device__ __forceinline__ void col_store_bf16(const float (&h)[32], uint16_t* yc, int64_t ld, int64_t col0,
                                                int64_t tok0, int lane) {
@@ -256,10 +252,8 @@ __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc,
   uint16_t* drow = KG ? P.d + static_cast<int64_t>(tc.e) * P.M * P.N + static_cast<int64_t>(tc.m0 + row) * P.N +
                             tc.nt * BN + hf * COLS
                       : P.d + static_cast<int64_t>(tc.m0 + row) * P.ldd + tc.nt * BN + hf * COLS;
-  uint4* d = reinterpret_cast<uint4*>(drow);
 #pragma unroll
-  for (int j = 0; j < COLS / 8; ++j)
-    d[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+  for (int j = 0; j < COLS / 16; ++j) st_global_v8(drow + 16 * j, packed + 8 * j);
 }
 
 // Gate-up tile: accumulator columns [0, BN/2) = gate j0.., [BN/2, BN) = up j0..
@@ -301,13 +295,11 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& t
         gp[i] = pack_bf16x2(u2f(g[c][2 * i]), u2f(g[c][2 * i + 1]));
         up[i] = pack_bf16x2(u2f(u[c][2 * i]), u2f(u[c][2 * i + 1]));
       }
-      uint4* gs = reinterpret_cast<uint4*>(P.gu_save + r * (2 * I) + col);
-      uint4* us = reinterpret_cast<uint4*>(P.gu_save + r * (2 * I) + I + col);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        gs[j] = make_uint4(gp[4 * j], gp[4 * j + 1], gp[4 * j + 2], gp[4 * j + 3]);
-        us[j] = make_uint4(up[4 * j], up[4 * j + 1], up[4 * j + 2], up[4 * j + 3]);
-      }
+      uint16_t* gs = P.gu_save + r * (2 * I) + col;
+      st_global_v8(gs, gp);
+      st_global_v8(gs + 16, gp + 8);
+      st_global_v8(gs + I, up);
+      st_global_v8(gs + I + 16, up + 8);
     }
     if constexpr (BF) {
       row_store_bf16(h, P.y_row + r * P.y_row_ld + col);
@@ -399,8 +391,8 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
     const int64_t col = j0 + c * 32;
     float dh[32], g[32], u[32], dg[32];
     unpack_bf16_32(reinterpret_cast<const uint4*>(srow + c * 32), dh);
-    unpack_bf16_32(reinterpret_cast<const uint4*>(P.gu_save + r * (2 * I) + col), g);
-    unpack_bf16_32(reinterpret_cast<const uint4*>(P.gu_save + r * (2 * I) + I + col), u);
+    load_bf16_32(P.gu_save + r * (2 * I) + col, g);
+    load_bf16_32(P.gu_save + r * (2 * I) + I + col, u);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float gf = g[i], uf = u[i];

@@ -65,7 +65,7 @@ extern "C" int mxg_route_permute_noalloc(const int32_t* ids, int T, int k, int E
   const uintptr_t mis = reinterpret_cast<uintptr_t>(ids) | reinterpret_cast<uintptr_t>(split_sizes) |
                         reinterpret_cast<uintptr_t>(src_of_row) | reinterpret_cast<uintptr_t>(row_of_src) |
                         reinterpret_cast<uintptr_t>(padded_offsets);
-  if (mis & 15u) return MXG_ERR_ALIGN;
+  if (mis & 31u) return MXG_ERR_ALIGN;
   int32_t* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return MXG_ERR_CUDA;
   const int nblk = permute_num_blocks(static_cast<int>(R));

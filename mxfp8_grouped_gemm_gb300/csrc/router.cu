@@ -352,7 +352,7 @@ extern "C" int mxg_router_fwd(const uint16_t* x, const uint16_t* w_router, int T
   if (!x || !w_router || !logits || !ids || !probs) return MXG_ERR_ARG;
   if (T <= 0 || H <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
   if (!router_shape_ok(T, H, E, k, kHChunk)) return MXG_ERR_SHAPE;
-  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_router)) & 15u) return MXG_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_router)) & 31u) return MXG_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t wbytes = static_cast<size_t>(E) * H * 2;
   if (E <= kStreamMaxE && wbytes <= kStreamMaxW) {
@@ -389,7 +389,7 @@ extern "C" int mxg_router_bwd(const uint16_t* x, const uint16_t* w_router, const
   if (T <= 0 || H <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
   if (!router_shape_ok(T, H, E, k, kDwCols)) return MXG_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_router) | reinterpret_cast<uintptr_t>(dx) |
-       reinterpret_cast<uintptr_t>(workspace)) & 15u)
+       reinterpret_cast<uintptr_t>(workspace)) & 31u)
     return MXG_ERR_ALIGN;
   if (workspace_bytes < mxg_router_bwd_workspace_bytes(T, H, E, k)) return MXG_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
