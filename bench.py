@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-router", action="store_true", help="skip timing the router front end")
+    ap.add_argument("--no-accum", action="store_true",
+                    help="skip timing gradient-accumulation micro-batches (weight cache + fp32 main_grad)")
     ap.add_argument("--precision", choices=["mxfp8", "bf16"], default="mxfp8",
                     help="bf16: the like-for-like BF16 grouped MLP instead of the MXFP8 path")
     return ap.parse_args()
@@ -332,6 +334,56 @@ def run_ours(args, rank, world):
         router = {"fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4),
                   "fwd_gbs": round(fb / (f_ms * 1e-3) / 1e9, 1), "bwd_gbs": round(bb / (b_ms * 1e-3) / 1e9, 1),
                   "note": "not part of the MLP step above"}
+    # ---- gradient accumulation (MXFP8 path): the weights quantised once into
+    # a weight cache per optimizer step, then micro-batches whose weight
+    # gradients are added into fp32 main_grad buffers; reported beside the step
+    accum = None
+    if args.precision == "mxfp8" and not args.no_accum:
+        mg = (torch.zeros((E, 2 * I, H), dtype=torch.float32, device=dev),
+              torch.zeros((E, H, I), dtype=torch.float32, device=dev))
+
+        def microbatch():
+            ids_, probs_ = layer.route(d["logits"])
+            layer.forward(d["x"], ids_, probs_)
+            layer.backward(d["dy"], main_grad=mg)
+        layer.quantize_weights(d["w_gate_up"], d["w_down"])
+        for _ in range(2):
+            microbatch()
+        def microbatch_bf16_dw():
+            ids_, probs_ = layer.route(d["logits"])
+            layer.forward(d["x"], ids_, probs_)
+            layer.backward(d["dy"])
+        reps = max(3, min(args.steps, 10))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        torch.cuda.synchronize(dev)
+        ev[0].record(stream)
+        layer.quantize_weights(d["w_gate_up"], d["w_down"])
+        ev[1].record(stream)
+        for _ in range(reps):
+            microbatch()
+        ev[2].record(stream)
+        for _ in range(reps):
+            microbatch_bf16_dw()
+        ev[3].record(stream)
+        wg = [m.BWD_STAGES.index("wgrad_down"), m.BWD_STAGES.index("wgrad_gate_up")]
+        for _ in range(reps):
+            layer.backward(d["dy"], stage=wg[0], main_grad=mg)
+        ev[4].record(stream)
+        for _ in range(reps):
+            layer.backward(d["dy"], stage=wg[1], main_grad=mg)
+        ev[5].record(stream)
+        torch.cuda.synchronize(dev)
+        q_ms = ev[0].elapsed_time(ev[1])
+        mb_ms, mb16_ms = ev[1].elapsed_time(ev[2]) / reps, ev[2].elapsed_time(ev[3]) / reps
+        accum = {"quantize_weights_ms": round(q_ms, 4),
+                 "ms_per_microbatch": round(mb_ms, 4),
+                 "tflops_per_microbatch": round(wl.gemm_flops(True) / (mb_ms * 1e-3) / 1e12, 2),
+                 "ms_per_microbatch_bf16_dw": round(mb16_ms, 4),
+                 "wgrad_main_grad_ms": {"wgrad_down": round(ev[3].elapsed_time(ev[4]) / reps, 4),
+                                        "wgrad_gate_up": round(ev[4].elapsed_time(ev[5]) / reps, 4)},
+                 "note": "weights quantised once per optimizer step (weight cache); each micro-batch runs "
+                         "route, forward and backward with dW added into fp32 main_grad (bf16_dw: dW written "
+                         "in bf16 instead); not the step above"}
     clk = clocks.stop()
     if layer.status() != 0:
         raise SystemExit(f"bench: device status {m.status_string(layer.status())}")
@@ -399,6 +451,8 @@ def run_ours(args, rank, world):
     }
     if router:
         res["router"] = router
+    if accum:
+        res["accumulation"] = accum
     if e2e:
         res["e2e"] = {"value": round(world * flops / (e2e["ms"] * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                       "ms_per_step": round(e2e["ms"], 4), "h2d_bytes_per_step": e2e["h2d"],

@@ -260,6 +260,12 @@ typedef struct {
   uint64_t workspace_bytes;
   int32_t save_for_backward; /* 0: inference (skips what only backward needs) */
   int32_t* dev_status;
+  /* Optional weight cache (NULL: quantise w_gate_up / w_down in this call).
+   * When given, the forward skips the weight quantisation stage and reads the
+   * MXFP8 weights written by mxg_mlp_quantize_weights(); w_gate_up and w_down
+   * may then be NULL, and `saved` needs only mxg_mlp_saved_bytes_cached(). */
+  const void* weight_cache;
+  uint64_t weight_cache_bytes;
 } mxg_mlp_fwd_args;
 
 typedef struct {
@@ -274,6 +280,17 @@ typedef struct {
   void* workspace;
   uint64_t workspace_bytes;
   int32_t* dev_status;
+  /* The weight cache the forward used (NULL if it quantised the weights
+   * itself); it must be unchanged since that forward. */
+  const void* weight_cache;
+  uint64_t weight_cache_bytes;
+  /* Optional fp32 gradient accumulators (main_grad), both or neither.  When
+   * given, the weight gradients are added into them in fp32 straight from the
+   * GEMM accumulators (a buffer's element belongs to one output tile, so the
+   * update is deterministic) and dw_gate_up / dw_down are not written (they
+   * may be NULL).  Experts without tokens leave their slices unchanged. */
+  float* main_grad_gate_up;  /* in/out fp32 [E][2I][H]                       */
+  float* main_grad_down;     /* in/out fp32 [E][H][I]                        */
 } mxg_mlp_bwd_args;
 
 /* The forward and backward are sequences of stages, each one kernel launch
@@ -312,6 +329,25 @@ size_t mxg_mlp_workspace_bytes(int T, int H, int I, int E, int k);
 int mxg_grouped_mlp_fwd(const mxg_mlp_fwd_args* args, void* stream);
 int mxg_grouped_mlp_bwd(const mxg_mlp_bwd_args* args, void* stream);
 
+/* Weight cache: the four MXFP8 weight tensors the MLP needs (W_gate_up
+ * quantised along H and along 2I, W_down along I and along H, codes and
+ * tensor-core scale layout), written once per weight update and reused by
+ * every forward / backward until the weights change (micro-batches of one
+ * optimizer step).  This is the forward's weight stage on its own ("Fusing
+ * precision conversion and expert computation": the recipe converts the bf16
+ * master weights to MXFP8 before the GEMMs).
+ *   mxg_mlp_weight_cache_bytes: bytes of the cache (0 for unsupported shapes).
+ *   mxg_mlp_quantize_weights: w_gate_up bf16 [E][2I][H], w_down bf16 [E][H][I]
+ *     (device) -> cache (device, caller-owned, >= cache_bytes).  Async on
+ *     `stream`; MXG_ERR_SHAPE / MXG_ERR_ALIGN / MXG_ERR_WORKSPACE before any
+ *     launch.
+ *   mxg_mlp_saved_bytes_cached: the `saved` size when the forward is given a
+ *     weight cache (the transposed weights then live in the cache only). */
+size_t mxg_mlp_weight_cache_bytes(int H, int I, int E);
+int mxg_mlp_quantize_weights(const uint16_t* w_gate_up, const uint16_t* w_down, int H, int I, int E, void* cache,
+                             size_t cache_bytes, void* stream);
+size_t mxg_mlp_saved_bytes_cached(int T, int H, int I, int E, int k);
+
 /* ----------------------------------------------------------------------------
  * The same grouped expert MLP in BF16: bf16 operands on the tensor cores with
  * fp32 accumulation, no quantisation; h and dGU are kept in bf16.  The like-
@@ -319,7 +355,8 @@ int mxg_grouped_mlp_bwd(const mxg_mlp_bwd_args* args, void* stream);
  * 5, compares the recipe's BF16 and MXFP8 runs).  Arguments, stages, outputs,
  * ownership and errors as mxg_grouped_mlp_fwd / _bwd, with `saved` and
  * `workspace` sized by the two _bf16_ queries (a saved buffer of one precision
- * cannot be passed to the other's backward).  Requires H % 256 == 0 and
+ * cannot be passed to the other's backward; weight_cache and the main_grad
+ * pointers must be NULL: MXG_ERR_ARG otherwise).  Requires H % 256 == 0 and
  * I % 256 == 0 (every GEMM runs as 256 x 256 CTA-pair tiles; expert groups
  * start on multiples of 256 padded rows).
  */

@@ -32,6 +32,7 @@ EXPORTS = [
     "mxg_mlp_row_capacity", "mxg_debug_grouped_gemm_stall", "mxg_router_fwd", "mxg_router_bwd_workspace_bytes",
     "mxg_router_bwd", "mxg_mlp_bf16_saved_bytes", "mxg_mlp_bf16_workspace_bytes", "mxg_grouped_mlp_bf16_fwd",
     "mxg_grouped_mlp_bf16_bwd", "mxg_grouped_mlp_bf16_fwd_stage", "mxg_grouped_mlp_bf16_bwd_stage",
+    "mxg_mlp_weight_cache_bytes", "mxg_mlp_quantize_weights", "mxg_mlp_saved_bytes_cached",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -51,7 +52,8 @@ class MlpFwdArgs(ctypes.Structure):
                 ("y", ctypes.c_void_p), ("split_sizes", ctypes.c_void_p), ("saved", ctypes.c_void_p),
                 ("saved_bytes", ctypes.c_uint64), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_uint64), ("save_for_backward", ctypes.c_int32),
-                ("dev_status", ctypes.c_void_p)]
+                ("dev_status", ctypes.c_void_p), ("weight_cache", ctypes.c_void_p),
+                ("weight_cache_bytes", ctypes.c_uint64)]
 
 
 class MlpBwdArgs(ctypes.Structure):
@@ -59,7 +61,9 @@ class MlpBwdArgs(ctypes.Structure):
                 ("k", ctypes.c_int32), ("dy", ctypes.c_void_p), ("saved", ctypes.c_void_p),
                 ("saved_bytes", ctypes.c_uint64), ("dx", ctypes.c_void_p), ("dw_gate_up", ctypes.c_void_p),
                 ("dw_down", ctypes.c_void_p), ("dprobs", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_uint64), ("dev_status", ctypes.c_void_p)]
+                ("workspace_bytes", ctypes.c_uint64), ("dev_status", ctypes.c_void_p),
+                ("weight_cache", ctypes.c_void_p), ("weight_cache_bytes", ctypes.c_uint64),
+                ("main_grad_gate_up", ctypes.c_void_p), ("main_grad_down", ctypes.c_void_p)]
 
 
 _lib = None
@@ -105,6 +109,9 @@ def lib() -> ctypes.CDLL:
         "mxg_grouped_mlp_bf16_bwd_stage": (I32, [ctypes.POINTER(MlpBwdArgs), I32, P]),
         "mxg_router_bwd_workspace_bytes": (SZ, [I32, I32, I32, I32]),
         "mxg_router_bwd": (I32, [P, P, P, P, P, I32, I32, I32, I32, P, P, P, SZ, P, P]),
+        "mxg_mlp_weight_cache_bytes": (SZ, [I32, I32, I32]),
+        "mxg_mlp_quantize_weights": (I32, [P, P, I32, I32, I32, P, SZ, P]),
+        "mxg_mlp_saved_bytes_cached": (SZ, [I32, I32, I32, I32, I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -143,8 +150,8 @@ def _stream(stream) -> int | None:
     return int(stream)
 
 
-def _bits(t: torch.Tensor) -> torch.Tensor:
-    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+def _bits(t: torch.Tensor | None) -> torch.Tensor | None:
+    return t.view(torch.int16) if t is not None and t.dtype == torch.bfloat16 else t
 
 
 # ------------------------------------------------------------------ entries --
@@ -290,21 +297,62 @@ def mxg_mlp_saved_view(saved: torch.Tensor, T, H, I, E, k, which: int) -> int:
     return int(lib().mxg_mlp_saved_view(_ptr(saved), T, H, I, E, k, which) or 0)
 
 
+class WeightCache:
+    """The MXFP8 weights of one expert MLP (all four orientations), written by
+    mxg_mlp_quantize_weights and read by forward / backward calls until the
+    weights change."""
+
+    def __init__(self, H: int, I: int, E: int, device="cuda"):
+        n = int(lib().mxg_mlp_weight_cache_bytes(H, I, E))
+        if n == 0:
+            raise ValueError(f"unsupported weight shape H={H} I={I} E={E}")
+        self.H, self.I, self.E = H, I, E
+        self.buffer = torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def mxg_mlp_saved_bytes_cached(T, H, I, E, k) -> int:
+    return int(lib().mxg_mlp_saved_bytes_cached(T, H, I, E, k))
+
+
+def mxg_mlp_quantize_weights(w_gate_up, w_down, cache: WeightCache | None = None, stream=None) -> WeightCache:
+    """Quantise the bf16 expert weights into a weight cache (allocated if not given)."""
+    E, N2, H = w_gate_up.shape
+    I = N2 // 2
+    if tuple(w_down.shape) != (E, H, I):
+        raise ValueError(f"w_down must be [E, H, I] = {(E, H, I)}, got {tuple(w_down.shape)}")
+    cache = WeightCache(H, I, E, w_gate_up.device) if cache is None else cache
+    if (cache.H, cache.I, cache.E) != (H, I, E):
+        raise ValueError("weight cache was made for another shape")
+    _check("mxg_mlp_quantize_weights",
+           lib().mxg_mlp_quantize_weights(_ptr(_bits(w_gate_up), torch.int16, "w_gate_up"),
+                                          _ptr(_bits(w_down), torch.int16, "w_down"), H, I, E,
+                                          _ptr(cache.buffer, torch.uint8, "cache"), cache.buffer.numel(),
+                                          _stream(stream)))
+    return cache
+
+
 def mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, saved, workspace, dev_status, y=None, split_sizes=None,
-                        save_for_backward: bool = True, stream=None, stage: int | None = None, bf16: bool = False):
+                        save_for_backward: bool = True, stream=None, stage: int | None = None, bf16: bool = False,
+                        weight_cache: WeightCache | None = None):
     """Full forward, or one stage of it (FWD_STAGES index) when ``stage`` is given
-    (``bf16``: the BF16 path, mxg_grouped_mlp_bf16_fwd)."""
+    (``bf16``: the BF16 path, mxg_grouped_mlp_bf16_fwd).  With ``weight_cache``
+    the weights are read from it and w_gate_up / w_down may be None."""
     T, H = x.shape
     k = ids.shape[1]
-    E, N2, _ = w_gate_up.shape
-    I = N2 // 2
+    if weight_cache is not None:
+        E, I = weight_cache.E, weight_cache.I
+    else:
+        E, N2, _ = w_gate_up.shape
+        I = N2 // 2
     y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if y is None else y
     split_sizes = torch.empty(E, dtype=torch.int32, device=x.device) if split_sizes is None else split_sizes
     a = MlpFwdArgs(T, H, I, E, k, _ptr(_bits(x), torch.int16, "x"), _ptr(ids, torch.int32, "ids"),
                    _ptr(probs, torch.float32, "probs"), _ptr(_bits(w_gate_up), torch.int16, "w_gate_up"),
                    _ptr(_bits(w_down), torch.int16, "w_down"), _ptr(_bits(y)), _ptr(split_sizes, torch.int32),
                    _ptr(saved, torch.uint8, "saved"), saved.numel(), _ptr(workspace, torch.uint8, "workspace"),
-                   workspace.numel(), 1 if save_for_backward else 0, _ptr(dev_status, torch.int32, "dev_status"))
+                   workspace.numel(), 1 if save_for_backward else 0, _ptr(dev_status, torch.int32, "dev_status"),
+                   None if weight_cache is None else _ptr(weight_cache.buffer, torch.uint8, "weight_cache"),
+                   0 if weight_cache is None else weight_cache.buffer.numel())
     name = "mxg_grouped_mlp_bf16_fwd" if bf16 else "mxg_grouped_mlp_fwd"
     if stage is None:
         _check(name, getattr(lib(), name)(ctypes.byref(a), _stream(stream)))
@@ -314,22 +362,37 @@ def mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, saved, workspace, dev_
 
 
 def mxg_grouped_mlp_bwd(dy, saved, workspace, dev_status, E: int, I: int, k: int, dx=None, dw_gate_up=None,
-                        dw_down=None, dprobs=None, stream=None, stage: int | None = None, bf16: bool = False):
+                        dw_down=None, dprobs=None, stream=None, stage: int | None = None, bf16: bool = False,
+                        weight_cache: WeightCache | None = None, main_grad=None):
     """Full backward, or one stage of it (BWD_STAGES index) when ``stage`` is given
-    (``bf16``: the BF16 path, mxg_grouped_mlp_bf16_bwd)."""
+    (``bf16``: the BF16 path, mxg_grouped_mlp_bf16_bwd).  ``weight_cache``: the
+    cache the forward used.  ``main_grad`` = (fp32 [E, 2I, H], fp32 [E, H, I]):
+    the weight gradients are added into these and returned in place of dW."""
     T, H = dy.shape
     dev = dy.device
     dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if dx is None else dx
-    dw_gate_up = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev) if dw_gate_up is None else dw_gate_up
-    dw_down = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev) if dw_down is None else dw_down
+    if main_grad is not None:
+        mg_gu, mg_d = main_grad
+        if tuple(mg_gu.shape) != (E, 2 * I, H) or tuple(mg_d.shape) != (E, H, I):
+            raise ValueError("main_grad must be fp32 [E, 2I, H] and [E, H, I]")
+        dw_gate_up = dw_down = None
+    else:
+        mg_gu = mg_d = None
+        dw_gate_up = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev) if dw_gate_up is None else dw_gate_up
+        dw_down = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev) if dw_down is None else dw_down
     dprobs = torch.empty((T, k), dtype=torch.float32, device=dev) if dprobs is None else dprobs
     a = MlpBwdArgs(T, H, I, E, k, _ptr(_bits(dy), torch.int16, "dy"), _ptr(saved, torch.uint8, "saved"),
                    saved.numel(), _ptr(_bits(dx)), _ptr(_bits(dw_gate_up)), _ptr(_bits(dw_down)),
                    _ptr(dprobs, torch.float32), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
-                   _ptr(dev_status, torch.int32, "dev_status"))
+                   _ptr(dev_status, torch.int32, "dev_status"),
+                   None if weight_cache is None else _ptr(weight_cache.buffer, torch.uint8, "weight_cache"),
+                   0 if weight_cache is None else weight_cache.buffer.numel(),
+                   _ptr(mg_gu, torch.float32, "main_grad_gate_up"), _ptr(mg_d, torch.float32, "main_grad_down"))
     name = "mxg_grouped_mlp_bf16_bwd" if bf16 else "mxg_grouped_mlp_bwd"
     if stage is None:
         _check(name, getattr(lib(), name)(ctypes.byref(a), _stream(stream)))
     else:
         _check(name + "_stage", getattr(lib(), name + "_stage")(ctypes.byref(a), stage, _stream(stream)))
+    if main_grad is not None:
+        return dx, mg_gu, mg_d, dprobs
     return dx, dw_gate_up, dw_down, dprobs

@@ -44,7 +44,8 @@ struct Carver {
 struct Plan {
   int64_t T, H, I, E, k, R, Rc;
   // saved (forward -> backward)
-  int64_t poff, prow_src, prow_of_src, probs_perm, gu, xc, sxc, hc, shc, wguT, swguT, wdT, swdT, saved_bytes;
+  int64_t poff, prow_src, prow_of_src, probs_perm, gu, xc, sxc, hc, shc, wguT, swguT, wdT, swdT, saved_bytes,
+      saved_cached_bytes;
   // forward scratch
   int64_t counts, bases, offsets, xq, sxq, hq, shq, wgu, swgu, wd, swd, yperm, fwd_bytes;
   // backward scratch
@@ -69,6 +70,7 @@ struct Plan {
     wdT = s.take(E * I * H);
     swdT = s.take(E * I * H / 32);
     saved_bytes = s.off;
+    saved_cached_bytes = wguT;   // the transposed weights are the last part of `saved`
 
     Carver f;
     const int64_t nblk = permute_num_blocks(static_cast<int>(R));
@@ -103,6 +105,24 @@ struct Plan {
   int64_t ws_bytes() const { return fwd_bytes > bwd_bytes ? fwd_bytes : bwd_bytes; }
 };
 
+// Byte offsets inside a weight cache: the four MXFP8 weight tensors (codes,
+// then tensor-core scales) in the order the forward and backward read them.
+struct WPlan {
+  int64_t wgu, swgu, wd, swd, wguT, swguT, wdT, swdT, bytes;
+  WPlan(int64_t H, int64_t I, int64_t E) {
+    Carver c;
+    wgu = c.take(E * 2 * I * H);
+    swgu = c.take(E * 2 * I * H / 32);
+    wd = c.take(E * H * I);
+    swd = c.take(E * H * I / 32);
+    wguT = c.take(E * H * 2 * I);
+    swguT = c.take(E * H * 2 * I / 32);
+    wdT = c.take(E * I * H);
+    swdT = c.take(E * I * H / 32);
+    bytes = c.off;
+  }
+};
+
 template <typename T>
 inline T* at(void* base, int64_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
@@ -124,6 +144,50 @@ bool mlp_shape_ok(int T, int H, int I, int E, int k) {
   if (H % 128 || I % 128) return false;
   if (k > E || E > 256 || k > 32) return false;
   return true;
+}
+
+// F4: W_gate_up and W_down, both orientations in one pass each: row-wise (the
+// forward GEMMs' B, MX along H / I) and column-wise (the dgrad GEMMs' B, MX
+// along 2I / H; skipped when q_guT is null).
+cudaError_t launch_weight_quant(const uint16_t* w_gate_up, const uint16_t* w_down, int64_t H, int64_t I, int64_t E,
+                                uint8_t* q_gu, uint8_t* s_gu, uint8_t* q_guT, uint8_t* s_guT, uint8_t* q_d,
+                                uint8_t* s_d, uint8_t* q_dT, uint8_t* s_dT, cudaStream_t s) {
+  QuantParams wq{};
+  wq.x = w_gate_up;
+  wq.ld_x = H;
+  wq.x_batch_stride = 2 * I * H;
+  wq.src_div = 1;
+  wq.rows = static_cast<int32_t>(2 * I);
+  wq.cols = static_cast<int32_t>(H);
+  wq.batch = static_cast<int32_t>(E);
+  wq.q_row = q_gu;
+  wq.s_row = s_gu;
+  wq.sf_row_rows = E * 2 * I;
+  if (q_guT != nullptr) {
+    wq.q_col = q_guT;
+    wq.s_col = s_guT;
+    wq.ld_col = 2 * I;
+    wq.sf_col_rows = E * H;
+  }
+  wq.layout = MXG_LAYOUT_MMA;
+  cudaError_t err = launch_quant(wq, s);
+  if (err != cudaSuccess) return err;
+  QuantParams dq = wq;
+  dq.x = w_down;
+  dq.ld_x = I;
+  dq.x_batch_stride = H * I;
+  dq.rows = static_cast<int32_t>(H);
+  dq.cols = static_cast<int32_t>(I);
+  dq.q_row = q_d;
+  dq.s_row = s_d;
+  dq.sf_row_rows = E * H;
+  if (q_dT != nullptr) {
+    dq.q_col = q_dT;
+    dq.s_col = s_dT;
+    dq.ld_col = H;
+    dq.sf_col_rows = E * I;
+  }
+  return launch_quant(dq, s);
 }
 
 }  // namespace
@@ -346,6 +410,31 @@ size_t mxg_mlp_workspace_bytes(int T, int H, int I, int E, int k) {
   return static_cast<size_t>(Plan(T, H, I, E, k).ws_bytes());
 }
 
+size_t mxg_mlp_saved_bytes_cached(int T, int H, int I, int E, int k) {
+  if (!mlp_shape_ok(T, H, I, E, k)) return 0;
+  return static_cast<size_t>(Plan(T, H, I, E, k).saved_cached_bytes);
+}
+
+size_t mxg_mlp_weight_cache_bytes(int H, int I, int E) {
+  if (!mlp_shape_ok(1, H, I, E, 1)) return 0;
+  return static_cast<size_t>(WPlan(H, I, E).bytes);
+}
+
+int mxg_mlp_quantize_weights(const uint16_t* w_gate_up, const uint16_t* w_down, int H, int I, int E, void* cache,
+                             size_t cache_bytes, void* stream) {
+  if (!w_gate_up || !w_down || !cache) return MXG_ERR_ARG;
+  if (H <= 0 || I <= 0 || E <= 0) return MXG_ERR_ARG;
+  if (!mlp_shape_ok(1, H, I, E, 1)) return MXG_ERR_SHAPE;
+  if (!aligned32(w_gate_up) || !aligned32(w_down) || !aligned32(cache)) return MXG_ERR_ALIGN;
+  const WPlan wp(H, I, E);
+  if (cache_bytes < static_cast<size_t>(wp.bytes)) return MXG_ERR_WORKSPACE;
+  return cuda_status(launch_weight_quant(w_gate_up, w_down, H, I, E, at<uint8_t>(cache, wp.wgu),
+                                         at<uint8_t>(cache, wp.swgu), at<uint8_t>(cache, wp.wguT),
+                                         at<uint8_t>(cache, wp.swguT), at<uint8_t>(cache, wp.wd),
+                                         at<uint8_t>(cache, wp.swd), at<uint8_t>(cache, wp.wdT),
+                                         at<uint8_t>(cache, wp.swdT), static_cast<cudaStream_t>(stream)));
+}
+
 const void* mxg_mlp_saved_view(const void* saved, int T, int H, int I, int E, int k, int which) {
   if (!saved || !mlp_shape_ok(T, H, I, E, k)) return nullptr;
   const Plan pl(T, H, I, E, k);
@@ -362,16 +451,19 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   const int T = A->T, H = A->H, I = A->I, E = A->E, k = A->k;
   if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
   if (!mlp_shape_ok(T, H, I, E, k)) return MXG_ERR_SHAPE;
-  if (!A->x || !A->ids || !A->probs || !A->w_gate_up || !A->w_down || !A->y || !A->split_sizes || !A->saved ||
-      !A->workspace || !A->dev_status)
+  const bool cached = A->weight_cache != nullptr;
+  if (!A->x || !A->ids || !A->probs || (!cached && (!A->w_gate_up || !A->w_down)) || !A->y || !A->split_sizes ||
+      !A->saved || !A->workspace || !A->dev_status)
     return MXG_ERR_ARG;
   if (!aligned32(A->x) || !aligned32(A->ids) || !aligned32(A->probs) || !aligned32(A->w_gate_up) ||
       !aligned32(A->w_down) || !aligned32(A->y) || !aligned32(A->split_sizes) || !aligned32(A->saved) ||
-      !aligned32(A->workspace))
+      !aligned32(A->workspace) || !aligned32(A->weight_cache))
     return MXG_ERR_ALIGN;
   const Plan pl(T, H, I, E, k);
-  if (A->saved_bytes < static_cast<uint64_t>(pl.saved_bytes) ||
-      A->workspace_bytes < static_cast<uint64_t>(pl.ws_bytes()))
+  const WPlan wp(H, I, E);
+  if (A->saved_bytes < static_cast<uint64_t>(cached ? pl.saved_cached_bytes : pl.saved_bytes) ||
+      A->workspace_bytes < static_cast<uint64_t>(pl.ws_bytes()) ||
+      (cached && A->weight_cache_bytes < static_cast<uint64_t>(wp.bytes)))
     return MXG_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* sv = A->saved;
@@ -380,6 +472,11 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   int32_t* st = A->dev_status;
   const int32_t* poff = at<int32_t>(sv, pl.poff);
   auto run = [stage](int id) { return stage < 0 || stage == id; };
+  // the forward GEMMs' MXFP8 weights: from the cache, or quantised below into the workspace
+  const uint8_t* wgu = cached ? at<uint8_t>(A->weight_cache, wp.wgu) : at<uint8_t>(ws, pl.wgu);
+  const uint8_t* swgu = cached ? at<uint8_t>(A->weight_cache, wp.swgu) : at<uint8_t>(ws, pl.swgu);
+  const uint8_t* wd = cached ? at<uint8_t>(A->weight_cache, wp.wd) : at<uint8_t>(ws, pl.wd);
+  const uint8_t* swd = cached ? at<uint8_t>(A->weight_cache, wp.swd) : at<uint8_t>(ws, pl.swd);
 
   // F2: permute (histogram -> scan -> stable scatter) into the padded layout
   if (run(MXG_FWD_PERMUTE)) {
@@ -400,44 +497,13 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   MXG_TRY(launch_permute(pp, s));
   }
 
-  // F4: weights, both orientations in one pass (the transposed ones only for backward)
-  if (run(MXG_FWD_QUANT_WEIGHTS)) {
-  QuantParams wq{};
-  wq.x = A->w_gate_up;
-  wq.ld_x = H;
-  wq.x_batch_stride = 2 * pl.I * H;
-  wq.src_div = 1;
-  wq.rows = 2 * I;
-  wq.cols = H;
-  wq.batch = E;
-  wq.q_row = at<uint8_t>(ws, pl.wgu);
-  wq.s_row = at<uint8_t>(ws, pl.swgu);
-  wq.sf_row_rows = pl.E * 2 * I;
-  if (save) {
-    wq.q_col = at<uint8_t>(sv, pl.wguT);
-    wq.s_col = at<uint8_t>(sv, pl.swguT);
-    wq.ld_col = 2 * I;
-    wq.sf_col_rows = pl.E * H;
-  }
-  wq.layout = MXG_LAYOUT_MMA;
-  MXG_TRY(launch_quant(wq, s));
-  QuantParams dq = wq;
-  dq.x = A->w_down;
-  dq.ld_x = I;
-  dq.x_batch_stride = pl.H * I;
-  dq.rows = H;
-  dq.cols = I;
-  dq.q_row = at<uint8_t>(ws, pl.wd);
-  dq.s_row = at<uint8_t>(ws, pl.swd);
-  dq.sf_row_rows = pl.E * H;
-  if (save) {
-    dq.q_col = at<uint8_t>(sv, pl.wdT);
-    dq.s_col = at<uint8_t>(sv, pl.swdT);
-    dq.ld_col = H;
-    dq.sf_col_rows = pl.E * I;
-  }
-  MXG_TRY(launch_quant(dq, s));
-  }
+  // F4: weights, both orientations in one pass (the transposed ones only for
+  // backward); nothing to do with a weight cache
+  if (run(MXG_FWD_QUANT_WEIGHTS) && !cached)
+    MXG_TRY(launch_weight_quant(A->w_gate_up, A->w_down, H, I, E, at<uint8_t>(ws, pl.wgu), at<uint8_t>(ws, pl.swgu),
+                                save ? at<uint8_t>(sv, pl.wguT) : nullptr, at<uint8_t>(sv, pl.swguT),
+                                at<uint8_t>(ws, pl.wd), at<uint8_t>(ws, pl.swd),
+                                save ? at<uint8_t>(sv, pl.wdT) : nullptr, at<uint8_t>(sv, pl.swdT), s));
 
   // F3: gather x into the padded per-expert layout and quantise (row-wise along
   // H for the gate-up GEMM; token-column-wise for the gate-up weight gradient)
@@ -475,8 +541,8 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   g.sa = at<uint8_t>(ws, pl.sxq);
   g.a_rows = pl.Rc;
   g.a_cols = H;
-  g.b = at<uint8_t>(ws, pl.wgu);
-  g.sb = at<uint8_t>(ws, pl.swgu);
+  g.b = wgu;
+  g.sb = swgu;
   g.b_rows = pl.E * 2 * I;
   g.b_cols = H;
   g.poff = poff;
@@ -512,8 +578,8 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   d.sa = at<uint8_t>(ws, pl.shq);
   d.a_rows = pl.Rc;
   d.a_cols = I;
-  d.b = at<uint8_t>(ws, pl.wd);
-  d.sb = at<uint8_t>(ws, pl.swd);
+  d.b = wd;
+  d.sb = swd;
   d.b_rows = pl.E * H;
   d.b_cols = I;
   d.poff = poff;
@@ -547,15 +613,21 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   const int T = A->T, H = A->H, I = A->I, E = A->E, k = A->k;
   if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
   if (!mlp_shape_ok(T, H, I, E, k)) return MXG_ERR_SHAPE;
-  if (!A->dy || !A->saved || !A->dx || !A->dw_gate_up || !A->dw_down || !A->dprobs || !A->workspace ||
-      !A->dev_status)
+  const bool cached = A->weight_cache != nullptr;
+  const bool main_grad = A->main_grad_gate_up != nullptr || A->main_grad_down != nullptr;
+  if (main_grad && (!A->main_grad_gate_up || !A->main_grad_down)) return MXG_ERR_ARG;
+  if (!A->dy || !A->saved || !A->dx || (!main_grad && (!A->dw_gate_up || !A->dw_down)) || !A->dprobs ||
+      !A->workspace || !A->dev_status)
     return MXG_ERR_ARG;
   if (!aligned32(A->dy) || !aligned32(A->saved) || !aligned32(A->dx) || !aligned32(A->dw_gate_up) ||
-      !aligned32(A->dw_down) || !aligned32(A->dprobs) || !aligned32(A->workspace))
+      !aligned32(A->dw_down) || !aligned32(A->dprobs) || !aligned32(A->workspace) || !aligned32(A->weight_cache) ||
+      !aligned32(A->main_grad_gate_up) || !aligned32(A->main_grad_down))
     return MXG_ERR_ALIGN;
   const Plan pl(T, H, I, E, k);
-  if (A->saved_bytes < static_cast<uint64_t>(pl.saved_bytes) ||
-      A->workspace_bytes < static_cast<uint64_t>(pl.ws_bytes()))
+  const WPlan wp(H, I, E);
+  if (A->saved_bytes < static_cast<uint64_t>(cached ? pl.saved_cached_bytes : pl.saved_bytes) ||
+      A->workspace_bytes < static_cast<uint64_t>(pl.ws_bytes()) ||
+      (cached && A->weight_cache_bytes < static_cast<uint64_t>(wp.bytes)))
     return MXG_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const void* sv = A->saved;
@@ -563,6 +635,12 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   int32_t* st = A->dev_status;
   const int32_t* poff = at<int32_t>(sv, pl.poff);
   auto run = [stage](int id) { return stage < 0 || stage == id; };
+  // the dgrad GEMMs' MXFP8 weights (MX along the contraction of the backward)
+  const void* wsrc = cached ? A->weight_cache : sv;
+  const uint8_t* wguT = at<uint8_t>(wsrc, cached ? wp.wguT : pl.wguT);
+  const uint8_t* swguT = at<uint8_t>(wsrc, cached ? wp.swguT : pl.swguT);
+  const uint8_t* wdT = at<uint8_t>(wsrc, cached ? wp.wdT : pl.wdT);
+  const uint8_t* swdT = at<uint8_t>(wsrc, cached ? wp.swdT : pl.swdT);
 
   // B1: gather dy and quantise (row-wise along H for dgrad, token-column-wise for wgrad)
   if (run(MXG_BWD_QUANT_DY)) {
@@ -595,8 +673,8 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   g.sa = at<uint8_t>(ws, pl.sdyq);
   g.a_rows = pl.Rc;
   g.a_cols = H;
-  g.b = at<uint8_t>(sv, pl.wdT);
-  g.sb = at<uint8_t>(sv, pl.swdT);
+  g.b = wdT;
+  g.sb = swdT;
   g.b_rows = pl.E * I;
   g.b_cols = H;
   g.poff = poff;
@@ -623,10 +701,10 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   MXG_TRY(launch_gemm(g, s));
   }
 
-  // B3: dW_down[e] = dYc^T Hc over the tokens of e
+  // B3: dW_down[e] = dYc^T Hc over the tokens of e (or added into main_grad_down)
   if (run(MXG_BWD_WGRAD_DOWN)) {
   GemmArgs w{};
-  w.epi = EPI_BF16;
+  w.epi = main_grad ? EPI_ACC_F32 : EPI_BF16;
   w.kgroup = true;
   w.pair = kUsePairTiles && H % 256 == 0 && I % 256 == 0;   // 256 x 256 output tiles
   w.a = at<uint8_t>(ws, pl.dyc);
@@ -642,6 +720,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   w.M = H;
   w.N = I;
   w.d = A->dw_down;
+  w.dacc = A->main_grad_down;
   w.ldd = I;
   w.status = st;
   w.tiles_upper = w.pair ? pl.E * (H / 256) * (I / 256) : pl.E * (H / 128) * (I / gemm_pick_bn(EPI_BF16, I));
@@ -657,8 +736,8 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   x.sa = at<uint8_t>(ws, pl.sdguq);
   x.a_rows = pl.Rc;
   x.a_cols = 2 * I;
-  x.b = at<uint8_t>(sv, pl.wguT);
-  x.sb = at<uint8_t>(sv, pl.swguT);
+  x.b = wguT;
+  x.sb = swguT;
   x.b_rows = pl.E * H;
   x.b_cols = 2 * I;
   x.poff = poff;
@@ -674,10 +753,10 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   MXG_TRY(launch_gemm(x, s));
   }
 
-  // B5: dW_gate_up[e] = dGUc^T Xc over the tokens of e
+  // B5: dW_gate_up[e] = dGUc^T Xc over the tokens of e (or added into main_grad_gate_up)
   if (run(MXG_BWD_WGRAD_GATE_UP)) {
   GemmArgs v{};
-  v.epi = EPI_BF16;
+  v.epi = main_grad ? EPI_ACC_F32 : EPI_BF16;
   v.kgroup = true;
   v.pair = kUsePairTiles && H % 256 == 0;   // 2I is a multiple of 256
   v.a = at<uint8_t>(ws, pl.dguc);
@@ -693,6 +772,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   v.M = 2 * I;
   v.N = H;
   v.d = A->dw_gate_up;
+  v.dacc = A->main_grad_gate_up;
   v.ldd = H;
   v.status = st;
   v.tiles_upper = v.pair ? pl.E * (2 * I / 256) * (H / 256) : pl.E * (2 * I / 128) * (H / gemm_pick_bn(EPI_BF16, H));

@@ -126,6 +126,7 @@ int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   const int T = A->T, H = A->H, I = A->I, E = A->E, k = A->k;
   if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
   if (!shape_ok(T, H, I, E, k)) return MXG_ERR_SHAPE;
+  if (A->weight_cache) return MXG_ERR_ARG;   // the weight cache holds MXFP8 weights
   if (!A->x || !A->ids || !A->probs || !A->w_gate_up || !A->w_down || !A->y || !A->split_sizes || !A->saved ||
       !A->workspace || !A->dev_status)
     return MXG_ERR_ARG;
@@ -254,6 +255,7 @@ int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   const int T = A->T, H = A->H, I = A->I, E = A->E, k = A->k;
   if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
   if (!shape_ok(T, H, I, E, k)) return MXG_ERR_SHAPE;
+  if (A->weight_cache || A->main_grad_gate_up || A->main_grad_down) return MXG_ERR_ARG;
   if (!A->dy || !A->saved || !A->dx || !A->dw_gate_up || !A->dw_down || !A->dprobs || !A->workspace ||
       !A->dev_status)
     return MXG_ERR_ARG;

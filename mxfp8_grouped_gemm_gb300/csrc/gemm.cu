@@ -14,6 +14,8 @@
 //
 // Epilogues (TMEM -> registers, one thread per output row):
 //   EPI_BF16    : store fp32 accumulators as bf16.
+//   EPI_ACC_F32 : (weight gradients) add the fp32 accumulators into an fp32
+//                 gradient buffer (main_grad accumulation across micro-batches).
 //   EPI_SWIGLU  : gate-up tile = 128 gate + 128 up columns; h = p*SiLU(g)*u
 //                 (ScaledSwiGLU, "Fusing precision conversion and expert
 //                 computation"), re-quantised to MXFP8 row-wise (the down
@@ -254,6 +256,32 @@ __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc,
                       : P.d + static_cast<int64_t>(tc.m0 + row) * P.ldd + tc.nt * BN + hf * COLS;
 #pragma unroll
   for (int j = 0; j < COLS / 16; ++j) st_global_v8(drow + 16 * j, packed + 8 * j);
+}
+
+// Weight-gradient tile added into an fp32 gradient buffer (main_grad): the
+// thread drains its half row of fp32 accumulators, releases the accumulator,
+// then reads, adds and writes back 32 bytes at a time.  Each element of the
+// buffer belongs to exactly one tile, so the update is a plain
+// read-modify-write.
+template <int BN>
+__device__ __forceinline__ void epi_acc_f32(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int row, int hf,
+                                            const AccRelease& tempty, int lane) {
+  constexpr int COLS = BN / 2;
+  uint32_t v[COLS / 32][32];
+#pragma unroll
+  for (int c = 0; c < COLS / 32; ++c) tmem_ld_32x32b_x32(tb + hf * COLS + c * 32, v[c]);
+  tmem_ld_wait();
+  release_acc(tempty, lane);
+  float* drow = P.dacc + static_cast<int64_t>(tc.e) * P.M * P.N + static_cast<int64_t>(tc.m0 + row) * P.N +
+                tc.nt * BN + hf * COLS;
+#pragma unroll
+  for (int j = 0; j < COLS / 8; ++j) {
+    uint32_t w[8];
+    ld_global_v8(drow + 8 * j, w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = f2u(u2f(w[i]) + u2f(v[j / 4][8 * (j % 4) + i]));
+    st_global_v8(drow + 8 * j, w);
+  }
 }
 
 // Gate-up tile: accumulator columns [0, BN/2) = gate j0.., [BN/2, BN) = up j0..
@@ -757,7 +785,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t t = tile0; t < total; t += tstep) {
       const TileCoord tc = decode(t);
       if (tc.num_k == 0) {
-        // token-grouped tile of an expert without tokens: exact zeros
+        // token-grouped tile of an expert without tokens: exact zeros (an fp32
+        // gradient buffer being accumulated into stays as it is)
+        if constexpr (EPI == EPI_ACC_F32) continue;
         uint16_t* drow = P.d + static_cast<int64_t>(tc.e) * P.M * P.N + static_cast<int64_t>(tc.m0 + row) * P.N +
                          tc.nt * BN + hf * (BN / 2);
 #pragma unroll 4
@@ -781,6 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if constexpr (EPI == EPI_DSWIGLU) {
         if constexpr (BN == 256) epi_dswiglu_staged<BF>(P, tc, tb, q, lane, hf, rel, reinterpret_cast<uint16_t*>(xpose));
         else epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
+      } else if constexpr (EPI == EPI_ACC_F32) {
+        epi_acc_f32<BN>(P, tc, tb, row, hf, rel, lane);
       } else {
         epi_bf16<BN, KG>(P, tc, tb, row, hf, rel, lane);
       }
@@ -929,6 +961,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
   if (g.pair) {  // CTA-pair tiles, 256 x 256
     if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, true>(g, s);
     if (g.epi == EPI_DSWIGLU) return launch_impl<256, EPI_DSWIGLU, false, true>(g, s);
+    if (g.kgroup && g.epi == EPI_ACC_F32) return launch_impl<256, EPI_ACC_F32, true, true>(g, s);
     if (g.kgroup) return launch_impl<256, EPI_BF16, true, true>(g, s);
     return launch_impl<256, EPI_BF16, false, true>(g, s);
   }
@@ -936,6 +969,8 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
   if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, false>(g, s);
   if (g.epi == EPI_DSWIGLU)
     return bn == 256 ? launch_impl<256, EPI_DSWIGLU, false, false>(g, s) : launch_impl<128, EPI_DSWIGLU, false, false>(g, s);
+  if (g.kgroup && g.epi == EPI_ACC_F32)
+    return bn == 256 ? launch_impl<256, EPI_ACC_F32, true, false>(g, s) : launch_impl<128, EPI_ACC_F32, true, false>(g, s);
   if (g.kgroup)
     return bn == 256 ? launch_impl<256, EPI_BF16, true, false>(g, s) : launch_impl<128, EPI_BF16, true, false>(g, s);
   return bn == 256 ? launch_impl<256, EPI_BF16, false, false>(g, s) : launch_impl<128, EPI_BF16, false, false>(g, s);

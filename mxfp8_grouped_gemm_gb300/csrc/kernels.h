@@ -63,7 +63,7 @@ cudaError_t launch_dprob(const float* part, int ld, const int32_t* prow_of_src, 
                          cudaStream_t s);
 
 // --------------------------------------------------------------------- GEMM
-enum Epi { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
+enum Epi { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_ACC_F32 = 3 };
 
 struct GemmArgs {
   int epi;
@@ -106,6 +106,7 @@ struct GemmArgs {
   int64_t y_row_ld;
   uint16_t* y_col;            // [cols][..] bf16 transposed output (h^T, or dGU^T)
   int64_t y_col_ld;
+  float* dacc;                // EPI_ACC_F32 (token-grouped): fp32 [E][M][N] that the tile is added into
   int64_t tiles_upper;        // host bound on the number of tiles (grid sizing)
   uint64_t wait_limit_ns;     // bound on every wait inside the kernel (0: default)
   int32_t debug_stall;        // test hook: the producer issues no copies

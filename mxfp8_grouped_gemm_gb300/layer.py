@@ -38,22 +38,45 @@ class GroupedMLP:
         self.dw_gate_up = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=self.device)
         self.dw_down = torch.empty((E, H, I), dtype=torch.bfloat16, device=self.device)
         self.dprobs = torch.empty((T, k), dtype=torch.float32, device=self.device)
+        self.weight_cache = None          # MXFP8 weights kept across micro-batches (quantize_weights)
+        self._fwd_cached = False
 
     def route(self, logits, stream=None):
         """Top-k routing into this object's ids/probs buffers."""
         return _lib.mxg_route_topk(logits, self.k, self.ids, self.probs, stream=stream)
 
-    def forward(self, x, ids, probs, w_gate_up, w_down, save_for_backward=True, stream=None, stage=None, y=None):
+    def quantize_weights(self, w_gate_up, w_down, stream=None):
+        """Quantise the weights once into this layer's weight cache (MXFP8 path):
+        forward calls given no weights then read it, e.g. for every micro-batch
+        of one optimizer step."""
+        if self.bf16:
+            raise NotImplementedError("the weight cache holds MXFP8 weights")
+        self.weight_cache = _lib.mxg_mlp_quantize_weights(w_gate_up, w_down, self.weight_cache, stream=stream)
+        return self.weight_cache
+
+    def forward(self, x, ids, probs, w_gate_up=None, w_down=None, save_for_backward=True, stream=None, stage=None,
+                y=None):
+        """w_gate_up / w_down None: use the weight cache (quantize_weights)."""
+        cached = w_gate_up is None and w_down is None
+        if cached and self.weight_cache is None:
+            raise ValueError("no weights given and no weight cache: call quantize_weights first")
+        self._fwd_cached = cached
         return _lib.mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, self.saved, self.workspace,
                                         self.dev_status, y=self.y if y is None else y,
                                         split_sizes=self.split_sizes, save_for_backward=save_for_backward,
-                                        stream=stream, stage=stage, bf16=self.bf16)
+                                        stream=stream, stage=stage, bf16=self.bf16,
+                                        weight_cache=self.weight_cache if cached else None)
 
-    def backward(self, dy, stream=None, stage=None, dx=None):
+    def backward(self, dy, stream=None, stage=None, dx=None, main_grad=None):
+        """main_grad = (fp32 [E, 2I, H], fp32 [E, H, I]): add the weight gradients
+        into these (returned in place of dW_gate_up, dW_down)."""
         return _lib.mxg_grouped_mlp_bwd(dy, self.saved, self.workspace, self.dev_status, self.E, self.I, self.k,
-                                        dx=self.dx if dx is None else dx, dw_gate_up=self.dw_gate_up,
-                                        dw_down=self.dw_down, dprobs=self.dprobs, stream=stream, stage=stage,
-                                        bf16=self.bf16)
+                                        dx=self.dx if dx is None else dx,
+                                        dw_gate_up=None if main_grad is not None else self.dw_gate_up,
+                                        dw_down=None if main_grad is not None else self.dw_down,
+                                        dprobs=self.dprobs, stream=stream, stage=stage, bf16=self.bf16,
+                                        weight_cache=self.weight_cache if self._fwd_cached else None,
+                                        main_grad=main_grad)
 
     def step(self, logits, x, w_gate_up, w_down, dy, stream=None):
         """One pass of the whole path: route, forward (saving for backward), backward."""

@@ -201,3 +201,58 @@ def test_struct_layout_matches_header(tmp_path):
         assert table[(cname, "size")] == ctypes.sizeof(cls)
         for f, _ in cls._fields_:
             assert table[(cname, f)] == getattr(cls, f).offset, (cname, f)
+
+
+def test_weight_cache_and_main_grad_validation(L):
+    import mxfp8_grouped_gemm_gb300 as m
+    H, I, E = 128, 256, 4
+
+    def carve(*sizes):
+        off = 0
+        for n in sizes:
+            off = (off + n + 255) // 256 * 256
+        return off
+    gu, d = E * 2 * I * H, E * H * I
+    assert L.mxg_mlp_weight_cache_bytes(H, I, E) == carve(gu, gu // 32, d, d // 32, gu, gu // 32, d, d // 32)
+    assert L.mxg_mlp_weight_cache_bytes(100, I, E) == 0
+    full, cached = L.mxg_mlp_saved_bytes(256, H, I, E, 2), L.mxg_mlp_saved_bytes_cached(256, H, I, E, 2)
+    assert 0 < cached < full
+    assert full - cached == carve(gu, gu // 32, d, d // 32)          # the transposed weights move to the cache
+    cb = L.mxg_mlp_weight_cache_bytes(H, I, E)
+    q = [FAKE, FAKE, H, I, E, FAKE, cb, None]
+    a = list(q); a[0] = None
+    assert L.mxg_mlp_quantize_weights(*a) == 1
+    a = list(q); a[2] = 96
+    assert L.mxg_mlp_quantize_weights(*a) == 2
+    a = list(q); a[5] = MISALIGNED
+    assert L.mxg_mlp_quantize_weights(*a) == 3
+    a = list(q); a[6] = cb - 1
+    assert L.mxg_mlp_quantize_weights(*a) == 5
+    # forward with a cache: weights may be NULL; the cached saved size suffices, a short cache does not
+    f = m.MlpFwdArgs(256, H, I, E, 2, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, cached, FAKE, 1 << 40, 1,
+                     FAKE, FAKE, cb)
+    bad = m.MlpFwdArgs.from_buffer_copy(f); bad.saved_bytes = cached - 1
+    assert L.mxg_grouped_mlp_fwd(ctypes.byref(bad), None) == 5
+    bad = m.MlpFwdArgs.from_buffer_copy(f); bad.weight_cache_bytes = cb - 1
+    assert L.mxg_grouped_mlp_fwd(ctypes.byref(bad), None) == 5
+    bad = m.MlpFwdArgs.from_buffer_copy(f); bad.weight_cache = None          # no weights at all
+    assert L.mxg_grouped_mlp_fwd(ctypes.byref(bad), None) == 1
+    bad = m.MlpFwdArgs.from_buffer_copy(f); bad.weight_cache = MISALIGNED
+    assert L.mxg_grouped_mlp_fwd(ctypes.byref(bad), None) == 3
+    # backward: main_grad both or neither; with it dW may be NULL
+    b = m.MlpBwdArgs(256, H, I, E, 2, FAKE, FAKE, 1 << 40, FAKE, None, None, FAKE, FAKE, 1 << 40, FAKE, None, 0,
+                     FAKE, None)
+    assert L.mxg_grouped_mlp_bwd(ctypes.byref(b), None) == 1
+    bad = m.MlpBwdArgs.from_buffer_copy(b); bad.main_grad_down = MISALIGNED
+    assert L.mxg_grouped_mlp_bwd(ctypes.byref(bad), None) == 3
+    bad = m.MlpBwdArgs.from_buffer_copy(b); bad.main_grad_down = FAKE; bad.weight_cache = FAKE
+    bad.weight_cache_bytes = cb - 1; bad.saved_bytes = cached
+    assert L.mxg_grouped_mlp_bwd(ctypes.byref(bad), None) == 5
+    # the BF16 path takes neither
+    H2, I2 = 256, 512
+    f2 = m.MlpFwdArgs(256, H2, I2, E, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, FAKE, 1 << 40, 1,
+                      FAKE, FAKE, 1 << 40)
+    assert L.mxg_grouped_mlp_bf16_fwd(ctypes.byref(f2), None) == 1
+    b2 = m.MlpBwdArgs(256, H2, I2, E, 2, FAKE, FAKE, 1 << 40, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, FAKE, None, 0,
+                      FAKE, FAKE)
+    assert L.mxg_grouped_mlp_bf16_bwd(ctypes.byref(b2), None) == 1
