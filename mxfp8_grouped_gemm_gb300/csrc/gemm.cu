@@ -794,6 +794,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN / 16; ++c) reinterpret_cast<uint4*>(drow)[c] = make_uint4(0u, 0u, 0u, 0u);
         continue;
       }
+      if constexpr (EPI == EPI_ACC_F32) {
+        // the gradient rows this thread will read-modify-write come into L2
+        // while the tile's MMAs run, so the epilogue's loads hit L2 instead of
+        // waiting on HBM
+        const float* pr = P.dacc + static_cast<int64_t>(tc.e) * P.M * P.N +
+                          static_cast<int64_t>(tc.m0 + row) * P.N + tc.nt * BN + hf * (BN / 2);
+#pragma unroll
+        for (int j = 0; j < BN / 2 / 32; ++j) prefetch_l2(pr + 32 * j);
+      }
       bool got = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, limit_ns);
       got = __all_sync(0xffffffffu, got);
       if (!got) {

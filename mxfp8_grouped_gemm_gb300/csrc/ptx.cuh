@@ -149,6 +149,11 @@ __device__ __forceinline__ void ld_global_v8(const void* src, uint32_t* w) {
                : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
                : "l"(src));
 }
+// Bring the 128-byte line holding `p` into L2 (no register result, no fault
+// semantics beyond a normal load of a valid address).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 // Plain arrive on this CTA's mbarrier, given as a shared-window address.
 __device__ __forceinline__ void mbar_arrive_u32(uint32_t saddr) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr) : "memory");
