@@ -36,22 +36,42 @@ biological AI training" (roboticlifestyle.com)):
 
 ``quant=False`` replaces every quantiser with the identity; the backward is then
 the exact gradient of the forward (used by the finite-difference pin).
+``quant="fp8"`` replaces every MX quantiser with per-tensor FP8 (oracle/fp8.py):
+one scale per expert operand — the expert's weight matrix, and the expert's
+rows of x, h, dy and dGU — the same scale in either orientation.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import mx
+from . import fp8, mx
 
 PAD = 128   # expert groups start on a multiple of 128 rows in the padded layout
 
 
 def _fq(v, quant):
+    if quant == "fp8":
+        return fp8.fake_quant(v)
     return mx.fake_quant(v) if quant else np.asarray(v, dtype=np.float64)
 
 
 def _fqc(a, quant):
+    if quant == "fp8":                  # per-tensor: orientation does not matter
+        return fp8.fake_quant(a)
     return mx.fake_quant_group_columns(a) if quant else np.asarray(a, dtype=np.float64)
+
+
+def _fq_groups(v, off, quant):
+    """Row-wise quantisation of the permuted activations: MX blocks lie inside a
+    row, so the whole matrix is quantised at once; per-tensor FP8 takes one
+    tensor per expert group of rows."""
+    if quant != "fp8":
+        return _fq(v, quant)
+    out = np.zeros(v.shape, dtype=np.float64)
+    for e in range(len(off) - 1):
+        if off[e + 1] > off[e]:
+            out[off[e]:off[e + 1]] = fp8.fake_quant(v[off[e]:off[e + 1]])
+    return out
 
 
 def silu(g):
@@ -173,7 +193,7 @@ def expert_weight_grads(dy_perm_e, h_e, dgu_e, x_perm_e, quant: bool = True):
 
 # ---------------------------------------------------------------- forward ----
 
-def mlp_fwd(x, ids, probs, w_gate_up, w_down, quant: bool = True) -> dict:
+def mlp_fwd(x, ids, probs, w_gate_up, w_down, quant: bool | str = True) -> dict:
     """Forward of the grouped expert MLP.  Shapes: x [T,H], ids/probs [T,k],
     w_gate_up [E,2I,H], w_down [E,H,I] (any float dtype; computed in fp64).
     Returns y [T,H] and the intermediates the backward and the tests need."""
@@ -188,12 +208,12 @@ def mlp_fwd(x, ids, probs, w_gate_up, w_down, quant: bool = True) -> dict:
     tok = src // k
     x_perm = x[tok]
     p_perm = np.asarray(probs, dtype=np.float64).reshape(-1)[src]
-    xq = _fq(x_perm, quant)                          # row-wise along H
+    off = perm["offsets"]
+    xq = _fq_groups(x_perm, off, quant)              # row-wise along H
     R = src.size
     gu = np.empty((R, 2 * I))
     h = np.empty((R, I))
     y_perm = np.empty((R, H))
-    off = perm["offsets"]
     for e in range(E):
         a, b = off[e], off[e + 1]
         if b == a:
@@ -222,7 +242,7 @@ def mlp_bwd(ctx: dict, dy) -> dict:
     src = perm["src_of_row"]
     tok = src // k
     dy_perm = dy[tok]
-    dyq = _fq(dy_perm, quant)                        # row-wise along H
+    dyq = _fq_groups(dy_perm, perm["offsets"], quant)   # row-wise along H
     gu, h, x_perm, p_perm = ctx["gu"], ctx["h"], ctx["x_perm"], ctx["p_perm"]
     R = src.size
     dgu = np.empty((R, 2 * I))
