@@ -38,7 +38,11 @@ biological AI training" (roboticlifestyle.com)):
 the exact gradient of the forward (used by the finite-difference pin).
 ``quant="fp8"`` replaces every MX quantiser with per-tensor FP8 (oracle/fp8.py):
 one scale per expert operand — the expert's weight matrix, and the expert's
-rows of x, h, dy and dGU — the same scale in either orientation.
+rows of x, h, dy and dGU — the same scale in either orientation.  Reading for
+that mode: a per-tensor scale needs the whole tensor before any element is
+quantised, so h and dGU exist as bf16 tensors between the GEMM that produces
+them and their quantisation (as in an unfused FP8 MLP, whose GEMM and
+activation outputs are bf16); the oracle rounds them to bf16 there.
 """
 from __future__ import annotations
 
@@ -59,6 +63,12 @@ def _fqc(a, quant):
     if quant == "fp8":                  # per-tensor: orientation does not matter
         return fp8.fake_quant(a)
     return mx.fake_quant_group_columns(a) if quant else np.asarray(a, dtype=np.float64)
+
+
+def _materialised(v, quant):
+    """An activation or activation gradient as it is stored before a per-tensor
+    FP8 quantisation (bf16); unchanged otherwise."""
+    return bf16_round(v) if quant == "fp8" else v
 
 
 def _fq_groups(v, off, quant):
@@ -168,7 +178,7 @@ def expert_forward_rows(xq_rows, p_rows, w: dict, quant: bool = True):
     gu = xq_rows @ w["wg"].T
     I = gu.shape[1] // 2
     h = scaled_swiglu(gu[:, :I], gu[:, I:], p_rows[:, None])
-    y = _fq(h, quant) @ w["wd"].T
+    y = _fq(_materialised(h, quant), quant) @ w["wd"].T
     return gu, h, y
 
 
@@ -179,15 +189,15 @@ def expert_backward_rows(dyq_rows, gu, p_rows, w: dict, quant: bool = True):
     dh = dyq_rows @ w["wdT"].T
     dg, du, dpt = dscaled_swiglu(dh, gu[:, :I], gu[:, I:], p_rows[:, None])
     dgu = np.concatenate([dg, du], axis=1)
-    dx = _fq(dgu, quant) @ w["wguT"].T
+    dx = _fq(_materialised(dgu, quant), quant) @ w["wguT"].T
     return dh, dgu, dpt.sum(axis=1), dx
 
 
 def expert_weight_grads(dy_perm_e, h_e, dgu_e, x_perm_e, quant: bool = True):
     """dW_down = colMX(dY)^T colMX(h) and dW_gate_up = colMX(dGU)^T colMX(X) over
     the expert's tokens (column-wise blocks of 32 tokens from its first row)."""
-    dw_d = _fqc(dy_perm_e, quant).T @ _fqc(h_e, quant)
-    dw_gu = _fqc(dgu_e, quant).T @ _fqc(x_perm_e, quant)
+    dw_d = _fqc(dy_perm_e, quant).T @ _fqc(_materialised(h_e, quant), quant)
+    dw_gu = _fqc(_materialised(dgu_e, quant), quant).T @ _fqc(x_perm_e, quant)
     return dw_d, dw_gu
 
 
