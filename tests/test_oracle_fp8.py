@@ -36,32 +36,32 @@ def _brute(p: float) -> int:
     return cands[0][0]
 
 
-def test_codes_are_nearest_e4m3_of_fp32_product():
+def test_codes_are_nearest_e4m3_of_scaled_values():
     rng = np.random.default_rng(3)
     bits = rng.integers(0, 1 << 16, 4000, dtype=np.uint32) << 16
-    v = bits.view(np.float32)
-    v = v[np.isfinite(v)]
-    v = v[np.abs(v) < 1e30]
-    amax = np.float32(np.max(np.abs(v)))
-    codes, s = fp8.quantize(v)
-    assert s == np.float32(448.0) / amax
-    p = (v * s).astype(np.float32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    v = f[np.abs(f) < 1e30].astype(np.float64)
+    amax = np.max(np.abs(v))
+    codes, e = fp8.quantize(v)
+    assert e == int(np.floor(np.log2(amax))) - 8
+    p = v * 2.0 ** -e
     for i in range(0, v.size, 7):
         assert codes[i] == _brute(float(p[i])), (v[i], p[i], codes[i])
 
 
-def test_tensor_max_maps_to_448_and_scale_rule():
-    v = np.array([0.5, -3.0, 1.25, 2.0], dtype=np.float32)
-    codes, s = fp8.quantize(v)
-    assert s == np.float32(448.0) / np.float32(3.0)
-    assert codes[1] == 0xFE                                  # -448
-    assert fp8.tensor_scale(0.0) == np.float32(1.0)
-    assert fp8.tensor_scale(np.float32(1e-40)) == np.finfo(np.float32).max
+def test_tensor_scale_rule_and_saturation():
+    codes, e = fp8.quantize(np.array([0.5, -3.0, 1.25, 2.0]))
+    assert e == -7 and codes[1] == 0xFC                      # -3 * 2^7 = -384
+    codes, e = fp8.quantize(np.array([1.9 * 2.0 ** 5, 1.0]))
+    assert e == -3 and codes[0] == 0x7E                      # 486.4 saturates to 448
+    assert fp8.tensor_exponent(0.0) == -127
+    assert fp8.tensor_exponent(1e-45) == -127                # clamped
 
 
 def test_zero_tensor():
-    codes, s = fp8.quantize(np.zeros(64, dtype=np.float32))
-    assert s == 1.0 and not codes.any()
+    codes, e = fp8.quantize(np.zeros(64))
+    assert e == -127 and not codes.any()
 
 
 def test_grid_values_round_trip_exactly():
@@ -69,19 +69,22 @@ def test_grid_values_round_trip_exactly():
     grid = np.array([v for _, v in CODES if v >= 0])
     for j in (-6, 0, 5):
         vals = np.concatenate([[448.0], rng.choice(grid, 500)]) * 2.0 ** j * rng.choice([-1, 1], 501)
-        codes, s = fp8.quantize(vals)
-        assert s == np.float32(2.0 ** -j)
-        assert np.array_equal(fp8.dequantize(codes, s), vals)
+        codes, e = fp8.quantize(vals)
+        assert e == j
+        assert np.array_equal(fp8.dequantize(codes, e), vals)
 
 
 def test_round_to_nearest_error_bound():
     rng = np.random.default_rng(7)
-    v = rng.standard_normal(20000).astype(np.float32) * 3
-    codes, s = fp8.quantize(v)
-    d = fp8.dequantize(codes, s)
-    # half an E4M3 quantum: 2^-4 relative for normals, 2^-10 / s absolute for subnormals
-    bound = np.maximum(2.0 ** -4 * np.abs(v), 2.0 ** -10 / float(s)) * (1 + 1e-6)
-    assert np.all(np.abs(d - v) <= bound)
+    v = rng.standard_normal(20000) * 3
+    codes, e = fp8.quantize(v)
+    d = fp8.dequantize(codes, e)
+    # half an E4M3 quantum: 2^-4 relative for normals, 2^(e-10) absolute for subnormals;
+    # the tensor maximum is at most 2^(e+9), so no value saturates by more than its rounding
+    bound = np.maximum(2.0 ** -4 * np.abs(v), 2.0 ** (e - 10)) * (1 + 1e-12)
+    sat = np.abs(v) * 2.0 ** -e > 448
+    assert np.all((np.abs(d - v) <= bound) | sat)
+    assert np.all(np.abs(d[sat]) == 448 * 2.0 ** e)
 
 
 def test_moe_fp8_mode_exact_on_grid_inputs():
