@@ -367,6 +367,35 @@ int mxg_grouped_mlp_bf16_bwd(const mxg_mlp_bwd_args* args, void* stream);
 int mxg_grouped_mlp_bf16_fwd_stage(const mxg_mlp_fwd_args* args, int stage, void* stream);
 int mxg_grouped_mlp_bf16_bwd_stage(const mxg_mlp_bwd_args* args, int stage, void* stream);
 
+/* ----------------------------------------------------------------------------
+ * The same grouped expert MLP in per-tensor FP8: E4M3 operands with one
+ * power-of-two scale per expert tensor (the MX rule with the whole tensor as
+ * its block, "current scaling": e = floor(log2 amax) - 8 of the tensor, a
+ * tensor being an expert's weight matrix or its rows of x, h, dy or dGU;
+ * codes E4M3(v * 2^-e), round to nearest even, saturating) on the tensor
+ * cores (kind::f8f6f4, fp32 accumulation scaled by both tensors' 2^e).  The FP8
+ * variant of the recipe ([Grouped] "Reducing memory pressure with MXFP8": FP8
+ * and MXFP8 differ in scaling granularity).  h and dGU are written in bf16 by
+ * the GEMM epilogues, which also take their per-expert amax, and quantised by
+ * a following pass (the gate-up and dgrad-down stages are two launches plus a
+ * memset; the quantise stages are a memset, an amax pass and the quantiser).
+ * Arguments, outputs, ownership and errors as mxg_grouped_mlp_fwd / _bwd with
+ * `saved` / `workspace` sized by the _fp8_ queries; weight_cache and the
+ * main_grad pointers must be NULL (MXG_ERR_ARG).  Requires H % 256 == 0 and
+ * I % 256 == 0.
+ */
+size_t mxg_mlp_fp8_saved_bytes(int T, int H, int I, int E, int k);
+size_t mxg_mlp_fp8_workspace_bytes(int T, int H, int I, int E, int k);
+int mxg_grouped_mlp_fp8_fwd(const mxg_mlp_fwd_args* args, void* stream);
+int mxg_grouped_mlp_fp8_bwd(const mxg_mlp_bwd_args* args, void* stream);
+int mxg_grouped_mlp_fp8_fwd_stage(const mxg_mlp_fwd_args* args, int stage, void* stream);
+int mxg_grouped_mlp_fp8_bwd_stage(const mxg_mlp_bwd_args* args, int stage, void* stream);
+/* Debug views into an FP8 `saved` buffer (device pointers; NULL on bad
+ * arguments) for the tests: 0 = x's codes transposed (uint8 [H][m_cap], the
+ * padded row layout of mxg_mlp_row_capacity), 1..4 = amax of x, W_gate_up,
+ * W_down, h per expert (fp32 [E]), 5 = padded_offsets (int32 [E+1]). */
+const void* mxg_mlp_fp8_saved_view(const void* saved, int T, int H, int I, int E, int k, int which);
+
 /* Debug views into `saved` (device pointers; NULL on bad arguments) used by the
  * tests to compare intermediates: 0 = GU (bf16 [m_cap][2I], the gate-up GEMM
  * output before the activation; m_cap = mxg_mlp_row_capacity), 1 =

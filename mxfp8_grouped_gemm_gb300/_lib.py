@@ -33,6 +33,8 @@ EXPORTS = [
     "mxg_router_bwd", "mxg_mlp_bf16_saved_bytes", "mxg_mlp_bf16_workspace_bytes", "mxg_grouped_mlp_bf16_fwd",
     "mxg_grouped_mlp_bf16_bwd", "mxg_grouped_mlp_bf16_fwd_stage", "mxg_grouped_mlp_bf16_bwd_stage",
     "mxg_mlp_weight_cache_bytes", "mxg_mlp_quantize_weights", "mxg_mlp_saved_bytes_cached",
+    "mxg_mlp_fp8_saved_bytes", "mxg_mlp_fp8_workspace_bytes", "mxg_grouped_mlp_fp8_fwd", "mxg_grouped_mlp_fp8_bwd",
+    "mxg_grouped_mlp_fp8_fwd_stage", "mxg_grouped_mlp_fp8_bwd_stage", "mxg_mlp_fp8_saved_view",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -112,6 +114,13 @@ def lib() -> ctypes.CDLL:
         "mxg_mlp_weight_cache_bytes": (SZ, [I32, I32, I32]),
         "mxg_mlp_quantize_weights": (I32, [P, P, I32, I32, I32, P, SZ, P]),
         "mxg_mlp_saved_bytes_cached": (SZ, [I32, I32, I32, I32, I32]),
+        "mxg_mlp_fp8_saved_bytes": (SZ, [I32, I32, I32, I32, I32]),
+        "mxg_mlp_fp8_workspace_bytes": (SZ, [I32, I32, I32, I32, I32]),
+        "mxg_grouped_mlp_fp8_fwd": (I32, [ctypes.POINTER(MlpFwdArgs), P]),
+        "mxg_grouped_mlp_fp8_bwd": (I32, [ctypes.POINTER(MlpBwdArgs), P]),
+        "mxg_grouped_mlp_fp8_fwd_stage": (I32, [ctypes.POINTER(MlpFwdArgs), I32, P]),
+        "mxg_grouped_mlp_fp8_bwd_stage": (I32, [ctypes.POINTER(MlpBwdArgs), I32, P]),
+        "mxg_mlp_fp8_saved_view": (P, [P, I32, I32, I32, I32, I32, I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -293,6 +302,14 @@ def mxg_mlp_bf16_workspace_bytes(T, H, I, E, k) -> int:
     return int(lib().mxg_mlp_bf16_workspace_bytes(T, H, I, E, k))
 
 
+def mxg_mlp_fp8_saved_bytes(T, H, I, E, k) -> int:
+    return int(lib().mxg_mlp_fp8_saved_bytes(T, H, I, E, k))
+
+
+def mxg_mlp_fp8_workspace_bytes(T, H, I, E, k) -> int:
+    return int(lib().mxg_mlp_fp8_workspace_bytes(T, H, I, E, k))
+
+
 def mxg_mlp_saved_view(saved: torch.Tensor, T, H, I, E, k, which: int) -> int:
     return int(lib().mxg_mlp_saved_view(_ptr(saved), T, H, I, E, k, which) or 0)
 
@@ -333,7 +350,7 @@ def mxg_mlp_quantize_weights(w_gate_up, w_down, cache: WeightCache | None = None
 
 def mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, saved, workspace, dev_status, y=None, split_sizes=None,
                         save_for_backward: bool = True, stream=None, stage: int | None = None, bf16: bool = False,
-                        weight_cache: WeightCache | None = None):
+                        weight_cache: WeightCache | None = None, fp8: bool = False):
     """Full forward, or one stage of it (FWD_STAGES index) when ``stage`` is given
     (``bf16``: the BF16 path, mxg_grouped_mlp_bf16_fwd).  With ``weight_cache``
     the weights are read from it and w_gate_up / w_down may be None."""
@@ -353,7 +370,7 @@ def mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, saved, workspace, dev_
                    workspace.numel(), 1 if save_for_backward else 0, _ptr(dev_status, torch.int32, "dev_status"),
                    None if weight_cache is None else _ptr(weight_cache.buffer, torch.uint8, "weight_cache"),
                    0 if weight_cache is None else weight_cache.buffer.numel())
-    name = "mxg_grouped_mlp_bf16_fwd" if bf16 else "mxg_grouped_mlp_fwd"
+    name = "mxg_grouped_mlp_bf16_fwd" if bf16 else ("mxg_grouped_mlp_fp8_fwd" if fp8 else "mxg_grouped_mlp_fwd")
     if stage is None:
         _check(name, getattr(lib(), name)(ctypes.byref(a), _stream(stream)))
     else:
@@ -363,7 +380,7 @@ def mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, saved, workspace, dev_
 
 def mxg_grouped_mlp_bwd(dy, saved, workspace, dev_status, E: int, I: int, k: int, dx=None, dw_gate_up=None,
                         dw_down=None, dprobs=None, stream=None, stage: int | None = None, bf16: bool = False,
-                        weight_cache: WeightCache | None = None, main_grad=None):
+                        weight_cache: WeightCache | None = None, main_grad=None, fp8: bool = False):
     """Full backward, or one stage of it (BWD_STAGES index) when ``stage`` is given
     (``bf16``: the BF16 path, mxg_grouped_mlp_bf16_bwd).  ``weight_cache``: the
     cache the forward used.  ``main_grad`` = (fp32 [E, 2I, H], fp32 [E, H, I]):
@@ -388,7 +405,7 @@ def mxg_grouped_mlp_bwd(dy, saved, workspace, dev_status, E: int, I: int, k: int
                    None if weight_cache is None else _ptr(weight_cache.buffer, torch.uint8, "weight_cache"),
                    0 if weight_cache is None else weight_cache.buffer.numel(),
                    _ptr(mg_gu, torch.float32, "main_grad_gate_up"), _ptr(mg_d, torch.float32, "main_grad_down"))
-    name = "mxg_grouped_mlp_bf16_bwd" if bf16 else "mxg_grouped_mlp_bwd"
+    name = "mxg_grouped_mlp_bf16_bwd" if bf16 else ("mxg_grouped_mlp_fp8_bwd" if fp8 else "mxg_grouped_mlp_bwd")
     if stage is None:
         _check(name, getattr(lib(), name)(ctypes.byref(a), _stream(stream)))
     else:

@@ -45,6 +45,18 @@ __device__ __forceinline__ float mx_inv_scale(uint32_t byte) {
   return __uint_as_float((254u - byte) << 23);
 }
 
+// Per-tensor FP8 (current scaling): the MX scale rule with a whole tensor as
+// the block, from the tensor's largest magnitude amax: codes are E4M3(v *
+// fp8_scale(amax)), fp8_scale = 2^-(floor(log2 amax) - 8) (clamped like the
+// E8M0 byte); a GEMM on two such operands multiplies its fp32 accumulator by
+// fp8_dequant(amax_a) * fp8_dequant(amax_b), both exact powers of two.
+__device__ __forceinline__ float fp8_scale(float amax) {
+  return mx_inv_scale(mx_scale_byte(__float_as_uint(amax) & 0x7fffffffu));
+}
+__device__ __forceinline__ float fp8_dequant(float amax) {
+  return __uint_as_float(mx_scale_byte(__float_as_uint(amax) & 0x7fffffffu) << 23);
+}
+
 // Two fp32 -> two E4M3 codes (round to nearest even, saturate to +-448);
 // a in the low byte, b in the high byte.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b) {

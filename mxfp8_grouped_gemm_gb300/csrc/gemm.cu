@@ -54,18 +54,22 @@ constexpr int BK = 128;
 // epilogue (two per TMEM lane quadrant)
 constexpr int kThreads = 384;
 
-template <int BN, int EPI, bool PAIR, bool BF = false>
+// Operand kinds: MXFP8 (E4M3 + E8M0 block scales in TMEM), bf16, and E4M3
+// with one scale per expert tensor applied in the epilogue.
+enum Opk { OPK_MX = 0, OPK_BF16 = 1, OPK_F8 = 2 };
+
+template <int BN, int EPI, bool PAIR, int OPK = OPK_MX>
 struct Cfg {
   // contraction elements per stage: one 128-byte swizzle row of A and B
-  static constexpr int kKElems = BF ? 64 : 128;
+  static constexpr int kKElems = OPK == OPK_BF16 ? 64 : 128;
   static constexpr int CG = PAIR ? 2 : 1;
   static constexpr int kTileM = PAIR ? 2 * BM : BM;         // rows of one tile (both CTAs)
   static constexpr int kBRows = PAIR ? BN / 2 : BN;         // rows of B held by one CTA
   static constexpr int kAcc = BN == 128 ? 2 : 1;            // accumulator buffers in TMEM
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = kBRows * BK;
-  static constexpr int kSfaBytes = BF ? 0 : BM * 4;         // 128 rows x 4 blocks of 32
-  static constexpr int kSfbBytes = BF ? 0 : BN * 4;         // every CTA holds the tile's full SFB
+  static constexpr int kSfaBytes = OPK == OPK_MX ? BM * 4 : 0;   // 128 rows x 4 blocks of 32
+  static constexpr int kSfbBytes = OPK == OPK_MX ? BN * 4 : 0;   // every CTA holds the tile's full SFB
   static constexpr uint32_t kTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStageBytes = (kTx + 1023) / 1024 * 1024;
   // dSwiGLU: BN = 256 stages the tile's dH as bf16 rows (padded to 264) so the
@@ -80,7 +84,7 @@ struct Cfg {
   // 4 per 128 rows), so the copy for the next K step never overwrites scales
   // that MMAs still in the tensor pipe are reading.
   static constexpr uint32_t kSfCol = kAcc * BN;             // first TMEM column of the slots
-  static constexpr uint32_t kSfSlot = BF ? 0 : 4 + BN / 32;
+  static constexpr uint32_t kSfSlot = OPK == OPK_MX ? 4 + BN / 32 : 0;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kCtrlBytes + kXposeBytes;
   static_assert(kSfCol + kStages * kSfSlot <= 512, "TMEM budget");
   static_assert(kABytes == BM * 128, "stage rows are one 128-byte swizzle row");
@@ -197,6 +201,28 @@ __device__ __forceinline__ void row_store_bf16(const float (&h)[32], uint16_t* d
   st_global_v8(dst, w);
   st_global_v8(dst + 16, w + 8);
 }
+// The same store, returning the largest magnitude written (as bf16 bits:
+// non-negative bf16 values order like their bit patterns).
+__device__ __forceinline__ uint32_t row_store_bf16_amax(const float (&h)[32], uint16_t* dst) {
+  uint32_t w[16];
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    w[i] = pack_bf16x2(h[2 * i], h[2 * i + 1]);
+    m = max(m, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
+  }
+  st_global_v8(dst, w);
+  st_global_v8(dst + 16, w + 8);
+  return m;
+}
+
+// Per-tensor FP8: fold this warp's largest magnitude (bf16 bits) into the
+// expert tensor's amax (fp32 bits; non-negative floats order like integers).
+__device__ __forceinline__ void warp_amax_to(float* amax, uint32_t m_bf16, int lane) {
+  const uint32_t m = __reduce_max_sync(0xffffffffu, m_bf16);
+  if (lane == 0 && m != 0) atomicMax(reinterpret_cast<unsigned int*>(amax), m << 16);
+}
+
 __device__ __forceinline__ void col_store_bf16(const float (&h)[32], uint16_t* yc, int64_t ld, int64_t col0,
                                                int64_t tok0, int lane) {
   uint16_t* dst = yc + col0 * ld + tok0 + lane;
@@ -233,10 +259,19 @@ __device__ __forceinline__ void release_acc(const AccRelease& rl, int lane) {
 // bf16 store.  The thread owns half of its row's BN columns; it drains them
 // from TMEM into packed bf16 registers, releases the accumulator, then stores,
 // so the next tile's MMAs overlap the global stores.
-template <int BN, bool KG>
+// The factor that turns a per-tensor FP8 tile's accumulators into values:
+// the dequantisation factors of the expert's A and B tensors (1 otherwise).
+template <int OPK>
+__device__ __forceinline__ float tile_scale(const GemmArgs& P, const TileCoord& tc) {
+  if constexpr (OPK == OPK_F8) return fp8_dequant(P.amax_a[tc.e]) * fp8_dequant(P.amax_b[tc.e]);
+  return 1.f;
+}
+
+template <int BN, bool KG, int OPK>
 __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int row, int hf,
                                          const AccRelease& tempty, int lane) {
   constexpr int COLS = BN / 2;
+  const float f = tile_scale<OPK>(P, tc);
   uint32_t packed[COLS / 2];
 #pragma unroll
   for (int c = 0; c < COLS / 32; c += 2) {
@@ -246,8 +281,13 @@ __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc,
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      packed[c * 16 + i] = pack_bf16x2(u2f(r0[2 * i]), u2f(r0[2 * i + 1]));
-      packed[(c + 1) * 16 + i] = pack_bf16x2(u2f(r1[2 * i]), u2f(r1[2 * i + 1]));
+      if constexpr (OPK == OPK_F8) {
+        packed[c * 16 + i] = pack_bf16x2(u2f(r0[2 * i]) * f, u2f(r0[2 * i + 1]) * f);
+        packed[(c + 1) * 16 + i] = pack_bf16x2(u2f(r1[2 * i]) * f, u2f(r1[2 * i + 1]) * f);
+      } else {
+        packed[c * 16 + i] = pack_bf16x2(u2f(r0[2 * i]), u2f(r0[2 * i + 1]));
+        packed[(c + 1) * 16 + i] = pack_bf16x2(u2f(r1[2 * i]), u2f(r1[2 * i + 1]));
+      }
     }
   }
   release_acc(tempty, lane);
@@ -288,7 +328,7 @@ __device__ __forceinline__ void epi_acc_f32(const GemmArgs& P, const TileCoord& 
 // (j0 = nt * BN/2).  The thread owns BN/4 h columns (half hf).  It drains its
 // accumulator columns into registers, releases the accumulator, then computes
 // h in fp32 and quantises and stores while the next tile's MMAs run.
-template <int BN, bool BF>
+template <int BN, int OPK>
 __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
                                            int hf, const AccRelease& tempty) {
   constexpr int HC = BN / 2;          // h columns per tile
@@ -307,6 +347,17 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& t
   }
   tmem_ld_wait();
   release_acc(tempty, lane);
+  if constexpr (OPK == OPK_F8) {        // per-tensor FP8: accumulators -> values
+    const float f = tile_scale<OPK>(P, tc);
+#pragma unroll
+    for (int c = 0; c < CH; ++c)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        g[c][i] = f2u(u2f(g[c][i]) * f);
+        u[c][i] = f2u(u2f(u[c][i]) * f);
+      }
+  }
+  uint32_t hmax = 0;
 #pragma unroll
   for (int c = 0; c < CH; ++c) {
     const int64_t col = j0 + c * 32;
@@ -329,8 +380,8 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& t
       st_global_v8(gs + I, up);
       st_global_v8(gs + I + 16, up + 8);
     }
-    if constexpr (BF) {
-      row_store_bf16(h, P.y_row + r * P.y_row_ld + col);
+    if constexpr (OPK != OPK_MX) {
+      hmax = max(hmax, row_store_bf16_amax(h, P.y_row + r * P.y_row_ld + col));
       if (P.y_col != nullptr) col_store_bf16(h, P.y_col, P.y_col_ld, col, tok0, lane);
     } else {
       const uint32_t sb = row_quant32(h, P.q_out + r * P.q_out_ld + col);
@@ -338,6 +389,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& t
       if (P.qc_out != nullptr) col_quant32(h, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
     }
   }
+  if constexpr (OPK == OPK_F8) warp_amax_to(P.amax_out + tc.e, hmax, lane);
 }
 
 // dgrad-down tile: accumulator = dH columns nt*BN.., the thread owns half hf.
@@ -385,7 +437,7 @@ __device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& 
 
 // BN = 256: drain the thread's 128 dH columns to a bf16 staging row in shared
 // memory, release the accumulator, then run the dSwiGLU epilogue from there.
-template <bool BF>
+template <int OPK>
 __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q,
                                                    int lane, int hf, const AccRelease& tempty, uint16_t* stage_base) {
   constexpr int COLS = 128;
@@ -393,12 +445,20 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
   const int64_t tok0 = tc.m0 + q * 32;
   const int64_t r = tok0 + lane;
   uint16_t* srow = stage_base + (q * 32 + lane) * STRIDE + hf * COLS;
+  const float f = tile_scale<OPK>(P, tc);         // per-tensor FP8: accumulators -> dH
 #pragma unroll
   for (int c = 0; c < COLS / 32; c += 2) {
     uint32_t a0[32], a1[32];
     tmem_ld_32x32b_x32(tb + hf * COLS + c * 32, a0);
     tmem_ld_32x32b_x32(tb + hf * COLS + (c + 1) * 32, a1);
     tmem_ld_wait();
+    if constexpr (OPK == OPK_F8) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        a0[i] = f2u(u2f(a0[i]) * f);
+        a1[i] = f2u(u2f(a1[i]) * f);
+      }
+    }
     uint4* d0 = reinterpret_cast<uint4*>(srow + c * 32);
     uint4* d1 = reinterpret_cast<uint4*>(srow + (c + 1) * 32);
 #pragma unroll
@@ -414,6 +474,7 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
   const int64_t I = P.I;
   const int j0 = tc.nt * 256 + hf * COLS;
   float dp = 0.f;
+  uint32_t gmax = 0;
 #pragma unroll 1
   for (int c = 0; c < COLS / 32; ++c) {
     const int64_t col = j0 + c * 32;
@@ -431,11 +492,13 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
       u[i] = a * sl;
       dp += dh[i] * sl * uf;
     }
-    if constexpr (BF) {
-      row_store_bf16(dg, P.y_row + r * P.y_row_ld + col);
-      col_store_bf16(dg, P.y_col, P.y_col_ld, col, tok0, lane);
-      row_store_bf16(u, P.y_row + r * P.y_row_ld + I + col);
-      col_store_bf16(u, P.y_col, P.y_col_ld, I + col, tok0, lane);
+    if constexpr (OPK != OPK_MX) {
+      gmax = max(gmax, row_store_bf16_amax(dg, P.y_row + r * P.y_row_ld + col));
+      gmax = max(gmax, row_store_bf16_amax(u, P.y_row + r * P.y_row_ld + I + col));
+      if (P.y_col != nullptr) {
+        col_store_bf16(dg, P.y_col, P.y_col_ld, col, tok0, lane);
+        col_store_bf16(u, P.y_col, P.y_col_ld, I + col, tok0, lane);
+      }
     } else {
       uint32_t sb = row_quant32(dg, P.q_out + r * P.q_out_ld + col);
       P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
@@ -446,13 +509,14 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
     }
   }
   P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp;
+  if constexpr (OPK == OPK_F8) warp_amax_to(P.amax_out + tc.e, gmax, lane);
 }
 
-template <int BN, int EPI, bool KG, bool PAIR, bool BF>
+template <int BN, int EPI, bool KG, bool PAIR, int OPK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, const GemmArgs P) {
-  using C = Cfg<BN, EPI, PAIR, BF>;
+  using C = Cfg<BN, EPI, PAIR, OPK>;
   constexpr int CG = C::CG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -626,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(&full[stage], 2 * C::kTx);   // both CTAs' bytes
               tma_load_2d(sA, &tmA, kx, a_row, &full[stage]);
               tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
-              if constexpr (!BF) {
+              if constexpr (OPK == OPK_MX) {
                 tma_load_2d(sSfa, &tmSA, 0, sa_atom, &full[stage]);
                 tma_load_2d(sSfb, &tmSB, 0, sb_atom0, &full[stage]);
                 tma_load_2d(sSfb + 512, &tmSB, 0, sb_atom1, &full[stage]);
@@ -635,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t bar0 = full0 + stage * 8;
               tma_load_2d_pair(sA, &tmA, kx, a_row, bar0);
               tma_load_2d_pair(sB, &tmB, kx, b_row0, bar0);
-              if constexpr (!BF) {
+              if constexpr (OPK == OPK_MX) {
                 tma_load_2d_pair(sSfa, &tmSA, 0, sa_atom, bar0);
                 tma_load_2d_pair(sSfb, &tmSB, 0, sb_atom0, bar0);
                 tma_load_2d_pair(sSfb + 512, &tmSB, 0, sb_atom1, bar0);
@@ -644,17 +708,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             mbar_arrive_expect_tx(&full[stage], C::kTx);
             tma_load_2d(sA, &tmA, kx, a_row, &full[stage]);
-            if constexpr (!BF) bulk_load(sSfa, P.sa + (kc * (P.a_rows >> 7) + (a_row >> 7)) * 512, 512, &full[stage]);
+            if constexpr (OPK == OPK_MX) bulk_load(sSfa, P.sa + (kc * (P.a_rows >> 7) + (a_row >> 7)) * 512, 512, &full[stage]);
             if (EPI == EPI_SWIGLU) {
               tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
               tma_load_2d(sB + 128 * 128, &tmB, kx, b_row1, &full[stage]);
-              if constexpr (!BF) {
+              if constexpr (OPK == OPK_MX) {
                 bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (b_row0 >> 7)) * 512, 512, &full[stage]);
                 bulk_load(sSfb + 512, P.sb + (kc * (P.b_rows >> 7) + (b_row1 >> 7)) * 512, 512, &full[stage]);
               }
             } else {
               tma_load_2d(sB, &tmB, kx, b_row0, &full[stage]);
-              if constexpr (!BF) bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (sfb0 >> 7)) * 512, BN * 4, &full[stage]);
+              if constexpr (OPK == OPK_MX) bulk_load(sSfb, P.sb + (kc * (P.b_rows >> 7) + (sfb0 >> 7)) * 512, BN * 4, &full[stage]);
             }
           }
           if (++stage == C::kStages) {
@@ -688,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // MXFP8: the copier thread has seen the stage's data land and its
           // scale factors are in TMEM slot `stage`; bf16: wait for the data
           bool in;
-          if constexpr (BF)
+          if constexpr (OPK != OPK_MX)
             in = PAIR ? mbar_wait_bounded_cluster(&full[stage], phase, abort_flag, limit_ns)
                       : mbar_wait_bounded(&full[stage], phase, abort_flag, limit_ns);
           else
@@ -703,11 +767,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sB = sA + C::kABytes;
           const uint64_t adesc = smem_desc(smem_u32(sA), 0, 1024, kLayoutSwizzle128B);
           const uint64_t bdesc = smem_desc(smem_u32(sB), 0, 1024, kLayoutSwizzle128B);
-          if constexpr (BF) {
+          if constexpr (OPK == OPK_BF16) {
             // four K = 16 steps of 32 bytes per 128-byte stage row
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_bf16<CG>(d_t, adesc + 2 * k, bdesc + 2 * k, idesc_bf16(C::kTileM, BN), (kb | k) != 0 ? 1u : 0u);
+          } else if constexpr (OPK == OPK_F8) {
+            // four K = 32 steps of E4M3 without scale factors
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_f8<CG>(d_t, adesc + 2 * k, bdesc + 2 * k, idesc_f8_e4m3(C::kTileM, BN), (kb | k) != 0 ? 1u : 0u);
           } else {
             const uint32_t sfa_t = tmem + C::kSfCol + stage * C::kSfSlot;
             const uint32_t sfb_t = sfa_t + 4;
@@ -743,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Waits for each stage's data and copies its scale factors into the
     // stage's TMEM slot.  Kept off the MMA thread: a barrier wait followed by
     // a shared->TMEM copy on the issuing thread starves the tensor pipe.
-    if (!BF && lane == 0 && rank == 0) {
+    if (OPK == OPK_MX && lane == 0 && rank == 0) {
       uint32_t stage = 0, phase = 0;
       bool aborted = false;
       for (int64_t t = tile0; t < total && !aborted; t += tstep) {
@@ -816,14 +885,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       rel.bar = rel.peer ? map_to_rank(smem_u32(&tempty[acc]), 0) : smem_u32(&tempty[acc]);
       rel.land = rel.peer ? map_to_rank(smem_u32(&landing[warp - 4]), 0) : 0u;
       if constexpr (EPI == EPI_SWIGLU) {
-        epi_swiglu<BN, BF>(P, tc, tb, q, lane, hf, rel);
+        epi_swiglu<BN, OPK>(P, tc, tb, q, lane, hf, rel);
       } else if constexpr (EPI == EPI_DSWIGLU) {
-        if constexpr (BN == 256) epi_dswiglu_staged<BF>(P, tc, tb, q, lane, hf, rel, reinterpret_cast<uint16_t*>(xpose));
+        if constexpr (BN == 256) epi_dswiglu_staged<OPK>(P, tc, tb, q, lane, hf, rel, reinterpret_cast<uint16_t*>(xpose));
         else epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
       } else if constexpr (EPI == EPI_ACC_F32) {
         epi_acc_f32<BN>(P, tc, tb, row, hf, rel, lane);
       } else {
-        epi_bf16<BN, KG>(P, tc, tb, row, hf, rel, lane);
+        epi_bf16<BN, KG, OPK>(P, tc, tb, row, hf, rel, lane);
       }
       if (++acc == C::kAcc) {
         acc = 0;
@@ -906,19 +975,19 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int BN, int EPI, bool KG, bool PAIR, bool BF = false>
+template <int BN, int EPI, bool KG, bool PAIR, int OPK = OPK_MX>
 cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
-  using C = Cfg<BN, EPI, PAIR, BF>;
+  using C = Cfg<BN, EPI, PAIR, OPK>;
   CUtensorMap ta, tb;
   const int b_box = (EPI == EPI_SWIGLU && !PAIR) ? 128 : C::kBRows;
-  if (BF) {
+  if (OPK == OPK_BF16) {
     if (!encode_bf16(&ta, g.a, g.a_cols, g.a_rows, BM)) return cudaErrorInvalidValue;
     if (!encode_bf16(&tb, g.b, g.b_cols, g.b_rows, b_box)) return cudaErrorInvalidValue;
   } else {
     if (!encode_u8(&ta, g.a, g.a_cols, g.a_rows, BK, BM)) return cudaErrorInvalidValue;
     if (!encode_u8(&tb, g.b, g.b_cols, g.b_rows, BK, b_box)) return cudaErrorInvalidValue;
   }
-  auto kern = gemm_kernel<BN, EPI, KG, PAIR, BF>;
+  auto kern = gemm_kernel<BN, EPI, KG, PAIR, OPK>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (err != cudaSuccess) return err;
   const int64_t units = PAIR ? num_sms() / 2 : num_sms();     // CTAs, or CTA pairs
@@ -940,7 +1009,7 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
   }
   // scale tensors as rows of 512-byte atoms, for the CTA pair's TMA loads
   CUtensorMap tsa = ta, tsb = tb;
-  if (PAIR && !BF) {
+  if (PAIR && OPK == OPK_MX) {
     if (!encode_atoms(&tsa, g.sa, (g.a_rows / 128) * (g.a_cols / 128))) return cudaErrorInvalidValue;
     if (!encode_atoms(&tsb, g.sb, (g.b_rows / 128) * (g.b_cols / 128))) return cudaErrorInvalidValue;
   }
@@ -962,10 +1031,17 @@ int dswiglu_partials(int I) { return 2 * (I / gemm_pick_bn(EPI_DSWIGLU, I)); }
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
   if (g.bf16) {  // BF16 path: CTA-pair tiles only
     if (!g.pair) return cudaErrorInvalidValue;
-    if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, true, true>(g, s);
-    if (g.epi == EPI_DSWIGLU) return launch_impl<256, EPI_DSWIGLU, false, true, true>(g, s);
-    if (g.kgroup) return launch_impl<256, EPI_BF16, true, true, true>(g, s);
-    return launch_impl<256, EPI_BF16, false, true, true>(g, s);
+    if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, true, OPK_BF16>(g, s);
+    if (g.epi == EPI_DSWIGLU) return launch_impl<256, EPI_DSWIGLU, false, true, OPK_BF16>(g, s);
+    if (g.kgroup) return launch_impl<256, EPI_BF16, true, true, OPK_BF16>(g, s);
+    return launch_impl<256, EPI_BF16, false, true, OPK_BF16>(g, s);
+  }
+  if (g.fp8) {  // FP8 path (per-tensor scales): CTA-pair tiles only
+    if (!g.pair || g.amax_a == nullptr || g.amax_b == nullptr) return cudaErrorInvalidValue;
+    if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, true, OPK_F8>(g, s);
+    if (g.epi == EPI_DSWIGLU) return launch_impl<256, EPI_DSWIGLU, false, true, OPK_F8>(g, s);
+    if (g.kgroup) return launch_impl<256, EPI_BF16, true, true, OPK_F8>(g, s);
+    return launch_impl<256, EPI_BF16, false, true, OPK_F8>(g, s);
   }
   if (g.pair) {  // CTA-pair tiles, 256 x 256
     if (g.epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, false, true>(g, s);

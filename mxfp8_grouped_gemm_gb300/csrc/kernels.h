@@ -32,8 +32,35 @@ struct QuantParams {
   // bf16 pass-through (the BF16 path): the staged rows copied out unchanged
   uint16_t* b_row;            // nullable: [batch*rows][cols] (gathered copy)
   uint16_t* b_col;            // nullable: [batch*cols][ld_col] (transposed copy)
+  // per-tensor FP8 (the FP8 path): when pt_amax is set, codes are E4M3(v * s)
+  // with s = fp8_scale(pt_amax[g]) for the tile's tensor g (the row group of
+  // pt_group_off [pt_groups + 1] that holds the tile, else the batch index);
+  // q_row / q_col get the codes, no scales are written
+  const float* pt_amax;
+  const int32_t* pt_group_off;
+  int32_t pt_groups;
 };
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
+
+// Largest magnitude of each tensor of a bf16 matrix batch (per-tensor FP8):
+// rows optionally gathered like QuantParams; a tensor is a row group of
+// group_off [groups + 1] (rows 32-aligned in groups) or a batch.  amax holds
+// fp32 values and must be zeroed by the caller (the kernel takes maxima).
+struct AmaxParams {
+  const uint16_t* x;
+  int64_t ld_x;
+  int64_t x_batch_stride;
+  const int32_t* src_rows;    // nullable: row p reads source row src_rows[p]/src_div; -1 = zero row
+  int32_t src_div;
+  int32_t rows;               // rows per batch (multiple of 32)
+  int32_t cols;               // multiple of 256
+  int32_t batch;
+  const int32_t* rows_valid;  // nullable device scalar
+  const int32_t* group_off;   // nullable
+  int32_t groups;
+  float* amax;
+};
+cudaError_t launch_amax(const AmaxParams& p, cudaStream_t s);
 
 // ------------------------------------------------------------ route/permute
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* probs, cudaStream_t s);
@@ -106,6 +133,14 @@ struct GemmArgs {
   int64_t y_row_ld;
   uint16_t* y_col;            // [cols][..] bf16 transposed output (h^T, or dGU^T)
   int64_t y_col_ld;
+  // FP8 path: E4M3 operands with one power-of-two scale per expert tensor (no scale
+  // factors); the epilogue multiplies by fp8_dequant(amax_a[e]) *
+  // fp8_dequant(amax_b[e]) and writes bf16 like the BF16 path, adding the
+  // largest magnitude of the bf16 h / dGU it writes into amax_out[e]
+  bool fp8;
+  const float* amax_a;
+  const float* amax_b;
+  float* amax_out;
   float* dacc;                // EPI_ACC_F32 (token-grouped): fp32 [E][M][N] that the tile is added into
   int64_t tiles_upper;        // host bound on the number of tiles (grid sizing)
   uint64_t wait_limit_ns;     // bound on every wait inside the kernel (0: default)

@@ -242,6 +242,27 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint6
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, bf16 operands, fp32 accumulators.
+// E4M3 x E4M3 -> fp32 without scale factors (kind::f8f6f4; the per-tensor
+// scales are applied by the caller).
+template <int CG>
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  if constexpr (CG == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 template <int CG>
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -322,6 +343,13 @@ constexpr uint32_t kLayoutNone = 0;
 __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(uint32_t M, uint32_t N, uint32_t sfa_id, uint32_t sfb_id) {
   return ((sfb_id & 3u) << 4) | (0u << 7) | (0u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
          ((sfa_id & 3u) << 29);
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (both K-major, no
+// scale factors) and fp32 accumulators: D format [4,6) (1 = f32), A/B format
+// [7,10) / [10,13) (0 = E4M3), N>>3 [17,23), M>>4 [24,29).
+__host__ __device__ constexpr uint32_t idesc_f8_e4m3(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A and B (both K-major) and

@@ -43,6 +43,17 @@ __device__ __forceinline__ void quant_store32(float (&v)[32], uint8_t* dst, uint
   *sdst = static_cast<uint8_t>(sb);
 }
 
+// Per-tensor FP8: the thread's 32 values times the tensor's scale, as codes.
+__device__ __forceinline__ void quant_store32_pt(float (&v)[32], uint8_t* dst, float s) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] *= s;
+  uint32_t w[8];
+  encode32(v, w);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
                "l"(gsrc)
@@ -65,7 +76,7 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t (&r)[4]) 
 // 8j+2m+1); the quad reduces the block maximum with two shuffles and each lane
 // writes its 8 codes as one 8-byte store.
 __device__ __forceinline__ void quant_col_block(const QuantParams& P, const uint16_t* buf, int col0, int64_t gcol0,
-                                                int p0, int lane) {
+                                                int p0, int lane, float pt_s) {
   const int m = lane >> 3, i = lane & 7;
   const int srow = 8 * (i >> 1) + 2 * m + (i & 1);
   const uint16_t* rowp = buf + srow * kStride;
@@ -80,20 +91,25 @@ __device__ __forceinline__ void quant_col_block(const QuantParams& P, const uint
       v[2 * q] = __uint_as_float(r[q] << 16);
       v[2 * q + 1] = __uint_as_float(r[q] & 0xffff0000u);
     }
-    uint32_t amax = 0;
+    uint32_t sb = 0;
+    float inv = pt_s;                         // per-tensor FP8: the tensor's scale
+    if (P.pt_amax == nullptr) {               // MX: the block's own scale
+      uint32_t amax = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) amax = max(amax, __float_as_uint(v[q]) & 0x7fffffffu);
-    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const uint32_t sb = mx_scale_byte(amax);
-    const float inv = mx_inv_scale(sb);
+      for (int q = 0; q < 8; ++q) amax = max(amax, __float_as_uint(v[q]) & 0x7fffffffu);
+      amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      sb = mx_scale_byte(amax);
+      inv = mx_inv_scale(sb);
+    }
     uint32_t w[2];
 #pragma unroll
     for (int q = 0; q < 2; ++q)
       w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
     const int64_t gcol = gcol0 + ct * 8 + (lane >> 2);
     *reinterpret_cast<uint2*>(P.q_col + gcol * P.ld_col + p0 + 8 * j) = make_uint2(w[0], w[1]);
-    if (j == 0) P.s_col[sf_offset(P.layout, gcol, p0 >> 5, P.sf_col_rows, P.ld_col >> 5)] = static_cast<uint8_t>(sb);
+    if (j == 0 && P.pt_amax == nullptr)
+      P.s_col[sf_offset(P.layout, gcol, p0 >> 5, P.sf_col_rows, P.ld_col >> 5)] = static_cast<uint8_t>(sb);
   }
 }
 
@@ -177,6 +193,15 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
     }
     __syncthreads();
     const uint16_t* buf = tile[t & 1];
+    float pt_s = 1.f;
+    if (P.pt_amax != nullptr) {
+      int g = b;
+      if (P.pt_group_off != nullptr) {      // the row group holding this tile (groups are 32-row aligned)
+        g = 0;
+        while (g + 1 < P.pt_groups && P.pt_group_off[g + 1] <= p0) ++g;
+      }
+      pt_s = fp8_scale(P.pt_amax[g]);
+    }
     if (P.probs_perm != nullptr && blockIdx.y == 0 && b == 0 && tid < kRows) {
       const int pp = p0 + tid;
       const int f = P.src_rows != nullptr ? P.src_rows[pp] : pp;
@@ -198,12 +223,15 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
         }
       }
       const int64_t grow = static_cast<int64_t>(b) * P.rows + p;
-      quant_store32(v, P.q_row + grow * P.cols + c0 + j * 32,
-                    P.s_row + sf_offset(P.layout, grow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5));
+      if (P.pt_amax != nullptr)
+        quant_store32_pt(v, P.q_row + grow * P.cols + c0 + j * 32, pt_s);
+      else
+        quant_store32(v, P.q_row + grow * P.cols + c0 + j * 32,
+                      P.s_row + sf_offset(P.layout, grow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5));
     }
     if (P.q_col != nullptr) {
       const int warp = tid >> 5;
-      quant_col_block(P, buf, warp * 32, static_cast<int64_t>(b) * P.cols + c0 + warp * 32, p0, tid & 31);
+      quant_col_block(P, buf, warp * 32, static_cast<int64_t>(b) * P.cols + c0 + warp * 32, p0, tid & 31, pt_s);
     }
     if (P.b_row != nullptr) {
       const int r = tid >> 2, j = tid & 3;
@@ -220,7 +248,57 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
   }
 }
 
+// Largest magnitude per tensor: a CTA of 256 threads reads a 32-row x
+// 256-column tile (thread t: row t/8, 32 columns, four 16-byte loads), reduces
+// over the warp and adds one atomic maximum per warp (non-negative floats
+// order like their bit patterns).
+__global__ void __launch_bounds__(256) amax_kernel(const AmaxParams P) {
+  const int b = blockIdx.z;
+  const int p0 = blockIdx.x * 32;
+  int limit = P.rows;
+  if (P.rows_valid != nullptr) limit = min(limit, *P.rows_valid);
+  if (p0 >= limit) return;
+  const int p = p0 + (threadIdx.x >> 3);
+  const int c = blockIdx.y * 256 + (threadIdx.x & 7) * 32;
+  uint32_t m = 0;
+  if (p < limit) {
+    int64_t srow = p;
+    if (P.src_rows != nullptr) {
+      const int f = P.src_rows[p];
+      srow = f < 0 ? -1 : f / P.src_div;
+    }
+    if (srow >= 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(P.x + static_cast<int64_t>(b) * P.x_batch_stride +
+                                                        srow * P.ld_x + c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 q = src[i];
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) m = max(m, max((w[h] << 16) & 0x7fffffffu, w[h] & 0x7fff0000u));
+      }
+    }
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0 && m != 0) {
+    int g = b;
+    if (P.group_off != nullptr) {
+      g = 0;
+      while (g + 1 < P.groups && P.group_off[g + 1] <= p0) ++g;
+    }
+    atomicMax(reinterpret_cast<unsigned int*>(P.amax + g), m);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_amax(const AmaxParams& p, cudaStream_t s) {
+  dim3 grid((p.rows + 31) / 32, p.cols / 256, p.batch);
+  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
+  amax_kernel<<<grid, 256, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s) {
   dim3 grid((p.rows / kRows + kTilesPerCta - 1) / kTilesPerCta, p.cols / kCols, p.batch);

@@ -8,25 +8,35 @@ import torch
 from . import _lib
 
 
+def precision_is_not_mx(layer) -> bool:
+    return layer.precision != "mxfp8"
+
+
 class GroupedMLP:
-    """precision "mxfp8" (the path) or "bf16" (the like-for-like BF16 reference:
-    H and I multiples of 256)."""
+    """precision "mxfp8" (the path), "bf16" (the like-for-like BF16 reference) or
+    "fp8" (per-tensor FP8, one scale per expert tensor); bf16 and fp8 need H and
+    I multiples of 256."""
 
     def __init__(self, T: int, H: int, I: int, E: int, k: int, device="cuda", precision: str = "mxfp8"):
-        if precision not in ("mxfp8", "bf16"):
-            raise ValueError(f"precision must be 'mxfp8' or 'bf16', got {precision!r}")
+        if precision not in ("mxfp8", "bf16", "fp8"):
+            raise ValueError(f"precision must be 'mxfp8', 'bf16' or 'fp8', got {precision!r}")
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        self.precision = precision
         self.bf16 = precision == "bf16"
+        self.fp8 = precision == "fp8"
         self.device = torch.device(device)
         if self.bf16:
             saved = _lib.mxg_mlp_bf16_saved_bytes(T, H, I, E, k)
             ws = _lib.mxg_mlp_bf16_workspace_bytes(T, H, I, E, k)
+        elif self.fp8:
+            saved = _lib.mxg_mlp_fp8_saved_bytes(T, H, I, E, k)
+            ws = _lib.mxg_mlp_fp8_workspace_bytes(T, H, I, E, k)
         else:
             saved = _lib.mxg_mlp_saved_bytes(T, H, I, E, k)
             ws = _lib.mxg_mlp_workspace_bytes(T, H, I, E, k)
         if saved == 0 or ws == 0:
             raise ValueError(f"unsupported {precision} shape T={T} H={H} I={I} E={E} k={k} "
-                             f"(H, I multiples of {256 if self.bf16 else 128}; k <= E <= 256)")
+                             f"(H, I multiples of {128 if precision == 'mxfp8' else 256}; k <= E <= 256)")
         self.saved = torch.empty(saved, dtype=torch.uint8, device=self.device)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=self.device)
@@ -49,7 +59,7 @@ class GroupedMLP:
         """Quantise the weights once into this layer's weight cache (MXFP8 path):
         forward calls given no weights then read it, e.g. for every micro-batch
         of one optimizer step."""
-        if self.bf16:
+        if precision_is_not_mx(self):
             raise NotImplementedError("the weight cache holds MXFP8 weights")
         self.weight_cache = _lib.mxg_mlp_quantize_weights(w_gate_up, w_down, self.weight_cache, stream=stream)
         return self.weight_cache
@@ -64,7 +74,7 @@ class GroupedMLP:
         return _lib.mxg_grouped_mlp_fwd(x, ids, probs, w_gate_up, w_down, self.saved, self.workspace,
                                         self.dev_status, y=self.y if y is None else y,
                                         split_sizes=self.split_sizes, save_for_backward=save_for_backward,
-                                        stream=stream, stage=stage, bf16=self.bf16,
+                                        stream=stream, stage=stage, bf16=self.bf16, fp8=self.fp8,
                                         weight_cache=self.weight_cache if cached else None)
 
     def backward(self, dy, stream=None, stage=None, dx=None, main_grad=None):
@@ -75,7 +85,7 @@ class GroupedMLP:
                                         dw_gate_up=None if main_grad is not None else self.dw_gate_up,
                                         dw_down=None if main_grad is not None else self.dw_down,
                                         dprobs=self.dprobs, stream=stream, stage=stage, bf16=self.bf16,
-                                        weight_cache=self.weight_cache if self._fwd_cached else None,
+                                        fp8=self.fp8, weight_cache=self.weight_cache if self._fwd_cached else None,
                                         main_grad=main_grad)
 
     def step(self, logits, x, w_gate_up, w_down, dy, stream=None):
@@ -89,7 +99,7 @@ class GroupedMLP:
 
     def gu_view(self) -> torch.Tensor:
         """The gate-up GEMM output (bf16 [m_cap, 2I]) kept in the saved buffer (MXFP8 path)."""
-        if self.bf16:
+        if precision_is_not_mx(self):
             raise NotImplementedError("gu_view reads the MXFP8 path's saved layout")
         base = self.saved.data_ptr()
         off = _lib.mxg_mlp_saved_view(self.saved, self.T, self.H, self.I, self.E, self.k, 0) - base
@@ -97,7 +107,7 @@ class GroupedMLP:
         return self.saved[off:off + m_cap * 2 * self.I * 2].view(torch.bfloat16).view(m_cap, 2 * self.I)
 
     def padded_offsets(self) -> torch.Tensor:
-        if self.bf16:
+        if precision_is_not_mx(self):
             raise NotImplementedError("padded_offsets reads the MXFP8 path's saved layout")
         base = self.saved.data_ptr()
         off = _lib.mxg_mlp_saved_view(self.saved, self.T, self.H, self.I, self.E, self.k, 1) - base

@@ -256,3 +256,27 @@ def test_weight_cache_and_main_grad_validation(L):
     b2 = m.MlpBwdArgs(256, H2, I2, E, 2, FAKE, FAKE, 1 << 40, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, FAKE, None, 0,
                       FAKE, FAKE)
     assert L.mxg_grouped_mlp_bf16_bwd(ctypes.byref(b2), None) == 1
+
+
+def test_fp8_mlp_sizes_and_validation(L):
+    import mxfp8_grouped_gemm_gb300 as m
+    assert L.mxg_mlp_fp8_saved_bytes(256, 256, 512, 4, 2) > 0
+    assert L.mxg_mlp_fp8_workspace_bytes(256, 256, 512, 4, 2) > 0
+    assert L.mxg_mlp_fp8_saved_bytes(256, 128, 512, 4, 2) == 0       # H not a multiple of 256
+    assert L.mxg_mlp_fp8_saved_bytes(256, 256, 384, 4, 2) == 0       # I not a multiple of 256
+    a = m.MlpFwdArgs(256, 128, 512, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, FAKE, 1 << 30, 1,
+                     FAKE, None, 0)
+    assert L.mxg_grouped_mlp_fp8_fwd(ctypes.byref(a), None) == 2
+    a = m.MlpFwdArgs(256, 256, 512, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, FAKE, 1 << 30, 1, FAKE,
+                     None, 0)
+    assert L.mxg_grouped_mlp_fp8_fwd(ctypes.byref(a), None) == 5      # saved buffer too small
+    bad = m.MlpFwdArgs.from_buffer_copy(a); bad.x = MISALIGNED; bad.saved_bytes = 1 << 30
+    assert L.mxg_grouped_mlp_fp8_fwd(ctypes.byref(bad), None) == 3
+    bad = m.MlpFwdArgs.from_buffer_copy(a); bad.weight_cache = FAKE
+    assert L.mxg_grouped_mlp_fp8_fwd(ctypes.byref(bad), None) == 1    # the weight cache is MXFP8-only
+    b = m.MlpBwdArgs(256, 256, 512, 4, 2, FAKE, FAKE, 1 << 30, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, FAKE, None, 0,
+                     FAKE, FAKE)
+    assert L.mxg_grouped_mlp_fp8_bwd(ctypes.byref(b), None) == 1      # main_grad is MXFP8-only
+    assert L.mxg_grouped_mlp_fp8_fwd_stage(ctypes.byref(a), 99, None) == 1
+    assert L.mxg_mlp_fp8_saved_view(None, 256, 256, 512, 4, 2, 0) is None
+    assert L.mxg_mlp_fp8_saved_view(FAKE, 256, 256, 512, 4, 2, 9) is None
