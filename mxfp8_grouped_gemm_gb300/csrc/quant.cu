@@ -27,10 +27,21 @@ constexpr int kStride = kCols + 8;   // bf16 per smem row (272 bytes: 16-byte al
 // groups.
 __device__ __forceinline__ int chunk_pos(int r, int c) { return c ^ (((r >> 3) & 3) << 1); }
 
-__device__ __forceinline__ void quant_store32(float (&v)[32], uint8_t* dst, uint8_t* sdst) {
-  uint32_t amax = 0;
+// Largest magnitude of packed bf16 pairs, as fp32 bits (non-negative bf16
+// values compare like floats; the sign bits are cleared first).
+__device__ __forceinline__ uint32_t pair_max_bits(const uint32_t* w, int n) {
+  const uint32_t z = 0;
+  __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162*>(&z);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
+  for (int i = 0; i < n; ++i) {
+    const uint32_t a = w[i] & 0x7fff7fffu;
+    m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162*>(&a));
+  }
+  const uint32_t mm = *reinterpret_cast<const uint32_t*>(&m);
+  return max(mm << 16, mm & 0xffff0000u);
+}
+
+__device__ __forceinline__ void quant_store32(float (&v)[32], uint8_t* dst, uint8_t* sdst, uint32_t amax) {
   const uint32_t sb = mx_scale_byte(amax);
   const float inv = mx_inv_scale(sb);
 #pragma unroll
@@ -94,9 +105,7 @@ __device__ __forceinline__ void quant_col_block(const QuantParams& P, const uint
     uint32_t sb = 0;
     float inv = pt_s;                         // per-tensor FP8: the tensor's scale
     if (P.pt_amax == nullptr) {               // MX: the block's own scale
-      uint32_t amax = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) amax = max(amax, __float_as_uint(v[q]) & 0x7fffffffu);
+      uint32_t amax = pair_max_bits(r, 4);
       amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       sb = mx_scale_byte(amax);
@@ -211,23 +220,29 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
       const int r = tid >> 2, j = tid & 3;
       const int p = p0 + r;
       float v[32];
+      uint32_t wv[16];
       const uint4* s4 = reinterpret_cast<const uint4*>(buf + r * kStride);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint4 q = s4[chunk_pos(r, 4 * j + i)];
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        wv[4 * i] = q.x;
+        wv[4 * i + 1] = q.y;
+        wv[4 * i + 2] = q.z;
+        wv[4 * i + 3] = q.w;
+      }
+      const uint32_t blk_max = pair_max_bits(wv, 16);
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          v[8 * i + 2 * h] = __uint_as_float(w[h] << 16);
-          v[8 * i + 2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
-        }
+      for (int h = 0; h < 16; ++h) {
+        v[2 * h] = __uint_as_float(wv[h] << 16);
+        v[2 * h + 1] = __uint_as_float(wv[h] & 0xffff0000u);
       }
       const int64_t grow = static_cast<int64_t>(b) * P.rows + p;
       if (P.pt_amax != nullptr)
         quant_store32_pt(v, P.q_row + grow * P.cols + c0 + j * 32, pt_s);
       else
         quant_store32(v, P.q_row + grow * P.cols + c0 + j * 32,
-                      P.s_row + sf_offset(P.layout, grow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5));
+                      P.s_row + sf_offset(P.layout, grow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5),
+                      blk_max);
     }
     if (P.q_col != nullptr) {
       const int warp = tid >> 5;
