@@ -6,6 +6,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "api_common.h"
 #include "kernels.h"
 
 namespace mxg {
@@ -15,10 +16,7 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
 
-constexpr int64_t kAlign = 256;
-
-inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
-inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+using namespace api;
 
 // CTA-pair GEMM tiles (256 x 256 over two SMs) for the MLP's GEMMs whose
 // output width is a multiple of 256.  Measured on GB300 (Mixtral layer): the
@@ -31,14 +29,6 @@ constexpr bool kUsePairTiles = true;
 constexpr int kMlpAlign = kUsePairTiles ? 256 : 128;
 inline int64_t row_cap(int64_t T, int64_t k, int64_t E) { return align_up(T * k, kMlpAlign) + kMlpAlign * E; }
 
-struct Carver {
-  int64_t off = 0;
-  int64_t take(int64_t bytes) {
-    const int64_t o = off;
-    off = align_up(off + bytes, kAlign);
-    return o;
-  }
-};
 
 // Byte offsets of every buffer inside `saved` and `workspace`.
 struct Plan {
@@ -123,21 +113,8 @@ struct WPlan {
   }
 };
 
-template <typename T>
-inline T* at(void* base, int64_t off) {
-  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
-}
-template <typename T>
-inline const T* at(const void* base, int64_t off) {
-  return reinterpret_cast<const T*>(static_cast<const uint8_t*>(base) + off);
-}
 
-inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA; }
 
-#define MXG_TRY(expr)                                 \
-  do {                                                \
-    if ((expr) != cudaSuccess) return MXG_ERR_CUDA;   \
-  } while (0)
 
 bool mlp_shape_ok(int T, int H, int I, int E, int k) {
   if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return false;

@@ -19,39 +19,19 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "api_common.h"
 #include "kernels.h"
 
 namespace mxg {
 namespace {
 
-constexpr int64_t kAlign = 256;
+using namespace api;
+
 constexpr int kGroupAlign = 256;   // CTA-pair tile height
 
-inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
-inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
-struct Carver {
-  int64_t off = 0;
-  int64_t take(int64_t bytes) {
-    const int64_t o = off;
-    off = align_up(off + bytes, kAlign);
-    return o;
-  }
-};
 
-template <typename T>
-inline T* at(void* base, int64_t off) {
-  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
-}
-template <typename T>
-inline const T* at(const void* base, int64_t off) {
-  return reinterpret_cast<const T*>(static_cast<const uint8_t*>(base) + off);
-}
 
-#define MXG_TRY(expr)                                 \
-  do {                                                \
-    if ((expr) != cudaSuccess) return MXG_ERR_CUDA;   \
-  } while (0)
 
 bool shape_ok(int T, int H, int I, int E, int k) {
   if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return false;
