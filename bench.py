@@ -416,6 +416,10 @@ def run_ours(args, rank, world):
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                 "frac": None, "traffic": None}
     gemm_ms = sum(stage_ms[s_] for s_ in stage_flops)
+    gemm_kernels = {"peak_tflops": round(p_mx, 1),
+                    **{s_: {"tflops": round(f / (stage_ms[s_] * 1e-3) / 1e12, 1),
+                            "frac": round(f / (stage_ms[s_] * 1e-3) / 1e12 / p_mx, 4)}
+                       for s_, f in stage_flops.items()}}
     # memory-bound kernels against the measured copy bandwidth: algorithmic
     # bytes (each input read once, each output written once) / CUDA-event time
     Rc = m.mxg_mlp_row_capacity(T, k, E)
@@ -448,6 +452,7 @@ def run_ours(args, rank, world):
         "split_sizes": {"min": int(split.min()), "max": int(split.max()), "mean": float(split.mean()),
                         "zeros": int((split == 0).sum())},
         "roofline": roof,
+        "gemm_kernels": gemm_kernels,
         "hbm_kernels": {"peak_gbs": float(peaks["hbm_gbs"]), "peak_source": f"{peaks_kind} copy", **hbm},
         "gpu_launches": int(round(launches)),
         "clocks": clk,
