@@ -400,7 +400,9 @@ const void* mxg_mlp_fp8_saved_view(const void* saved, int T, int H, int I, int E
  * tests to compare intermediates: 0 = GU (bf16 [m_cap][2I], the gate-up GEMM
  * output before the activation; m_cap = mxg_mlp_row_capacity), 1 =
  * padded_offsets (int32 [E+1], multiples of mxg_mlp_group_align()), 2 =
- * row_of_src in the padded layout (int32 [T*k]). */
+ * row_of_src in the padded layout (int32 [T*k]), 3 / 4 = x's token-column-wise
+ * codes (uint8 [H][m_cap]) / scales (tensor-core layout, H rows x m_cap/32
+ * blocks), 5 / 6 = the same for h (I rows). */
 const void* mxg_mlp_saved_view(const void* saved, int T, int H, int I, int E, int k, int which);
 
 #ifdef __cplusplus

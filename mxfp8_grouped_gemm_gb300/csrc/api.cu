@@ -419,6 +419,10 @@ const void* mxg_mlp_saved_view(const void* saved, int T, int H, int I, int E, in
     case 0: return at<uint8_t>(saved, pl.gu);
     case 1: return at<uint8_t>(saved, pl.poff);
     case 2: return at<uint8_t>(saved, pl.prow_of_src);
+    case 3: return at<uint8_t>(saved, pl.xc);
+    case 4: return at<uint8_t>(saved, pl.sxc);
+    case 5: return at<uint8_t>(saved, pl.hc);
+    case 6: return at<uint8_t>(saved, pl.shc);
     default: return nullptr;
   }
 }

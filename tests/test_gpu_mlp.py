@@ -11,8 +11,9 @@ import pytest
 import torch
 
 import synthetic
-from gpu_helpers import assert_rel_close, assert_rms_close, np_, require_gpu
-from oracle import moe
+from gpu_helpers import assert_rel_close, assert_rms_close, codes_equal_up_to_zero_sign, mma_to_canonical, np_, \
+    require_gpu
+from oracle import moe, mx
 
 pytestmark = pytest.mark.gpu
 
@@ -39,12 +40,21 @@ def run_gpu(m, shape, inp):
     y, split = layer.forward(x, ids, probs, wgu, wd, save_for_backward=True)
     gu = layer.gu_view().clone()
     poff = layer.padded_offsets().clone()
+    mcap = layer.padded_rows_capacity()
+    views = {}
+    for name, which, rows in (("xc", 3, H), ("sxc", 4, H), ("hc", 5, I), ("shc", 6, I)):
+        ptr = m.mxg_mlp_saved_view(layer.saved, T, H, I, E, k, which)
+        off = ptr - layer.saved.data_ptr()
+        n = rows * mcap if name in ("xc", "hc") else rows * mcap // 32
+        views[name] = layer.saved[off:off + n].clone()
     dx, dwgu, dwd, dprobs = layer.backward(dy)
     torch.cuda.synchronize()
     out = {"ids": ids, "probs": probs, "y": y, "split": split, "gu": gu, "poff": poff, "dx": dx,
            "dwgu": dwgu, "dwd": dwd, "dprobs": dprobs}
     out = {n: np_(v) for n, v in out.items()}
     out["status"] = layer.status()
+    out["mcap"] = mcap
+    out.update({n: v.cpu().numpy() for n, v in views.items()})
     return out
 
 
@@ -81,4 +91,32 @@ def test_mlp_fwd_bwd_matches_oracle(name):
     report["dw_down"] = assert_rms_close(got["dwd"], g["dw_down"], 2e-2, "dW_down")
     for e in np.nonzero(perm["split_sizes"] == 0)[0]:
         assert not got["dwgu"][e].any() and not got["dwd"][e].any()
-    print(name, {n: (round(a, 5), round(b, 5)) for n, (a, b) in report.items()})
+
+    # token-column-wise MXFP8 kept for the weight gradients: x's (an input) bit
+    # for bit; h's (re-quantised from the GEMM's fp32 h) as the fraction of
+    # codes and scales that differ from the oracle's quantisation of its fp64 h
+    mcap = got["mcap"]
+    xc, hc = got["xc"].reshape(H, mcap), got["hc"].reshape(I, mcap)
+    sxc = mma_to_canonical(torch.from_numpy(got["sxc"]), H, mcap // 32)
+    shc = mma_to_canonical(torch.from_numpy(got["shc"]), I, mcap // 32)
+    diff_codes = diff_scales = n_codes = n_scales = 0
+    for e in range(E):
+        a, b = perm["offsets"][e], perm["offsets"][e + 1]
+        if b == a:
+            continue
+        p0 = poff[e]
+        codes, scales = mx.quantize_group_columns(ctx["x_perm"][a:b])
+        w = codes.shape[1]
+        d, z = codes_equal_up_to_zero_sign(xc[:, p0:p0 + w], codes)
+        assert d == 0, f"x column codes, expert {e}: {d} differ"
+        assert np.array_equal(sxc[:, p0 // 32:(p0 + w) // 32], scales), f"x column scales, expert {e}"
+        codes, scales = mx.quantize_group_columns(ctx["h"][a:b])
+        d, z = codes_equal_up_to_zero_sign(hc[:, p0:p0 + w], codes)
+        diff_codes += d
+        n_codes += codes.size
+        diff_scales += int((shc[:, p0 // 32:(p0 + w) // 32] != scales).sum())
+        n_scales += scales.size
+    frac = diff_codes / n_codes
+    report["h column codes differing"] = (frac, diff_scales / n_scales)
+    assert frac < 1e-3 and diff_scales / n_scales < 1e-3, (frac, diff_scales / n_scales)
+    print(name, {n: (round(a, 6), round(b, 6)) for n, (a, b) in report.items()})
