@@ -404,6 +404,12 @@ const void* mxg_mlp_fp8_saved_view(const void* saved, int T, int H, int I, int E
  * codes (uint8 [H][m_cap]) / scales (tensor-core layout, H rows x m_cap/32
  * blocks), 5 / 6 = the same for h (I rows). */
 const void* mxg_mlp_saved_view(const void* saved, int T, int H, int I, int E, int k, int which);
+/* Debug views into the MXFP8 `workspace` after a backward (device pointers;
+ * NULL on bad arguments): the dSwiGLU epilogue's re-quantised dGU, 0 / 1 =
+ * row-wise codes (uint8 [m_cap][2I]) / scales (tensor-core layout, m_cap rows
+ * x 2I/32 blocks), 2 / 3 = token-column-wise codes (uint8 [2I][m_cap]) /
+ * scales (2I rows x m_cap/32 blocks).  Valid until the workspace is reused. */
+const void* mxg_mlp_workspace_view(const void* workspace, int T, int H, int I, int E, int k, int which);
 
 #ifdef __cplusplus
 }

@@ -35,6 +35,7 @@ EXPORTS = [
     "mxg_mlp_weight_cache_bytes", "mxg_mlp_quantize_weights", "mxg_mlp_saved_bytes_cached",
     "mxg_mlp_fp8_saved_bytes", "mxg_mlp_fp8_workspace_bytes", "mxg_grouped_mlp_fp8_fwd", "mxg_grouped_mlp_fp8_bwd",
     "mxg_grouped_mlp_fp8_fwd_stage", "mxg_grouped_mlp_fp8_bwd_stage", "mxg_mlp_fp8_saved_view",
+    "mxg_mlp_workspace_view",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -121,6 +122,7 @@ def lib() -> ctypes.CDLL:
         "mxg_grouped_mlp_fp8_fwd_stage": (I32, [ctypes.POINTER(MlpFwdArgs), I32, P]),
         "mxg_grouped_mlp_fp8_bwd_stage": (I32, [ctypes.POINTER(MlpBwdArgs), I32, P]),
         "mxg_mlp_fp8_saved_view": (P, [P, I32, I32, I32, I32, I32, I32]),
+        "mxg_mlp_workspace_view": (P, [P, I32, I32, I32, I32, I32, I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -312,6 +314,10 @@ def mxg_mlp_fp8_workspace_bytes(T, H, I, E, k) -> int:
 
 def mxg_mlp_saved_view(saved: torch.Tensor, T, H, I, E, k, which: int) -> int:
     return int(lib().mxg_mlp_saved_view(_ptr(saved), T, H, I, E, k, which) or 0)
+
+
+def mxg_mlp_workspace_view(workspace: torch.Tensor, T, H, I, E, k, which: int) -> int:
+    return int(lib().mxg_mlp_workspace_view(_ptr(workspace), T, H, I, E, k, which) or 0)
 
 
 class WeightCache:

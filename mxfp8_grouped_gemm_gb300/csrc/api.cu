@@ -427,6 +427,18 @@ const void* mxg_mlp_saved_view(const void* saved, int T, int H, int I, int E, in
   }
 }
 
+const void* mxg_mlp_workspace_view(const void* workspace, int T, int H, int I, int E, int k, int which) {
+  if (!workspace || !mlp_shape_ok(T, H, I, E, k)) return nullptr;
+  const Plan pl(T, H, I, E, k);
+  switch (which) {
+    case 0: return at<uint8_t>(workspace, pl.dguq);
+    case 1: return at<uint8_t>(workspace, pl.sdguq);
+    case 2: return at<uint8_t>(workspace, pl.dguc);
+    case 3: return at<uint8_t>(workspace, pl.sdguc);
+    default: return nullptr;
+  }
+}
+
 static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   if (!A) return MXG_ERR_ARG;
   const int T = A->T, H = A->H, I = A->I, E = A->E, k = A->k;
