@@ -347,6 +347,13 @@ size_t mxg_mlp_weight_cache_bytes(int H, int I, int E);
 int mxg_mlp_quantize_weights(const uint16_t* w_gate_up, const uint16_t* w_down, int H, int I, int E, void* cache,
                              size_t cache_bytes, void* stream);
 size_t mxg_mlp_saved_bytes_cached(int T, int H, int I, int E, int k);
+/* Debug view into a weight cache (device pointer; NULL on bad arguments) for
+ * the tests: 0 / 1 = W_gate_up along H: codes uint8 [E*2I][H] / scales
+ * (tensor-core layout, E*2I rows x H/32 blocks); 2 / 3 = W_down along I:
+ * [E*H][I] / (E*H rows x I/32); 4 / 5 = W_gate_up along 2I, transposed:
+ * [E*H][2I] / (E*H rows x 2I/32); 6 / 7 = W_down along H, transposed:
+ * [E*I][H] / (E*I rows x H/32). */
+const void* mxg_mlp_weight_cache_view(const void* cache, int H, int I, int E, int which);
 
 /* ----------------------------------------------------------------------------
  * The same grouped expert MLP in BF16: bf16 operands on the tensor cores with

@@ -35,7 +35,7 @@ EXPORTS = [
     "mxg_mlp_weight_cache_bytes", "mxg_mlp_quantize_weights", "mxg_mlp_saved_bytes_cached",
     "mxg_mlp_fp8_saved_bytes", "mxg_mlp_fp8_workspace_bytes", "mxg_grouped_mlp_fp8_fwd", "mxg_grouped_mlp_fp8_bwd",
     "mxg_grouped_mlp_fp8_fwd_stage", "mxg_grouped_mlp_fp8_bwd_stage", "mxg_mlp_fp8_saved_view",
-    "mxg_mlp_workspace_view",
+    "mxg_mlp_workspace_view", "mxg_mlp_weight_cache_view",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -123,6 +123,7 @@ def lib() -> ctypes.CDLL:
         "mxg_grouped_mlp_fp8_bwd_stage": (I32, [ctypes.POINTER(MlpBwdArgs), I32, P]),
         "mxg_mlp_fp8_saved_view": (P, [P, I32, I32, I32, I32, I32, I32]),
         "mxg_mlp_workspace_view": (P, [P, I32, I32, I32, I32, I32, I32]),
+        "mxg_mlp_weight_cache_view": (P, [P, I32, I32, I32, I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)

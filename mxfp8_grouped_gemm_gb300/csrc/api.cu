@@ -397,6 +397,22 @@ size_t mxg_mlp_weight_cache_bytes(int H, int I, int E) {
   return static_cast<size_t>(WPlan(H, I, E).bytes);
 }
 
+const void* mxg_mlp_weight_cache_view(const void* cache, int H, int I, int E, int which) {
+  if (!cache || !mlp_shape_ok(1, H, I, E, 1)) return nullptr;
+  const WPlan wp(H, I, E);
+  switch (which) {
+    case 0: return at<uint8_t>(cache, wp.wgu);
+    case 1: return at<uint8_t>(cache, wp.swgu);
+    case 2: return at<uint8_t>(cache, wp.wd);
+    case 3: return at<uint8_t>(cache, wp.swd);
+    case 4: return at<uint8_t>(cache, wp.wguT);
+    case 5: return at<uint8_t>(cache, wp.swguT);
+    case 6: return at<uint8_t>(cache, wp.wdT);
+    case 7: return at<uint8_t>(cache, wp.swdT);
+    default: return nullptr;
+  }
+}
+
 int mxg_mlp_quantize_weights(const uint16_t* w_gate_up, const uint16_t* w_down, int H, int I, int E, void* cache,
                              size_t cache_bytes, void* stream) {
   if (!w_gate_up || !w_down || !cache) return MXG_ERR_ARG;

@@ -106,3 +106,33 @@ def test_main_grad_accumulates_fp32(name):
         for e in np.nonzero(split == 0)[0]:
             assert np.array_equal(a[e], s0[e]), f"{nm}: expert {e} without tokens changed"
         assert_rms_close(inc / 2, oracle_dw, 2e-2, nm)
+
+
+def test_weight_cache_holds_the_oracles_codes():
+    """The cache's four MXFP8 weight tensors, bit for bit against the MX
+    quantiser oracle (the inputs are the same bf16 values): W_gate_up along H
+    and along 2I (transposed), W_down along I and along H (transposed)."""
+    from gpu_helpers import mma_to_canonical
+    from oracle import mx
+    m = require_gpu()
+    H, I, E = 256, 384, 3
+    inp = synthetic.make_case(64, H, I, E, 2, seed=9)
+    wgu, wd = inp["w_gate_up"], inp["w_down"]
+    cache = m.mxg_mlp_quantize_weights(wgu.cuda(), wd.cuda())
+    torch.cuda.synchronize()
+    base = cache.buffer.data_ptr()
+
+    def view(which, rows, cols, codes):
+        off = m.lib().mxg_mlp_weight_cache_view(base, H, I, E, which) - base
+        n = rows * cols if codes else rows * cols // 32
+        t = cache.buffer[off:off + n]
+        return t.cpu().numpy().reshape(rows, cols) if codes else mma_to_canonical(t, rows, cols // 32)
+
+    W_gu, W_d = wgu.double().numpy(), wd.double().numpy()
+    for which, rows, cols, ref in ((0, E * 2 * I, H, [W_gu[e] for e in range(E)]),
+                                   (2, E * H, I, [W_d[e] for e in range(E)]),
+                                   (4, E * H, 2 * I, [W_gu[e].T for e in range(E)]),
+                                   (6, E * I, H, [W_d[e].T for e in range(E)])):
+        codes, scales = mx.quantize_blocks(np.concatenate(ref, axis=0))
+        assert np.array_equal(view(which, rows, cols, True), codes), which
+        assert np.array_equal(view(which + 1, rows, cols, False), scales), which + 1
