@@ -303,7 +303,7 @@ enum {
   MXG_FWD_QUANT_X = 2,       /* gather x to the padded layout + quantise               */
   MXG_FWD_GATE_UP = 3,       /* gate-up GEMM + ScaledSwiGLU + requantise               */
   MXG_FWD_DOWN = 4,          /* down GEMM                                              */
-  MXG_FWD_COMBINE = 5,       /* y[t] = sum_j Y[row(t, j)]                              */
+  MXG_FWD_COMBINE = 5,       /* y[t] = sum_j Y[row(t, j)] (MXFP8: fused into DOWN, empty) */
   MXG_FWD_NUM_STAGES = 6
 };
 enum {
@@ -312,7 +312,7 @@ enum {
   MXG_BWD_WGRAD_DOWN = 2,    /* dW_down GEMM (token-grouped)                           */
   MXG_BWD_DGRAD_GATE_UP = 3, /* dX GEMM                                                */
   MXG_BWD_WGRAD_GATE_UP = 4, /* dW_gate_up GEMM (token-grouped)                        */
-  MXG_BWD_COMBINE_DX = 5,    /* dx[t] = sum_j dX[row(t, j)]                            */
+  MXG_BWD_COMBINE_DX = 5,    /* dx[t] = sum_j dX[row(t, j)] (MXFP8: fused into DGRAD_GATE_UP) */
   MXG_BWD_DPROBS = 6,        /* dprobs[t, j] from the per-tile partials                */
   MXG_BWD_NUM_STAGES = 7
 };
@@ -411,11 +411,14 @@ const void* mxg_mlp_fp8_saved_view(const void* saved, int T, int H, int I, int E
  * codes (uint8 [H][m_cap]) / scales (tensor-core layout, H rows x m_cap/32
  * blocks), 5 / 6 = the same for h (I rows). */
 const void* mxg_mlp_saved_view(const void* saved, int T, int H, int I, int E, int k, int which);
-/* Debug views into the MXFP8 `workspace` after a backward (device pointers;
- * NULL on bad arguments): the dSwiGLU epilogue's re-quantised dGU, 0 / 1 =
+/* Debug views into the MXFP8 `workspace` (device pointers; NULL on bad
+ * arguments): after a backward, the dSwiGLU epilogue's re-quantised dGU, 0 / 1 =
  * row-wise codes (uint8 [m_cap][2I]) / scales (tensor-core layout, m_cap rows
  * x 2I/32 blocks), 2 / 3 = token-column-wise codes (uint8 [2I][m_cap]) /
- * scales (2I rows x m_cap/32 blocks).  Valid until the workspace is reused. */
+ * scales (2I rows x m_cap/32 blocks); 4 = the down GEMM's rows before the
+ * combine (bf16 [m_cap][H], after a forward), 5 = the dgrad-gate-up GEMM's rows
+ * before the combine (bf16 [m_cap][H], after a backward).  Valid until the
+ * workspace is reused. */
 const void* mxg_mlp_workspace_view(const void* workspace, int T, int H, int I, int E, int k, int which);
 
 #ifdef __cplusplus

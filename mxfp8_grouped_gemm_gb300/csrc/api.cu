@@ -37,9 +37,9 @@ struct Plan {
   int64_t poff, prow_src, prow_of_src, probs_perm, gu, xc, sxc, hc, shc, wguT, swguT, wdT, swdT, saved_bytes,
       saved_cached_bytes;
   // forward scratch
-  int64_t counts, bases, offsets, xq, sxq, hq, shq, wgu, swgu, wd, swd, yperm, fwd_bytes;
+  int64_t counts, bases, offsets, xq, sxq, hq, shq, wgu, swgu, wd, swd, yperm, cmb_cnt, fwd_bytes;
   // backward scratch
-  int64_t dyq, sdyq, dyc, sdyc, dguq, sdguq, dguc, sdguc, dxperm, dp, bwd_bytes;
+  int64_t dyq, sdyq, dyc, sdyc, dguq, sdguq, dguc, sdguc, dxperm, dp, cmb_cnt_b, bwd_bytes;
   int64_t dp_ld;
 
   Plan(int64_t T_, int64_t H_, int64_t I_, int64_t E_, int64_t k_) : T(T_), H(H_), I(I_), E(E_), k(k_) {
@@ -76,6 +76,7 @@ struct Plan {
     wd = f.take(E * H * I);
     swd = f.take(E * H * I / 32);
     yperm = f.take(2 * Rc * H);
+    cmb_cnt = f.take(4 * T * (H / 128) * 2);
     fwd_bytes = f.off;
 
     Carver b;
@@ -90,6 +91,7 @@ struct Plan {
     sdguc = b.take(2 * I * Rc / 32);
     dxperm = b.take(2 * Rc * H);
     dp = b.take(4 * Rc * dp_ld);
+    cmb_cnt_b = b.take(4 * T * (H / 128) * 2);
     bwd_bytes = b.off;
   }
   int64_t ws_bytes() const { return fwd_bytes > bwd_bytes ? fwd_bytes : bwd_bytes; }
@@ -451,6 +453,8 @@ const void* mxg_mlp_workspace_view(const void* workspace, int T, int H, int I, i
     case 1: return at<uint8_t>(workspace, pl.sdguq);
     case 2: return at<uint8_t>(workspace, pl.dguc);
     case 3: return at<uint8_t>(workspace, pl.sdguc);
+    case 4: return at<uint8_t>(workspace, pl.yperm);
+    case 5: return at<uint8_t>(workspace, pl.dxperm);
     default: return nullptr;
   }
 }
@@ -599,14 +603,19 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   d.b_rows_per_expert = H;
   d.d = at<uint16_t>(ws, pl.yperm);
   d.ldd = H;
+  // F7 fused: the thread that stores the last of a token's k rows sums them into y
+  MXG_TRY(cudaMemsetAsync(at<int32_t>(ws, pl.cmb_cnt), 0, 4 * pl.T * (H / 128) * 2, s));
+  d.cmb_out = A->y;
+  d.cmb_prow_src = at<int32_t>(sv, pl.prow_src);
+  d.cmb_prow_of_src = at<int32_t>(sv, pl.prow_of_src);
+  d.cmb_count = at<int32_t>(ws, pl.cmb_cnt);
+  d.cmb_k = k;
   d.status = st;
   d.tiles_upper = d.pair ? (pl.Rc / 256) * (H / 256) : (pl.Rc / 128) * (H / gemm_pick_bn(EPI_BF16, H));
   MXG_TRY(launch_gemm(d, s));
   }
 
-  // F7: combine
-  if (run(MXG_FWD_COMBINE))
-    MXG_TRY(launch_combine(at<uint16_t>(ws, pl.yperm), at<int32_t>(sv, pl.prow_of_src), T, k, H, A->y, s));
+  // F7: fused into the down GEMM above (the combine stage has nothing left to do)
   return MXG_OK;
 }
 
@@ -757,6 +766,13 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   x.b_rows_per_expert = H;
   x.d = at<uint16_t>(ws, pl.dxperm);
   x.ldd = H;
+  // B6 fused: dx[t] summed by the thread that stores the last of the token's rows
+  MXG_TRY(cudaMemsetAsync(at<int32_t>(ws, pl.cmb_cnt_b), 0, 4 * pl.T * (H / 128) * 2, s));
+  x.cmb_out = A->dx;
+  x.cmb_prow_src = at<int32_t>(sv, pl.prow_src);
+  x.cmb_prow_of_src = at<int32_t>(sv, pl.prow_of_src);
+  x.cmb_count = at<int32_t>(ws, pl.cmb_cnt_b);
+  x.cmb_k = k;
   x.status = st;
   x.tiles_upper = x.pair ? (pl.Rc / 256) * (H / 256) : (pl.Rc / 128) * (H / gemm_pick_bn(EPI_BF16, H));
   MXG_TRY(launch_gemm(x, s));
@@ -790,8 +806,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
 
   // B6, B7: combine dx, reduce d(prob)
   const int32_t* prow_of_src = at<int32_t>(sv, pl.prow_of_src);
-  if (run(MXG_BWD_COMBINE_DX))
-    MXG_TRY(launch_combine(at<uint16_t>(ws, pl.dxperm), prow_of_src, T, k, H, A->dx, s));
+  // B6: fused into the dgrad-gate-up GEMM above
   if (run(MXG_BWD_DPROBS))
     MXG_TRY(launch_dprob(at<float>(ws, pl.dp), static_cast<int>(pl.dp_ld), prow_of_src, static_cast<int>(pl.R),
                          A->dprobs, s));

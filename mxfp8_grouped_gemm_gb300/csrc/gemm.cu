@@ -261,6 +261,56 @@ __device__ __forceinline__ float tile_scale(const GemmArgs& P, const TileCoord& 
   return 1.f;
 }
 
+// Combine fused into a row-grouped bf16 epilogue.  The thread has just
+// stored its half row (COLS columns) of padded row m0 + row, which is slot j of
+// token t.  It counts its segment in for (t, column tile, half); the thread
+// that brings the count to k sums the token's k segments in slot order (fp32,
+// from bf16: the same arithmetic as the combine kernel), writes y[t]'s segment
+// and resets the counter.  Each writer fences its stores before its atomic,
+// and the summing thread fences after it and reads through L2, so it sees the
+// other CTAs' segments.  No thread waits on another.
+template <int BN, int COLS>
+__device__ __forceinline__ void fused_combine(const GemmArgs& P, const TileCoord& tc, int row, int hf,
+                                              const uint32_t (&packed)[COLS / 2]) {
+  const int prow = tc.m0 + row;
+  const int f = P.cmb_prow_src[prow];
+  if (f < 0) return;                              // padding row
+  const int k = P.cmb_k;
+  const int t = f / k;
+  int32_t* cnt = P.cmb_count + (static_cast<int64_t>(t) * (P.N / BN) + tc.nt) * 2 + hf;
+  __threadfence();
+  if (atomicAdd(cnt, 1) != k - 1) return;
+  __threadfence();
+  *cnt = 0;
+  const int64_t c0 = static_cast<int64_t>(tc.nt) * BN + hf * COLS;
+  const int32_t* slots = P.cmb_prow_of_src + static_cast<int64_t>(t) * k;
+#pragma unroll
+  for (int jc = 0; jc < COLS / 16; ++jc) {
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int pr = slots[j];
+      uint32_t w[8];
+      if (pr == prow) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = packed[8 * jc + i];
+      } else {
+        ld_global_cg_v8(P.d + static_cast<int64_t>(pr) * P.ldd + c0 + 16 * jc, w);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        acc[2 * i] += u2f(w[i] << 16);
+        acc[2 * i + 1] += u2f(w[i] & 0xffff0000u);
+      }
+    }
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+    st_global_v8(P.cmb_out + static_cast<int64_t>(t) * P.N + c0 + 16 * jc, o);
+  }
+}
+
 template <int BN, bool KG, int OPK>
 __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int row, int hf,
                                          const AccRelease& tempty, int lane) {
@@ -290,6 +340,8 @@ __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc,
                       : P.d + static_cast<int64_t>(tc.m0 + row) * P.ldd + tc.nt * BN + hf * COLS;
 #pragma unroll
   for (int j = 0; j < COLS / 16; ++j) st_global_v8(drow + 16 * j, packed + 8 * j);
+  if constexpr (!KG)
+    if (P.cmb_out != nullptr) fused_combine<BN, COLS>(P, tc, row, hf, packed);
 }
 
 // Weight-gradient tile added into an fp32 gradient buffer (main_grad): the

@@ -142,6 +142,15 @@ struct GemmArgs {
   const float* amax_b;
   float* amax_out;
   float* dacc;                // EPI_ACC_F32 (token-grouped): fp32 [E][M][N] that the tile is added into
+  // Combine fused into a row-grouped bf16 epilogue: out[t] = sum over the k
+  // rows of token t (slot order) of D, written by whichever thread stores the
+  // last of them (counters [T][N/BN][2], zero before the launch; they are left
+  // at zero again).  Null: no combine.
+  uint16_t* cmb_out;          // [T][N] bf16
+  const int32_t* cmb_prow_src;     // [M] padded row -> flat index t*k + j (-1: padding)
+  const int32_t* cmb_prow_of_src;  // [T*k] flat index -> padded row
+  int32_t* cmb_count;
+  int32_t cmb_k;
   int64_t tiles_upper;        // host bound on the number of tiles (grid sizing)
   uint64_t wait_limit_ns;     // bound on every wait inside the kernel (0: default)
   int32_t debug_stall;        // test hook: the producer issues no copies

@@ -154,6 +154,14 @@ __device__ __forceinline__ void ld_global_v8(const void* src, uint32_t* w) {
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
+// 32-byte global load served from L2 (not L1): sees data other CTAs wrote
+// before a fence and an atomic that this thread has observed.
+__device__ __forceinline__ void ld_global_cg_v8(const void* src, uint32_t* w) {
+  asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "l"(src)
+               : "memory");
+}
 // Plain arrive on this CTA's mbarrier, given as a shared-window address.
 __device__ __forceinline__ void mbar_arrive_u32(uint32_t saddr) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr) : "memory");

@@ -38,6 +38,9 @@ def run_gpu(m, shape, inp):
     wgu, wd, dy = inp["w_gate_up"].to(dev), inp["w_down"].to(dev), inp["dy"].to(dev)
     ids, probs = layer.route(logits)
     y, split = layer.forward(x, ids, probs, wgu, wd, save_for_backward=True)
+    mcap0 = layer.padded_rows_capacity()
+    off = m.mxg_mlp_workspace_view(layer.workspace, T, H, I, E, k, 4) - layer.workspace.data_ptr()
+    yperm = layer.workspace[off:off + 2 * mcap0 * H].clone()
     gu = layer.gu_view().clone()
     poff = layer.padded_offsets().clone()
     mcap = layer.padded_rows_capacity()
@@ -49,6 +52,8 @@ def run_gpu(m, shape, inp):
         views[name] = layer.saved[off:off + n].clone()
     dx, dwgu, dwd, dprobs = layer.backward(dy)
     torch.cuda.synchronize()
+    off = m.mxg_mlp_workspace_view(layer.workspace, T, H, I, E, k, 5) - layer.workspace.data_ptr()
+    dxperm = layer.workspace[off:off + 2 * mcap0 * H].clone()
     for name, which, n in (("dguq", 0, mcap * 2 * I), ("sdguq", 1, mcap * 2 * I // 32), ("dguc", 2, 2 * I * mcap),
                            ("sdguc", 3, 2 * I * mcap // 32)):
         off = m.mxg_mlp_workspace_view(layer.workspace, T, H, I, E, k, which) - layer.workspace.data_ptr()
@@ -58,6 +63,21 @@ def run_gpu(m, shape, inp):
     out = {n: np_(v) for n, v in out.items()}
     out["status"] = layer.status()
     out["mcap"] = mcap
+    # the combine is fused into the down / dgrad-gate-up epilogues: recompute it
+    # from their rows with the combine's arithmetic (fp32 sum in slot order, one
+    # bf16 rounding) for a bit-exact comparison
+    rows = layer.padded_rows_capacity()
+    poff_np = out["poff"]
+    perm = moe.permute(out["ids"].astype(np.int64), E, pad=m.mxg_mlp_group_align())
+    e_of_row = np.repeat(np.arange(E), perm["split_sizes"])
+    prow_of_flat = np.empty(T * k, dtype=np.int64)
+    prow_of_flat[perm["src_of_row"]] = poff_np[e_of_row] + (np.arange(T * k) - perm["offsets"][e_of_row])
+    for name, rows_t in (("y_fused_ref", yperm), ("dx_fused_ref", dxperm)):
+        Y = rows_t.view(torch.bfloat16).float().cpu().numpy().reshape(rows, H)
+        acc = np.zeros((T, H), dtype=np.float32)
+        for j in range(k):
+            acc += Y[prow_of_flat.reshape(T, k)[:, j]]
+        out[name] = torch.from_numpy(acc).to(torch.bfloat16).double().numpy()
     out.update({n: v.cpu().numpy() for n, v in views.items()})
     return out
 
@@ -87,6 +107,8 @@ def test_mlp_fwd_bwd_matches_oracle(name):
     prow = poff[e_of_row] + (np.arange(T * k) - perm["offsets"][e_of_row])
     assert_rel_close(got["gu"][prow], ctx["gu"], tol=1e-2, floor=1.0, name="gate-up")
 
+    assert np.array_equal(got["y"], got["y_fused_ref"]), "fused combine (forward) differs from the combine arithmetic"
+    assert np.array_equal(got["dx"], got["dx_fused_ref"]), "fused combine (backward) differs from the combine arithmetic"
     report = {}
     report["y"] = assert_rms_close(got["y"], ctx["y"], 2e-2, "y")
     report["dx"] = assert_rms_close(got["dx"], g["dx"], 2e-2, "dx")
