@@ -74,8 +74,10 @@ struct Cfg {
   static constexpr int kStageBytes = (kTx + 1023) / 1024 * 1024;
   // dSwiGLU: BN = 256 stages the tile's dH as bf16 rows (padded to 264) so the
   // accumulator is released before the epilogue math; BN = 128 keeps a 32 x 33
-  // fp32 transpose tile per epilogue warp for the column-wise quantiser
-  static constexpr int kXposeBytes = EPI == 2 ? (BN == 256 ? 128 * (256 + 8) * 2 : 8 * 32 * 33 * 4) : 0;
+  // fp32 transpose tile per epilogue warp for the column-wise quantiser.
+  // MXFP8 gate-up: a 32 x 20-word scratch per epilogue warp for the column-wise
+  // quantiser (20 KB, what the six-stage ring leaves free)
+  static constexpr int kXposeBytes = EPI == 2 ? (BN == 256 ? 128 * (256 + 8) * 2 : 8 * 32 * 33 * 4) : (EPI == 1 && OPK == OPK_MX ? 8 * 32 * 20 * 4 : 0);
   static constexpr int kCtrlBytes = 2048;
   static constexpr int kStages = (232448 - 1024 - kCtrlBytes - kXposeBytes) / kStageBytes > 8
                                      ? 8
@@ -145,23 +147,10 @@ __device__ __forceinline__ uint32_t row_quant32(const float (&h)[32], uint8_t* d
   return sb;
 }
 
-// Column-wise MX across the warp: lane l holds row tok0+l; for each of the 32
-// columns col0+i the warp's 32 rows form one block (tok0 is 32-aligned and
-// inside one expert group).  Codes go to qc[(col0+i)*ld + tok0 + lane].
-__device__ __forceinline__ void col_quant32(const float (&h)[32], uint8_t* qc, uint8_t* sc, int64_t ld,
-                                            int64_t sc_rows, int64_t col0, int64_t tok0, int lane) {
-  uint32_t my_sb = 0;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, f2u(h[i]) & 0x7fffffffu);
-    const uint32_t sb = mx_scale_byte(m);
-    qc[(col0 + i) * ld + tok0 + lane] = static_cast<uint8_t>(cvt_e4m3x2(h[i] * mx_inv_scale(sb), 0.f) & 0xffu);
-    if (lane == i) my_sb = sb;
-  }
-  sc[sf_mma_offset(col0 + lane, tok0 >> 5, sc_rows)] = static_cast<uint8_t>(my_sb);
-}
-
-// The same column-wise MX through a 32 x 33 fp32 shared tile: the warp writes
+// Column-wise MX of the warp's 32 x 32 block (lane l holds row tok0 + l; for
+// each column col0 + i the 32 rows form one block, tok0 32-aligned and inside
+// one expert group; codes go to qc[(col0 + i) * ld + tok0 + row]) through a
+// 32 x 33 fp32 shared tile: the warp writes
 // its 32 rows, each lane then reads one column (its 32 tokens), quantises it in
 // registers and writes the 32 codes as one contiguous run of the transposed
 // output.  Bank-conflict free in both directions.
@@ -189,6 +178,55 @@ __device__ __forceinline__ void col_quant32_xpose(const float (&h)[32], float* x
   d[0] = make_uint4(w[0], w[1], w[2], w[3]);
   d[1] = make_uint4(w[4], w[5], w[6], w[7]);
   sc[sf_mma_offset(col0 + lane, tok0 >> 5, sc_rows)] = static_cast<uint8_t>(sb);
+}
+
+// The same column-wise MX through the warp's own 32 x 16 fp32 scratch: lane
+// l's 64-byte slot is at slot + l * pitch words (16-byte aligned; pitch % 8 ==
+// 4, so rows 12 or 20 apart start 16 banks apart, and eight consecutive rows'
+// slots start in distinct groups of four banks).  Two passes of 16 columns:
+// every lane writes its row's 16 values, then reads one column (cl = lane % 16)
+// for half of the block's rows, lanes 0-15 rows 0-15 and lanes 16-31 rows
+// 16-31 taken in the order 16 + (j ^ 4), so that at each read the two
+// half-warps cover the 32 banks once.  The halves' maxima meet in one shuffle
+// and each lane stores its 16 codes as one 16-byte run of the transposed
+// output (lanes l and l + 16 fill one 32-byte sector).
+__device__ __forceinline__ void col_quant32_slots(const float (&h)[32], float* slot, int pitch, uint8_t* qc,
+                                                  uint8_t* sc, int64_t ld, int64_t sc_rows, int64_t col0,
+                                                  int64_t tok0, int lane) {
+  const int g = lane >> 4, cl = lane & 15;
+  float4* mine = reinterpret_cast<float4*>(slot + lane * pitch);
+  // rows j ^ (4g) of this half: j with bit 2 clear sit 4g rows below j, the others 4g rows above
+  const float* lo = slot + (16 * g + 4 * g) * pitch + cl;
+  const float* hi = slot + (16 * g - 4 * g) * pitch + cl;
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    __syncwarp();  // the previous pass's readers are done with the slots
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      mine[k] = make_float4(h[16 * pass + 4 * k], h[16 * pass + 4 * k + 1], h[16 * pass + 4 * k + 2],
+                            h[16 * pass + 4 * k + 3]);
+    __syncwarp();
+    float v[16];
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      v[j] = (j & 4) ? hi[j * pitch] : lo[j * pitch];
+      m = fmaxf(m, fabsf(v[j]));
+    }
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+    const uint32_t sb = mx_scale_byte(f2u(m));
+    const float inv = mx_inv_scale(sb);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = cvt_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
+             (cvt_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+    // v[j] holds row j ^ (4g): for g = 1 the words of rows 0-3 / 4-7 (and 8-11 / 12-15) trade places
+    const uint4 out = g ? make_uint4(w[1], w[0], w[3], w[2]) : make_uint4(w[0], w[1], w[2], w[3]);
+    const int64_t col = col0 + 16 * pass + cl;
+    *reinterpret_cast<uint4*>(qc + col * ld + tok0 + 16 * g) = out;
+    if (g == 0) sc[sf_mma_offset(col, tok0 >> 5, sc_rows)] = static_cast<uint8_t>(sb);
+  }
 }
 
 // bf16 outputs of the fused epilogues (BF16 and FP8 paths): the transposed
@@ -376,7 +414,7 @@ __device__ __forceinline__ void epi_acc_f32(const GemmArgs& P, const TileCoord& 
 // h in fp32 and quantises and stores while the next tile's MMAs run.
 template <int BN, int OPK>
 __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
-                                           int hf, const AccRelease& tempty) {
+                                           int hf, const AccRelease& tempty, float* slots) {
   constexpr int HC = BN / 2;          // h columns per tile
   constexpr int CH = HC / 64;         // 32-column chunks per thread
   const int64_t tok0 = tc.m0 + q * 32;
@@ -432,7 +470,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& t
     } else {
       const uint32_t sb = row_quant32(h, P.q_out + r * P.q_out_ld + col);
       P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-      if (P.qc_out != nullptr) col_quant32(h, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
+      if (P.qc_out != nullptr) col_quant32_slots(h, slots, 20, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
     }
   }
   if constexpr (OPK == OPK_F8) warp_amax_to(P.amax_out + tc.e, hmax, lane);
@@ -546,12 +584,14 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
         col_store_bf16(u, P.y_col, P.y_col_ld, I + col, tok0, lane);
       }
     } else {
+      // this chunk's dH slots (the warp's 32 rows x 64 bytes, already read) serve as scratch
+      float* slot = reinterpret_cast<float*>(stage_base + q * 32 * STRIDE + hf * COLS + c * 32);
       uint32_t sb = row_quant32(dg, P.q_out + r * P.q_out_ld + col);
       P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-      col_quant32(dg, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
+      col_quant32_slots(dg, slot, STRIDE / 2, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
       sb = row_quant32(u, P.q_out + r * P.q_out_ld + I + col);
       P.s_out[sf_mma_offset(r, (I + col) >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-      col_quant32(u, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
+      col_quant32_slots(u, slot, STRIDE / 2, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
     }
   }
   P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp;
@@ -931,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       rel.bar = rel.peer ? map_to_rank(smem_u32(&tempty[acc]), 0) : smem_u32(&tempty[acc]);
       rel.land = rel.peer ? map_to_rank(smem_u32(&landing[warp - 4]), 0) : 0u;
       if constexpr (EPI == EPI_SWIGLU) {
-        epi_swiglu<BN, OPK>(P, tc, tb, q, lane, hf, rel);
+        epi_swiglu<BN, OPK>(P, tc, tb, q, lane, hf, rel, xpose + (warp - 4) * 32 * 20);
       } else if constexpr (EPI == EPI_DSWIGLU) {
         if constexpr (BN == 256) epi_dswiglu_staged<OPK>(P, tc, tb, q, lane, hf, rel, reinterpret_cast<uint16_t*>(xpose));
         else epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
