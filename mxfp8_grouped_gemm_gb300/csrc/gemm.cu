@@ -133,10 +133,10 @@ __device__ __forceinline__ void unpack_bf16_32(const uint4* src, float (&v)[32])
 // Row-wise MX of one thread's 32 consecutive values: codes to dst (32 bytes),
 // scale byte returned.
 __device__ __forceinline__ uint32_t row_quant32(const float (&h)[32], uint8_t* dst) {
-  uint32_t amax = 0;
+  float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = max(amax, f2u(h[i]) & 0x7fffffffu);
-  const uint32_t sb = mx_scale_byte(amax);
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+  const uint32_t sb = mx_scale_byte(f2u(amax));
   const float inv = mx_inv_scale(sb);
   float v[32];
 #pragma unroll
@@ -571,10 +571,11 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
       const float gf = g[i], uf = u[i];
       const float s = __fdividef(1.f, 1.f + __expf(-gf));
       const float sl = gf * s;
-      const float a = dh[i] * p;
-      dg[i] = a * uf * s * (1.f + gf * (1.f - s));
-      u[i] = a * sl;
-      dp += dh[i] * sl * uf;
+      // d silu(g)/dg = s (1 + g (1 - s)) = s + sl - sl s
+      const float t = dh[i] * uf;
+      dp = fmaf(t, sl, dp);
+      dg[i] = (t * p) * fmaf(-sl, s, s + sl);
+      u[i] = (dh[i] * p) * sl;
     }
     if constexpr (OPK != OPK_MX) {
       gmax = max(gmax, row_store_bf16_amax(dg, P.y_row + r * P.y_row_ld + col));
