@@ -72,12 +72,16 @@ struct Cfg {
   static constexpr int kSfbBytes = OPK == OPK_MX ? BN * 4 : 0;   // every CTA holds the tile's full SFB
   static constexpr uint32_t kTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStageBytes = (kTx + 1023) / 1024 * 1024;
-  // dSwiGLU: BN = 256 stages the tile's dH as bf16 rows (padded to 264) so the
-  // accumulator is released before the epilogue math; BN = 128 keeps a 32 x 33
-  // fp32 transpose tile per epilogue warp for the column-wise quantiser.
-  // MXFP8 gate-up: a 32 x 20-word scratch per epilogue warp for the column-wise
-  // quantiser (20 KB, what the six-stage ring leaves free)
-  static constexpr int kXposeBytes = EPI == 2 ? (BN == 256 ? 128 * (256 + 8) * 2 : 8 * 32 * 33 * 4) : (EPI == 1 && OPK == OPK_MX ? 8 * 32 * 20 * 4 : 0);
+  // dSwiGLU at BN = 256 parks the tile's dH as packed bf16 in TMEM columns
+  // [kDsCol, kDsCol + 128) so the accumulator is released before the epilogue
+  // math.  MXFP8 gate-up and dSwiGLU at BN = 256: a 32 x 20-word scratch per
+  // epilogue warp for the column-wise quantiser (20 KB, what a six-stage ring
+  // leaves free); BN = 128 dSwiGLU keeps a 32 x 33 fp32 transpose tile per warp.
+  static constexpr bool kDsTmem = EPI == 2 && BN == 256;
+  static constexpr uint32_t kDsCol = 384;
+  static constexpr int kXposeBytes = EPI == 2 && BN == 128 ? 8 * 32 * 33 * 4
+                                     : (EPI == 1 || EPI == 2) && OPK == OPK_MX ? 8 * 32 * 20 * 4
+                                                                             : 0;
   static constexpr int kCtrlBytes = 2048;
   static constexpr int kStages = (232448 - 1024 - kCtrlBytes - kXposeBytes) / kStageBytes > 8
                                      ? 8
@@ -88,7 +92,7 @@ struct Cfg {
   static constexpr uint32_t kSfCol = kAcc * BN;             // first TMEM column of the slots
   static constexpr uint32_t kSfSlot = OPK == OPK_MX ? 4 + BN / 32 : 0;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kCtrlBytes + kXposeBytes;
-  static_assert(kSfCol + kStages * kSfSlot <= 512, "TMEM budget");
+  static_assert(kSfCol + kStages * kSfSlot <= (kDsTmem ? kDsCol : 512u), "TMEM budget");
   static_assert(kABytes == BM * 128, "stage rows are one 128-byte swizzle row");
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(!PAIR || BN == 256, "CTA-pair tiles are 256 x 256");
@@ -114,19 +118,6 @@ __device__ __forceinline__ void load_bf16_32(const uint16_t* src, float (&v)[32]
   for (int j = 0; j < 16; ++j) {
     v[2 * j] = u2f(w[j] << 16);
     v[2 * j + 1] = u2f(w[j] & 0xffff0000u);
-  }
-}
-
-__device__ __forceinline__ void unpack_bf16_32(const uint4* src, float (&v)[32]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 q = src[i];
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[8 * i + 2 * j] = u2f(w[j] << 16);
-      v[8 * i + 2 * j + 1] = u2f(w[j] & 0xffff0000u);
-    }
   }
 }
 
@@ -519,16 +510,18 @@ __device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& 
 }
 
 
-// BN = 256: drain the thread's 128 dH columns to a bf16 staging row in shared
-// memory, release the accumulator, then run the dSwiGLU epilogue from there.
+// BN = 256: drain the thread's 128 dH columns, park them as 64 packed bf16
+// pairs in the warp's own TMEM columns (tstage: this warp's lanes, columns
+// kDsCol + 64·hf ..), release the accumulator, then run the dSwiGLU epilogue
+// from there while the next tile's MMAs fill the accumulator.  `slots` is the
+// warp's 32 x 20-word scratch for the column-wise quantiser.
 template <int OPK>
 __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q,
-                                                   int lane, int hf, const AccRelease& tempty, uint16_t* stage_base) {
+                                                   int lane, int hf, const AccRelease& tempty, uint32_t tstage,
+                                                   float* slots) {
   constexpr int COLS = 128;
-  constexpr int STRIDE = 256 + 8;                 // bf16 per staging row
   const int64_t tok0 = tc.m0 + q * 32;
   const int64_t r = tok0 + lane;
-  uint16_t* srow = stage_base + (q * 32 + lane) * STRIDE + hf * COLS;
   const float f = tile_scale<OPK>(P, tc);         // per-tensor FP8: accumulators -> dH
 #pragma unroll
   for (int c = 0; c < COLS / 32; c += 2) {
@@ -543,16 +536,15 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
         a1[i] = f2u(u2f(a1[i]) * f);
       }
     }
-    uint4* d0 = reinterpret_cast<uint4*>(srow + c * 32);
-    uint4* d1 = reinterpret_cast<uint4*>(srow + (c + 1) * 32);
+    uint32_t w[32];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      d0[i] = make_uint4(pack_bf16x2(u2f(a0[8 * i]), u2f(a0[8 * i + 1])), pack_bf16x2(u2f(a0[8 * i + 2]), u2f(a0[8 * i + 3])),
-                         pack_bf16x2(u2f(a0[8 * i + 4]), u2f(a0[8 * i + 5])), pack_bf16x2(u2f(a0[8 * i + 6]), u2f(a0[8 * i + 7])));
-      d1[i] = make_uint4(pack_bf16x2(u2f(a1[8 * i]), u2f(a1[8 * i + 1])), pack_bf16x2(u2f(a1[8 * i + 2]), u2f(a1[8 * i + 3])),
-                         pack_bf16x2(u2f(a1[8 * i + 4]), u2f(a1[8 * i + 5])), pack_bf16x2(u2f(a1[8 * i + 6]), u2f(a1[8 * i + 7])));
+    for (int i = 0; i < 16; ++i) {
+      w[i] = pack_bf16x2(u2f(a0[2 * i]), u2f(a0[2 * i + 1]));
+      w[16 + i] = pack_bf16x2(u2f(a1[2 * i]), u2f(a1[2 * i + 1]));
     }
+    tmem_st_32x32b_x32(tstage + 16 * c, w);
   }
+  tmem_st_wait();
   release_acc(tempty, lane);
   const float p = P.probs_perm[r];
   const int64_t I = P.I;
@@ -563,7 +555,16 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
   for (int c = 0; c < COLS / 32; ++c) {
     const int64_t col = j0 + c * 32;
     float dh[32], g[32], u[32], dg[32];
-    unpack_bf16_32(reinterpret_cast<const uint4*>(srow + c * 32), dh);
+    {
+      uint32_t w[16];
+      tmem_ld_32x32b_x16(tstage + 16 * c, w);
+      tmem_ld_wait();
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        dh[2 * m] = u2f(w[m] << 16);
+        dh[2 * m + 1] = u2f(w[m] & 0xffff0000u);
+      }
+    }
     load_bf16_32(P.gu_save + r * (2 * I) + col, g);
     load_bf16_32(P.gu_save + r * (2 * I) + I + col, u);
 #pragma unroll
@@ -585,14 +586,12 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
         col_store_bf16(u, P.y_col, P.y_col_ld, I + col, tok0, lane);
       }
     } else {
-      // this chunk's dH slots (the warp's 32 rows x 64 bytes, already read) serve as scratch
-      float* slot = reinterpret_cast<float*>(stage_base + q * 32 * STRIDE + hf * COLS + c * 32);
       uint32_t sb = row_quant32(dg, P.q_out + r * P.q_out_ld + col);
       P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-      col_quant32_slots(dg, slot, STRIDE / 2, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
+      col_quant32_slots(dg, slots, 20, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
       sb = row_quant32(u, P.q_out + r * P.q_out_ld + I + col);
       P.s_out[sf_mma_offset(r, (I + col) >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-      col_quant32_slots(u, slot, STRIDE / 2, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
+      col_quant32_slots(u, slots, 20, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
     }
   }
   P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp;
@@ -974,7 +973,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (EPI == EPI_SWIGLU) {
         epi_swiglu<BN, OPK>(P, tc, tb, q, lane, hf, rel, xpose + (warp - 4) * 32 * 20);
       } else if constexpr (EPI == EPI_DSWIGLU) {
-        if constexpr (BN == 256) epi_dswiglu_staged<OPK>(P, tc, tb, q, lane, hf, rel, reinterpret_cast<uint16_t*>(xpose));
+        if constexpr (BN == 256)
+          epi_dswiglu_staged<OPK>(P, tc, tb, q, lane, hf, rel,
+                                  tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kDsCol + hf * 64,
+                                  xpose + (warp - 4) * 32 * 20);
         else epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
       } else if constexpr (EPI == EPI_ACC_F32) {
         epi_acc_f32<BN>(P, tc, tb, row, hf, rel, lane);

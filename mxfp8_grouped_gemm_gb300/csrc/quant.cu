@@ -141,18 +141,6 @@ __device__ __forceinline__ void copy_col_block(const QuantParams& P, const uint1
   const int srow = 8 * (i >> 1) + 2 * m + (i & 1);
   const uint16_t* rowp = buf + srow * kStride;
   const int j = lane & 3;
-  // this lane's output column for ct = 0 and the steps to the next 8 columns:
-  // the codes' row (column of x) advances by 8, and so does the scale's row
-  // (inside one 32-row group of the tensor-core layout: 8 rows = 128 bytes)
-  const int64_t gc = gcol0 + (lane >> 2);
-  uint8_t* qdst = P.q_col + gc * P.ld_col + p0 + 8 * j;
-  const int64_t qstep = 8 * P.ld_col;
-  const bool store_scale = j == 0 && P.pt_amax == nullptr;
-  int64_t soff = 0, sstep = 0;
-  if (store_scale) {
-    soff = sf_offset(P.layout, gc, p0 >> 5, P.sf_col_rows, P.ld_col >> 5);
-    sstep = P.layout == MXG_LAYOUT_MMA ? 128 : 8 * (P.ld_col >> 5);
-  }
 #pragma unroll
   for (int ct = 0; ct < 4; ++ct) {
     uint32_t r[4];
