@@ -128,10 +128,14 @@ __device__ __forceinline__ uint32_t row_quant32(const float (&h)[32], uint8_t* d
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
   const uint32_t sb = mx_scale_byte(f2u(amax));
-  const float inv = mx_inv_scale(sb);
+  const float2 inv = make_float2(mx_inv_scale(sb), mx_inv_scale(sb));
   float v[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = h[i] * inv;
+  for (int i = 0; i < 32; i += 2) {
+    const float2 t = mul2(make_float2(h[i], h[i + 1]), inv);
+    v[i] = t.x;
+    v[i + 1] = t.y;
+  }
   uint32_t w[8];
   encode32(v, w);
   st_global_v8(dst, w);
@@ -206,12 +210,14 @@ __device__ __forceinline__ void col_quant32_slots(const float (&h)[32], float* s
     }
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
     const uint32_t sb = mx_scale_byte(f2u(m));
-    const float inv = mx_inv_scale(sb);
+    const float2 inv = make_float2(mx_inv_scale(sb), mx_inv_scale(sb));
     uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      w[i] = cvt_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
-             (cvt_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+    for (int i = 0; i < 4; ++i) {
+      const float2 lo = mul2(make_float2(v[4 * i], v[4 * i + 1]), inv);
+      const float2 hi = mul2(make_float2(v[4 * i + 2], v[4 * i + 3]), inv);
+      w[i] = cvt_e4m3x2(lo.x, lo.y) | (cvt_e4m3x2(hi.x, hi.y) << 16);
+    }
     // v[j] holds row j ^ (4g): for g = 1 the words of rows 0-3 / 4-7 (and 8-11 / 12-15) trade places
     const uint4 out = g ? make_uint4(w[1], w[0], w[3], w[2]) : make_uint4(w[0], w[1], w[2], w[3]);
     const int64_t col = col0 + 16 * pass + cl;
@@ -549,7 +555,8 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
   const float p = P.probs_perm[r];
   const int64_t I = P.I;
   const int j0 = tc.nt * 256 + hf * COLS;
-  float dp = 0.f;
+  float2 dp2 = make_float2(0.f, 0.f);
+  const float2 one2 = make_float2(1.f, 1.f), p2 = make_float2(p, p);
   uint32_t gmax = 0;
 #pragma unroll 1
   for (int c = 0; c < COLS / 32; ++c) {
@@ -568,15 +575,22 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
     load_bf16_32(P.gu_save + r * (2 * I) + col, g);
     load_bf16_32(P.gu_save + r * (2 * I) + I + col, u);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float gf = g[i], uf = u[i];
-      const float s = __fdividef(1.f, 1.f + __expf(-gf));
-      const float sl = gf * s;
-      // d silu(g)/dg = s (1 + g (1 - s)) = s + sl - sl s
-      const float t = dh[i] * uf;
-      dp = fmaf(t, sl, dp);
-      dg[i] = (t * p) * fmaf(-sl, s, s + sl);
-      u[i] = (dh[i] * p) * sl;
+    for (int i = 0; i < 32; i += 2) {
+      // lanes i, i + 1 as packed pairs; s = sigmoid(g), sl = silu(g),
+      // d silu(g)/dg = s (1 + g (1 - s)) = s + sl (1 - s)
+      const float2 g2 = make_float2(g[i], g[i + 1]), u2 = make_float2(u[i], u[i + 1]);
+      const float2 dh2 = make_float2(dh[i], dh[i + 1]);
+      const float2 d2 = add2(one2, make_float2(__expf(-g2.x), __expf(-g2.y)));
+      const float2 s2 = make_float2(__fdividef(1.f, d2.x), __fdividef(1.f, d2.y));
+      const float2 sl2 = mul2(g2, s2);
+      const float2 t2 = mul2(dh2, u2);
+      dp2 = fma2(t2, sl2, dp2);
+      const float2 dg2 = mul2(mul2(t2, p2), fma2(sl2, sub2(one2, s2), s2));
+      const float2 du2 = mul2(mul2(dh2, p2), sl2);
+      dg[i] = dg2.x;
+      dg[i + 1] = dg2.y;
+      u[i] = du2.x;
+      u[i + 1] = du2.y;
     }
     if constexpr (OPK != OPK_MX) {
       gmax = max(gmax, row_store_bf16_amax(dg, P.y_row + r * P.y_row_ld + col));
@@ -594,7 +608,7 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
       col_quant32_slots(u, slots, 20, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
     }
   }
-  P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp;
+  P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp2.x + dp2.y;
   if constexpr (OPK == OPK_F8) warp_amax_to(P.amax_out + tc.e, gmax, lane);
 }
 
