@@ -43,9 +43,13 @@ __device__ __forceinline__ uint32_t pair_max_bits(const uint32_t* w, int n) {
 
 __device__ __forceinline__ void quant_store32(float (&v)[32], uint8_t* dst, uint8_t* sdst, uint32_t amax) {
   const uint32_t sb = mx_scale_byte(amax);
-  const float inv = mx_inv_scale(sb);
+  const float2 inv = make_float2(mx_inv_scale(sb), mx_inv_scale(sb));
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] *= inv;
+  for (int i = 0; i < 32; i += 2) {
+    const float2 t = mul2(make_float2(v[i], v[i + 1]), inv);
+    v[i] = t.x;
+    v[i + 1] = t.y;
+  }
   uint32_t w[8];
   encode32(v, w);
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -124,9 +128,13 @@ __device__ __forceinline__ void quant_col_block(const QuantParams& P, const uint
       inv = mx_inv_scale(sb);
     }
     uint32_t w[2];
+    const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
-      w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
+    for (int q = 0; q < 2; ++q) {
+      const float2 lo = mul2(make_float2(v[4 * q], v[4 * q + 1]), inv2);
+      const float2 hi = mul2(make_float2(v[4 * q + 2], v[4 * q + 3]), inv2);
+      w[q] = cvt_e4m3x2(lo.x, lo.y) | (cvt_e4m3x2(hi.x, hi.y) << 16);
+    }
     *reinterpret_cast<uint2*>(qdst + ct * qstep) = make_uint2(w[0], w[1]);
     if (store_scale) P.s_col[soff + ct * sstep] = static_cast<uint8_t>(sb);
   }
