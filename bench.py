@@ -43,7 +43,7 @@ FALLBACK_HBM = 6800.0                # GB/s
 # CPU sample of the workload for the oracle: the first T_S tokens, all experts,
 # full hidden size, the intermediate dimension cut to its first I_S columns.
 CPU_SAMPLE_TOKENS = 512
-CPU_SAMPLE_I = 1024          # the reported cpu_baseline (~10-30 s of host work)
+CPU_SAMPLE_I = 2048          # the reported cpu_baseline (~10-30 s of host work: ~10 s on 16 Grace cores)
 CPU_SAMPLE_I_REF = 256       # per step of the reference arm (K + W steps within a few minutes)
 
 
