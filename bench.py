@@ -28,6 +28,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -156,6 +157,19 @@ def cpu_baseline(inp, wl, reps: int = 1, quant: bool | str = True) -> dict:
 
 
 # ------------------------------------------------------------------- GPU --
+def code_hash(path: str) -> str:
+    """sha256 (16 hex digits) of a source file's code: `//` comments, trailing
+    blanks and empty lines are left out, so a comment edit keeps a profile valid
+    while any change to the code itself invalidates it."""
+    lines = []
+    for ln in open(path, encoding="utf-8").read().splitlines():
+        code = re.sub(r"//.*$", "", ln) if '"' not in ln else ln
+        code = code.rstrip()
+        if code:
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def traffic_for(stage: str, workload: str) -> int | None:
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
     current source of the kernel (else None)."""
@@ -165,7 +179,7 @@ def traffic_for(stage: str, workload: str) -> int | None:
     with open(p) as f:
         d = json.load(f)
     src = os.path.join(ROOT, "mxfp8_grouped_gemm_gb300", "csrc", d.get("source", "gemm.cu"))
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] if os.path.exists(src) else None
+    h = code_hash(src) if os.path.exists(src) else None
     e = d.get("entries", {}).get(f"{workload}/{stage}")
     if not e or e.get("source_sha") != h:
         return None

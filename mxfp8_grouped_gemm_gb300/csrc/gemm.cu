@@ -25,8 +25,9 @@
 //                 (s = sigmoid(g)), d(prob) partial sum_i dH g s u; dGU
 //                 quantised row-wise (dgrad A) and token-column-wise (wgrad A).
 //                 With BN = 256 the accumulator is single-buffered, so dH is
-//                 first drained to shared memory as bf16 and the accumulator
-//                 released; the math then overlaps the next tile's MMAs.
+//                 first parked as bf16 pairs in spare TMEM columns and the
+//                 accumulator released; the math then overlaps the next
+//                 tile's MMAs.
 //
 // CTA = 12 warps: warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs,
 // warp 2 copies each stage's scale factors into TMEM, warps 4-11 run the
@@ -36,8 +37,9 @@
 // CTA pair (cta_group::2: each SM holds its 128 rows of A and half of B, so
 // the operand bytes per MMA flop drop by a third); 4-8-stage smem ring with a
 // matching ring of scale-factor slots in TMEM; the accumulator is
-// double-buffered in TMEM when it fits next to them (BN = 128).  Every wait is bounded; a wait that gives up records
-// MXG_ERR_TIMEOUT, stops the CTA's pipeline and still frees TMEM.
+// double-buffered in TMEM when it fits next to them (BN = 128).  Every wait is
+// bounded; a wait that gives up records MXG_ERR_TIMEOUT, stops the CTA's
+// pipeline and still frees TMEM.
 #include <mutex>
 
 #include "common.cuh"
