@@ -303,7 +303,7 @@ enum {
   MXG_FWD_QUANT_X = 2,       /* gather x to the padded layout + quantise               */
   MXG_FWD_GATE_UP = 3,       /* gate-up GEMM + ScaledSwiGLU + requantise               */
   MXG_FWD_DOWN = 4,          /* down GEMM                                              */
-  MXG_FWD_COMBINE = 5,       /* y[t] = sum_j Y[row(t, j)] (MXFP8: fused into DOWN, empty) */
+  MXG_FWD_COMBINE = 5,       /* y[t] = sum_j Y[row(t, j)] (MXFP8: fused into DOWN for long K) */
   MXG_FWD_NUM_STAGES = 6
 };
 enum {
@@ -312,7 +312,7 @@ enum {
   MXG_BWD_WGRAD_DOWN = 2,    /* dW_down GEMM (token-grouped)                           */
   MXG_BWD_DGRAD_GATE_UP = 3, /* dX GEMM                                                */
   MXG_BWD_WGRAD_GATE_UP = 4, /* dW_gate_up GEMM (token-grouped)                        */
-  MXG_BWD_COMBINE_DX = 5,    /* dx[t] = sum_j dX[row(t, j)] (MXFP8: fused into DGRAD_GATE_UP) */
+  MXG_BWD_COMBINE_DX = 5,    /* dx[t] = sum_j dX[row(t, j)] (MXFP8: fused for long K) */
   MXG_BWD_DPROBS = 6,        /* dprobs[t, j] from the per-tile partials                */
   MXG_BWD_NUM_STAGES = 7
 };

@@ -29,6 +29,20 @@ constexpr bool kUsePairTiles = true;
 constexpr int kMlpAlign = kUsePairTiles ? 256 : 128;
 inline int64_t row_cap(int64_t T, int64_t k, int64_t E) { return align_up(T * k, kMlpAlign) + kMlpAlign * E; }
 
+// Whether a bf16-output GEMM with contraction length K sums each token's k
+// rows in its epilogue (the tile that stores a token's last row reads the other
+// k - 1 back through L2) instead of leaving that to the combine kernel.  The
+// reads wait on L2 one after another, which a long mainloop hides and a short
+// one does not.  Measured on GB300: Mixtral (k = 2, K = 14336 and 28672) fused
+// saves ~0.07 ms per step; 64 experts top-8 (K = 1024 and 2048) fused ran the
+// down GEMM at 0.13 of peak.  Rule: fuse when the tile has at least 32 K steps
+// of 128 per extra row (k = 1 is a plain scatter: always fused), or when the
+// layer routes at most 4096 rows: such a step is bound by its launches (the
+// 256-token, top-2 shape runs 0.39 ms fused against 0.47 ms with the kernel).
+inline bool fuse_combine(int64_t k, int64_t K, int64_t R) {
+  return k == 1 || K / 128 >= 32 * (k - 1) || R <= 4096;
+}
+
 
 // Byte offsets of every buffer inside `saved` and `workspace`.
 struct Plan {
@@ -603,19 +617,24 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   d.b_rows_per_expert = H;
   d.d = at<uint16_t>(ws, pl.yperm);
   d.ldd = H;
-  // F7 fused: the thread that stores the last of a token's k rows sums them into y
-  MXG_TRY(cudaMemsetAsync(at<int32_t>(ws, pl.cmb_cnt), 0, 4 * pl.T * (H / 128) * 2, s));
-  d.cmb_out = A->y;
-  d.cmb_prow_src = at<int32_t>(sv, pl.prow_src);
-  d.cmb_prow_of_src = at<int32_t>(sv, pl.prow_of_src);
-  d.cmb_count = at<int32_t>(ws, pl.cmb_cnt);
-  d.cmb_k = k;
+  if (fuse_combine(k, I, pl.R)) {
+    // F7 fused: the thread that stores the last of a token's k rows sums them into y
+    MXG_TRY(cudaMemsetAsync(at<int32_t>(ws, pl.cmb_cnt), 0, 4 * pl.T * (H / 128) * 2, s));
+    d.cmb_out = A->y;
+    d.cmb_prow_src = at<int32_t>(sv, pl.prow_src);
+    d.cmb_prow_of_src = at<int32_t>(sv, pl.prow_of_src);
+    d.cmb_count = at<int32_t>(ws, pl.cmb_cnt);
+    d.cmb_k = k;
+  }
   d.status = st;
   d.tiles_upper = d.pair ? (pl.Rc / 256) * (H / 256) : (pl.Rc / 128) * (H / gemm_pick_bn(EPI_BF16, H));
   MXG_TRY(launch_gemm(d, s));
   }
 
-  // F7: fused into the down GEMM above (the combine stage has nothing left to do)
+  // F7: y[t] = sum_j Y[row(t, j)] (fused into the down GEMM above for long contractions)
+  if (run(MXG_FWD_COMBINE) && !fuse_combine(k, I, pl.R))
+    MXG_TRY(launch_combine(at<uint16_t>(ws, pl.yperm), at<int32_t>(sv, pl.prow_of_src), static_cast<int>(pl.T),
+                           static_cast<int>(k), static_cast<int>(H), A->y, s));
   return MXG_OK;
 }
 
@@ -766,13 +785,15 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   x.b_rows_per_expert = H;
   x.d = at<uint16_t>(ws, pl.dxperm);
   x.ldd = H;
-  // B6 fused: dx[t] summed by the thread that stores the last of the token's rows
-  MXG_TRY(cudaMemsetAsync(at<int32_t>(ws, pl.cmb_cnt_b), 0, 4 * pl.T * (H / 128) * 2, s));
-  x.cmb_out = A->dx;
-  x.cmb_prow_src = at<int32_t>(sv, pl.prow_src);
-  x.cmb_prow_of_src = at<int32_t>(sv, pl.prow_of_src);
-  x.cmb_count = at<int32_t>(ws, pl.cmb_cnt_b);
-  x.cmb_k = k;
+  if (fuse_combine(k, 2 * I, pl.R)) {
+    // B6 fused: dx[t] summed by the thread that stores the last of the token's rows
+    MXG_TRY(cudaMemsetAsync(at<int32_t>(ws, pl.cmb_cnt_b), 0, 4 * pl.T * (H / 128) * 2, s));
+    x.cmb_out = A->dx;
+    x.cmb_prow_src = at<int32_t>(sv, pl.prow_src);
+    x.cmb_prow_of_src = at<int32_t>(sv, pl.prow_of_src);
+    x.cmb_count = at<int32_t>(ws, pl.cmb_cnt_b);
+    x.cmb_k = k;
+  }
   x.status = st;
   x.tiles_upper = x.pair ? (pl.Rc / 256) * (H / 256) : (pl.Rc / 128) * (H / gemm_pick_bn(EPI_BF16, H));
   MXG_TRY(launch_gemm(x, s));
@@ -806,7 +827,10 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
 
   // B6, B7: combine dx, reduce d(prob)
   const int32_t* prow_of_src = at<int32_t>(sv, pl.prow_of_src);
-  // B6: fused into the dgrad-gate-up GEMM above
+  // B6: dx[t] = sum_j dX[row(t, j)] (fused into the dgrad-gate-up GEMM above for long contractions)
+  if (run(MXG_BWD_COMBINE_DX) && !fuse_combine(k, 2 * I, pl.R))
+    MXG_TRY(launch_combine(at<uint16_t>(ws, pl.dxperm), prow_of_src, static_cast<int>(pl.T), static_cast<int>(k),
+                           static_cast<int>(H), A->dx, s));
   if (run(MXG_BWD_DPROBS))
     MXG_TRY(launch_dprob(at<float>(ws, pl.dp), static_cast<int>(pl.dp_ld), prow_of_src, static_cast<int>(pl.R),
                          A->dprobs, s));
