@@ -456,11 +456,7 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if args.precision == "bf16" else "e4m3", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: Mixtral-8x7B MoE layer T={T} H={H} I={I} E={E} top-{k}"
-                   if wl.name == "mixtral" else f"{wl.name}: T={T} H={H} I={I} E={E} top-{k}",
-                   "precision": args.precision, "tokens_per_step": T, "gemm_flops_per_step": flops,
-                   "l2": "no flush: every step streams > 10 GB (weights 2.8 GB) through HBM, inputs > L2",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": workload_config(wl, args.precision, world),
         "tokens_per_s": round(world * T / (ms * 1e-3), 1),
         "gemm_tflops": round(world * flops / (gemm_ms * 1e-3) / 1e12, 2),
         ("frac_of_bf16_peak" if args.precision == "bf16" else "frac_of_mxfp8_peak"): round(value / world / p_mx, 4),
@@ -486,6 +482,17 @@ def run_ours(args, rank, world):
     return res
 
 
+def workload_config(wl, precision: str, world: int) -> dict:
+    """The `config` object of the JSON line (both arms report the same one)."""
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    name = (f"{wl.name}: Mixtral-8x7B MoE layer T={T} H={H} I={I} E={E} top-{k}" if wl.name == "mixtral"
+            else f"{wl.name}: T={T} H={H} I={I} E={E} top-{k}")
+    return {"workload": name, "precision": precision, "tokens_per_step": T,
+            "gemm_flops_per_step": wl.gemm_flops(True),
+            "l2": "no flush: every step streams > 10 GB (weights 2.8 GB) through HBM, inputs > L2",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args):
     import synthetic
     wl = synthetic.WORKLOADS[args.workload]
@@ -506,7 +513,7 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{wl.name}: T={wl.T} H={wl.H} I={wl.I} E={wl.E} top-{wl.k} (bounded sample)"},
+            "config": workload_config(wl, "mxfp8", 1),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
