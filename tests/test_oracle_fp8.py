@@ -4,7 +4,6 @@ landing on 448, exact round trips of values on a per-tensor grid, the all-zero
 tensor, the error bound of round-to-nearest, and the MoE oracle's fp8 mode
 reducing to the exact MLP on inputs that lie on every expert operand's grid."""
 import numpy as np
-import pytest
 
 from oracle import fp8, moe
 
