@@ -175,6 +175,25 @@ int mxg_route_permute_noalloc(const int32_t* ids, int T, int k, int E, int32_t* 
                               int32_t* row_of_src, int32_t* padded_offsets, int32_t* dev_status, void* stream);
 
 /* ----------------------------------------------------------------------------
+ * Measurement entry (no counterpart in the paper's API): the MXFP8 tensor-core
+ * ceiling of the current GPU.  One CTA per SM runs `steps` steps of four
+ * block-scaled E4M3 MMAs (tcgen05 kind::mxf8f6f4, 128 x 256 x 32 each, fp32
+ * accumulators in TMEM) on operands resident in shared memory, the scale
+ * factors copied into TMEM per stage as the grouped GEMM does; nothing is read
+ * from or written to global memory except dev_status.  The operand values are
+ * fixed small E4M3 codes and the results are discarded.
+ * [Grouped] "Reducing memory pressure with MXFP8": the recipe's gain comes
+ * from 8-bit tensor-core math; the dense MXFP8 rate is measured here so the
+ * GEMMs' fraction of peak has a denominator taken on the same GPU.
+ *   steps      > 0; every step is 4 * 2 * 128 * 256 * 32 flop per SM
+ *   flops      host out: the flop count of the launch (SM count x steps x 4 x
+ *              2 * 128 * 256 * 32); time the launch with events on `stream`
+ *   dev_status device int32; MXG_ERR_TIMEOUT if a bounded wait gave up
+ * The kernel holds all 512 TMEM columns of every SM while it runs: launch it
+ * alone, not concurrently with other tensor-core kernels. */
+int mxg_bench_mxfp8_mma_peak(int steps, double* flops, int32_t* dev_status, void* stream);
+
+/* ----------------------------------------------------------------------------
  * MXFP8 quantisation of a bf16 matrix x [rows][cols].  [Grouped] "Reducing
  * memory pressure with MXFP8", Fig. 3; [Overhead] "How MXFP8 reduces memory
  * use".  Scale rule (OCP MX): e = floor(log2(max|v| over the block)) - 8,

@@ -35,7 +35,7 @@ EXPORTS = [
     "mxg_mlp_weight_cache_bytes", "mxg_mlp_quantize_weights", "mxg_mlp_saved_bytes_cached",
     "mxg_mlp_fp8_saved_bytes", "mxg_mlp_fp8_workspace_bytes", "mxg_grouped_mlp_fp8_fwd", "mxg_grouped_mlp_fp8_bwd",
     "mxg_grouped_mlp_fp8_fwd_stage", "mxg_grouped_mlp_fp8_bwd_stage", "mxg_mlp_fp8_saved_view",
-    "mxg_mlp_workspace_view", "mxg_mlp_weight_cache_view",
+    "mxg_mlp_workspace_view", "mxg_mlp_weight_cache_view", "mxg_bench_mxfp8_mma_peak",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -124,6 +124,7 @@ def lib() -> ctypes.CDLL:
         "mxg_mlp_fp8_saved_view": (P, [P, I32, I32, I32, I32, I32, I32]),
         "mxg_mlp_workspace_view": (P, [P, I32, I32, I32, I32, I32, I32]),
         "mxg_mlp_weight_cache_view": (P, [P, I32, I32, I32, I32]),
+        "mxg_bench_mxfp8_mma_peak": (I32, [I32, ctypes.POINTER(ctypes.c_double), P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -420,3 +421,12 @@ def mxg_grouped_mlp_bwd(dy, saved, workspace, dev_status, E: int, I: int, k: int
     if main_grad is not None:
         return dx, mg_gu, mg_d, dprobs
     return dx, dw_gate_up, dw_down, dprobs
+
+
+def mxg_bench_mxfp8_mma_peak(steps: int, dev_status: torch.Tensor, stream=None) -> float:
+    """Enqueue the MXFP8 MMA-only peak loop; returns the launch's flop count
+    (time it with events on the same stream)."""
+    flops = ctypes.c_double(0.0)
+    _check("mxg_bench_mxfp8_mma_peak", lib().mxg_bench_mxfp8_mma_peak(
+        int(steps), ctypes.byref(flops), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+    return float(flops.value)

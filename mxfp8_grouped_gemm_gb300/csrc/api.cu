@@ -3,6 +3,7 @@
 // passes.  Nothing here allocates or synchronises; every call only enqueues
 // work on the caller's stream.
 #include <atomic>
+#include <climits>
 #include <cstring>
 
 #include "common.cuh"
@@ -136,6 +137,8 @@ bool mlp_shape_ok(int T, int H, int I, int E, int k) {
   if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return false;
   if (H % 128 || I % 128) return false;
   if (k > E || E > 256 || k > 32) return false;
+  // padded row indices are int32: T*k rows plus up to 256 padding rows per group
+  if (static_cast<int64_t>(T) * k + 256 * (static_cast<int64_t>(E) + 1) > INT32_MAX) return false;
   return true;
 }
 
@@ -227,7 +230,9 @@ int mxg_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float
 
 size_t mxg_route_permute_workspace_bytes(int T, int k, int E) {
   if (T <= 0 || k <= 0 || E <= 0) return 0;
-  const int64_t nblk = permute_num_blocks(T * k);
+  const int64_t R = static_cast<int64_t>(T) * k;     // routed entries; must fit the kernels' int32 indices
+  if (R > INT32_MAX) return 0;
+  const int64_t nblk = permute_num_blocks(static_cast<int>(R));
   return static_cast<size_t>(align_up(4 * nblk * E, kAlign) * 2 + align_up(4 * (E + 1), kAlign));
 }
 
@@ -238,14 +243,16 @@ int mxg_route_permute(const int32_t* ids, int T, int k, int E, int32_t* split_si
     return MXG_ERR_ARG;
   if (T <= 0 || k <= 0 || E <= 0) return MXG_ERR_ARG;
   if (k > E || E > 256) return MXG_ERR_SHAPE;
+  const int64_t R = static_cast<int64_t>(T) * k;
+  if (R > INT32_MAX) return MXG_ERR_SHAPE;           // row indices are int32
   if (!aligned32(ids) || !aligned32(split_sizes) || !aligned32(src_of_row) || !aligned32(row_of_src) ||
       !aligned32(padded_offsets) || !aligned32(ws))
     return MXG_ERR_ALIGN;
   if (ws_bytes < mxg_route_permute_workspace_bytes(T, k, E)) return MXG_ERR_WORKSPACE;
-  const int64_t nblk = permute_num_blocks(T * k);
+  const int64_t nblk = permute_num_blocks(static_cast<int>(R));
   PermuteParams p{};
   p.ids = ids;
-  p.R = T * k;
+  p.R = static_cast<int32_t>(R);
   p.E = E;
   p.counts = at<int32_t>(ws, 0);
   p.bases = at<int32_t>(ws, align_up(4 * nblk * E, kAlign));

@@ -12,6 +12,7 @@
 // h and dGU in bf16 (row-major and transposed) instead of MXFP8.  All GEMMs run
 // as 256 x 256 CTA-pair tiles, so H and I must be multiples of 256 and expert
 // groups start on multiples of 256 rows.
+#include <climits>
 #include <cstring>
 
 #include "common.cuh"
@@ -33,6 +34,8 @@ bool shape_ok(int T, int H, int I, int E, int k) {
   if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return false;
   if (H % 256 || I % 256) return false;
   if (k > E || E > 256 || k > 32) return false;
+  // padded row indices are int32: T*k rows plus up to 256 padding rows per group
+  if (static_cast<int64_t>(T) * k + 256 * (static_cast<int64_t>(E) + 1) > INT32_MAX) return false;
   return true;
 }
 

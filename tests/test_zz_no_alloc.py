@@ -48,6 +48,61 @@ def test_noalloc_permute_matches_regular_entry_twice():
                 assert torch.equal(got[name], ref[name]), (T, E, k, call, name)
 
 
+def test_noalloc_permute_at_its_size_limit():
+    """E = 256 with exactly mxg_route_permute_noalloc_max_entries(256) routed
+    entries: the scratch's per-chunk counts and bases fill the static array to
+    its end; results must still equal the regular entry point's, and one more
+    entry is rejected on the host."""
+    m = require_gpu()
+    L = m.lib()
+    E, k = 256, 8
+    limit = int(L.mxg_route_permute_noalloc_max_entries(E))
+    assert limit % k == 0
+    T = limit // k
+    rng = np.random.default_rng(11)
+    logits = torch.from_numpy(rng.standard_normal((T, E)).astype(np.float32)).cuda()
+    ids, _ = m.mxg_route_topk(logits, k)
+    st_ref = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = m.mxg_route_permute(ids, E, st_ref)
+    for call in range(2):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        got = _noalloc(L, ids, E, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0 and int(st_ref.item()) == 0
+        for name in ref:
+            assert torch.equal(got[name], ref[name]), (call, name)
+    fake = ctypes.c_void_p(0x10000)
+    rc = L.mxg_route_permute_noalloc(fake, limit + 1, 1, E, fake, fake, fake, fake, fake, None)
+    assert rc == 5                                   # MXG_ERR_WORKSPACE, nothing launched
+
+
+def test_noalloc_permute_leaves_device_memory_unchanged():
+    """After a first call on the device, a call changes neither the free device
+    memory nor torch's allocated bytes: the entry point allocates nothing."""
+    m = require_gpu()
+    L = m.lib()
+    T, E, k = 2048, 8, 2
+    rng = np.random.default_rng(12)
+    logits = torch.from_numpy(rng.standard_normal((T, E)).astype(np.float32)).cuda()
+    ids, _ = m.mxg_route_topk(logits, k)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _noalloc(L, ids, E, st)                          # first call on this device: address lookup, module load
+    out = {"split_sizes": torch.empty(E, dtype=torch.int32, device="cuda"),
+           "src_of_row": torch.empty(T * k, dtype=torch.int32, device="cuda"),
+           "row_of_src": torch.empty(T * k, dtype=torch.int32, device="cuda"),
+           "padded_offsets": torch.empty(E + 1, dtype=torch.int32, device="cuda")}
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    rc = L.mxg_route_permute_noalloc(ids.data_ptr(), T, k, E, out["split_sizes"].data_ptr(),
+                                     out["src_of_row"].data_ptr(), out["row_of_src"].data_ptr(),
+                                     out["padded_offsets"].data_ptr(), st.data_ptr(),
+                                     torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0 and int(st.item()) == 0
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == alloc0
+
+
 def test_noalloc_permute_rejects_oversize_on_host():
     m = require_gpu()
     L = m.lib()
