@@ -274,3 +274,95 @@ def test_weight_quant_pool_equals_oracle():
         pool.close()
     for n in ("wg", "wd", "wdT", "wguT"):
         assert np.array_equal(got[n], ref[n]), n
+
+
+def test_backward_quantised_dgrad_and_wgrad_gate_up_operands():
+    """With quantisation on, dX of an expert's rows equals deq(MX(dGU) along 2I)
+    times deq(MX(W_gate_up^T) along 2I), and dW_gate_up equals
+    deq(colMX(dGU))^T deq(colMX(X)) with token blocks from the group's first
+    row.  Every operand is built here from codes and scale bytes along the
+    stated axis; the plausible mistakes (the weight quantised along H, dGU
+    quantised over tokens for the dgrad, or row-wise for the wgrad) are shown
+    to give different results, so the pin tells them apart."""
+    T, H, I, E, k = 80, 64, 96, 3, 2                 # H != 2I: a transposed operand cannot go unnoticed
+    c = _case(T, H, I, E, k, 83)
+    ids, probs = moe.route_topk(c["logits"], k)
+    ctx = moe.mlp_fwd(c["x"], ids, probs, c["w_gate_up"], c["w_down"])
+    g = moe.mlp_bwd(ctx, c["dy"])
+    perm = ctx["perm"]
+    tok = perm["src_of_row"] // k
+    for e in range(E):
+        a, b = perm["offsets"][e], perm["offsets"][e + 1]
+        m = b - a
+        assert m > 32                                  # spans more than one token block
+        dgu = g["dgu"][a:b]                            # [m, 2I]
+        dgu_q = mx.dequantize_blocks(*mx.quantize_blocks(dgu))              # blocks along 2I
+        wT = np.ascontiguousarray(c["w_gate_up"][e].T)                      # [H, 2I]
+        wT_q = mx.dequantize_blocks(*mx.quantize_blocks(wT))                # blocks along 2I
+        dx_rows = dgu_q @ wT_q.T
+        np.testing.assert_allclose(g["dx_perm"][a:b], dx_rows, rtol=1e-12, atol=1e-13)
+        w_along_h = mx.fake_quant(c["w_gate_up"][e])                       # [2I, H], blocks along H
+        assert not np.allclose(g["dx_perm"][a:b], dgu_q @ w_along_h, rtol=1e-6, atol=0)
+        dgu_tok = mx.fake_quant_group_columns(dgu)                          # blocks over tokens
+        assert not np.allclose(g["dx_perm"][a:b], dgu_tok @ wT_q.T, rtol=1e-6, atol=0)
+
+        x_perm = c["x"][tok[a:b]]                      # [m, H]
+        cd, sd = mx.quantize_group_columns(dgu)        # [2I, mpad]: 32-token blocks from the group start
+        cx, sx = mx.quantize_group_columns(x_perm)     # [H, mpad]
+        mpad = cd.shape[1]
+        assert mpad == -(-m // 32) * 32 and cx.shape == (H, mpad)
+        dw = mx.dequantize_blocks(cd, sd) @ mx.dequantize_blocks(cx, sx).T  # padding tokens are zero codes
+        np.testing.assert_allclose(g["dw_gate_up"][e], dw, rtol=1e-12, atol=1e-13)
+        row_wise = dgu_q.T @ mx.fake_quant_group_columns(x_perm)
+        assert not np.allclose(g["dw_gate_up"][e], row_wise, rtol=1e-6, atol=0)
+
+
+def _f32_patterns() -> np.ndarray:
+    """fp32 bit patterns covering every exponent and sign with the low 16 bits
+    at 0, 1, just below / at / just above the halfway point and all ones, the
+    kept bit (bit 16) both 0 and 1, plus the overflow boundary, the largest
+    finite values, infinities, zeros and a random sweep (no NaNs: out of scope)."""
+    pats = []
+    for sign in (0, 1):
+        for e in range(0, 255):
+            for keep in (0, 1):
+                for upper in (0x00, 0x15, 0x3F):          # mantissa bits 17..22
+                    for low in (0x0000, 0x0001, 0x7FFF, 0x8000, 0x8001, 0xFFFF):
+                        pats.append((sign << 31) | (e << 23) | (upper << 17) | (keep << 16) | low)
+    pats += [0x7F7F7FFF, 0x7F7F8000, 0x7F7FFFFF, 0x7F800000, 0xFF800000, 0x00000000, 0x80000000,
+             0x00008000, 0x00018000, 0x80008000]
+    rng = np.random.default_rng(7)
+    rnd = rng.integers(0, 2 ** 32, size=200_000, dtype=np.uint64).astype(np.uint32)
+    rnd = rnd[((rnd >> 23) & 0xFF) != 0xFF]            # drop NaN / inf exponents from the random part
+    return np.concatenate([np.array(pats, dtype=np.uint32), rnd])
+
+
+def test_bf16_round_matches_torch_cast_on_fp32_patterns():
+    """moe.bf16_round on fp32-representable values (its first step, fp64 ->
+    fp32, is then exact) equals torch's round-to-nearest-even fp32 -> bf16
+    cast bit for bit, ties to even included, overflow to infinity included."""
+    bits = _f32_patterns()
+    f = bits.view(np.float32)
+    ours = moe.bf16_round(f.astype(np.float64)).astype(np.float32).view(np.uint32)
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).to(torch.float32).numpy().view(np.uint32)
+    bad = np.nonzero(ours != ref)[0]
+    assert bad.size == 0, [hex(int(bits[i])) for i in bad[:8]]
+    # spot values: a tie rounds to the even neighbour, one unit above it rounds up
+    one = np.float64(1.0)
+    assert moe.bf16_round(np.array([one + 2.0 ** -8]))[0] == one               # tie, even below
+    assert moe.bf16_round(np.array([one + 3 * 2.0 ** -8]))[0] == one + 2.0 ** -6  # tie, even above
+    assert moe.bf16_round(np.array([one + 2.0 ** -8 + 2.0 ** -20]))[0] == one + 2.0 ** -7
+
+
+def test_bf16_round_of_fp64_values_is_rounding_via_fp32():
+    """For general fp64 values the result is the fp32 rounding followed by the
+    bf16 rounding (what the docstring states), checked against torch doing the
+    same two casts, and it is always one of the two bf16 neighbours of v."""
+    rng = np.random.default_rng(8)
+    v = rng.standard_normal(100_000) * np.exp2(rng.integers(-30, 30, size=100_000))
+    ours = moe.bf16_round(v)
+    ref = torch.from_numpy(v).to(torch.float32).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(ours, ref)
+    lo = torch.from_numpy(v).to(torch.bfloat16).double().numpy()   # some bf16 neighbour of v
+    assert np.all(np.abs(ours - v) <= np.abs(v) * 2.0 ** -8 * (1 + 2.0 ** -15))
+    assert np.all((ours == lo) | (np.abs(ours - lo) <= np.abs(v) * 2.0 ** -7))
