@@ -8,6 +8,6 @@ from ._lib import (  # noqa: F401
     mxg_device_supported, mxg_grouped_gemm, mxg_grouped_gemm_wgrad, mxg_grouped_mlp_bwd, mxg_grouped_mlp_fwd,
     mxg_launch_count, mxg_mlp_group_align, mxg_mlp_row_capacity, mxg_mlp_saved_bytes, mxg_mlp_saved_view, mxg_mlp_workspace_bytes, mxg_mlp_workspace_view, mxg_mxfp8_quantize,
     mxg_route_permute, mxg_route_topk, mxg_router_bwd, mxg_router_bwd_workspace_bytes, mxg_router_fwd, status_string,
-    WeightCache, mxg_mlp_quantize_weights, mxg_mlp_saved_bytes_cached,
+    WeightCache, mxg_mlp_quantize_weights, mxg_mlp_saved_bytes_cached, mxg_bench_mxfp8_mma_peak,
 )
 from .layer import GroupedMLP  # noqa: F401
