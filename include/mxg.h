@@ -55,7 +55,8 @@ typedef enum {
   /* device-detected, reported through dev_status */
   MXG_ERR_EXPERT_ID = 16, /* an expert id outside [0, E)                             */
   MXG_ERR_OFFSETS = 17,   /* group offsets not monotone / not 128-aligned / too big  */
-  MXG_ERR_TIMEOUT = 18    /* a bounded wait inside a kernel gave up                  */
+  MXG_ERR_TIMEOUT = 18,   /* a bounded wait inside a kernel gave up                  */
+  MXG_ERR_INDEX = 19      /* a row index outside the buffer it indexes               */
 } mxg_status;
 
 /* Layout of MXFP8 scale bytes. */
@@ -210,6 +211,71 @@ int mxg_mxfp8_quantize(const uint16_t* x, int rows, int cols, uint8_t* q_row, ui
                        uint8_t* s_col, int layout, void* stream);
 
 /* ----------------------------------------------------------------------------
+ * MXFP8 quantisation of rows that come in groups (the tokens of each expert,
+ * one count per expert: [Grouped] "Grouping fragmented expert workloads"),
+ * with the column-wise blocks of 32 rows restarting at every group's first
+ * row, as the weight-gradient operands need them ([Grouped] "Fusing precision
+ * conversion and expert computation": MXFP8 in the backward too; the blocks
+ * run over tokens because the weight gradients contract over tokens).  Scale
+ * rule as mxg_mxfp8_quantize.
+ *   x               bf16 [rows][cols] (device), the groups one after another
+ *   group_offsets   int32 [groups+1] (device): 0 = off[0] <= ... <= off[groups]
+ *                   = rows; group g is rows [off[g], off[g+1])
+ *   padded_offsets  int32 [groups+1] out (device): the output row layout;
+ *                   group g occupies padded rows [poff[g], poff[g+1]), its
+ *                   size rounded up to A rows, A = 32 (MXG_LAYOUT_CANONICAL) or
+ *                   128 (MXG_LAYOUT_MMA, the grouped GEMMs' tile height)
+ *   q_row/s_row     (nullable) row-wise (blocks along cols): codes uint8
+ *                   [cap][cols], scales per `layout` (R = cap rows)
+ *   q_col/s_col     (nullable) column-wise, transposed: codes uint8
+ *                   [cols][cap], blocks of 32 consecutive padded rows (never
+ *                   straddling groups); scales per `layout` (R = cols rows,
+ *                   K = cap)
+ *   cap             = mxg_mxfp8_grouped_rows_capacity(rows, groups, layout)
+ * Padding rows inside a group's padded range are zero codes (and zero scale
+ * bytes where a whole block is padding); rows at or past poff[groups] are not
+ * written.  Requires cols % 128 == 0, 1 <= groups <= 2^20.  Offsets that do not
+ * start at 0, decrease, or do not end at `rows` set MXG_ERR_OFFSETS in
+ * dev_status; padded_offsets is then all zeros and nothing is quantised.
+ * Two launches (the padded offsets, then the quantiser). */
+size_t mxg_mxfp8_grouped_rows_capacity(int rows, int groups, int layout);
+int mxg_mxfp8_quantize_grouped(const uint16_t* x, int rows, int cols, const int32_t* group_offsets, int groups,
+                               int32_t* padded_offsets, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                               uint8_t* s_col, int layout, int32_t* dev_status, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * Row gather: dst row r = src row index[r] / div, for rows of row_bytes bytes
+ * (a multiple of 4).  The dispatch and return steps around grouped tokens:
+ * x in permuted order (index = src_of_row, div = k), the per-row routing
+ * probabilities (index = src_of_row, div = 1, row_bytes = 4), the rows an
+ * expert-parallel exchange brings back, or dprobs[t][j] = dprob_rows[
+ * row_of_src[t*k+j]] ([Grouped] "Grouping fragmented expert workloads": tokens
+ * are grouped per expert before the grouped GEMMs and returned after).
+ *   src    device, src_rows rows;  index int32 [rows] (device)
+ *   dst    device, rows rows (must not overlap src)
+ * An index outside [0, src_rows * div) gives a zero row and MXG_ERR_INDEX in
+ * dev_status.  Pointers 4-byte aligned (16-byte aligned rows go as 16-byte
+ * vectors).  HBM-bound: one read and one write per byte. */
+int mxg_gather_rows(const void* src, int64_t src_rows, int64_t row_bytes, const int32_t* index, int div,
+                    int64_t rows, void* dst, int32_t* dev_status, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * Combine (unpermute + sum): y[t] = sum_j rows[row_of_src[t*k + j]] for
+ * j = 0..k-1, accumulated in fp32 in slot order, one bf16 rounding.  The
+ * weighted sum of [Grouped] Fig. 1 with the routing probability already
+ * applied to each row (inside ScaledSwiGLU, "Fusing precision conversion and
+ * expert computation"), so this is a plain sum.  The MLP calls run it (or
+ * its fused form) themselves; this entry serves rows that come back from
+ * elsewhere (an expert-parallel return, or mxg_grouped_mlp_fwd_grouped).
+ *   rows        bf16 [src_rows][H] (device);  row_of_src int32 [T*k] (device;
+ *               a negative entry is skipped; one >= src_rows is skipped and
+ *               reported as MXG_ERR_INDEX)
+ *   y           bf16 [T][H] out
+ * Requires H % 8 == 0, k <= 32; rows and y 16-byte aligned. */
+int mxg_combine(const uint16_t* rows, int64_t src_rows, const int32_t* row_of_src, int T, int k, int H, uint16_t* y,
+                int32_t* dev_status, void* stream);
+
+/* ----------------------------------------------------------------------------
  * Grouped MXFP8 GEMM, row-grouped (the GroupedLinear forward/dgrad shape;
  * [Grouped] "Grouping fragmented expert workloads"): for each expert e, rows
  * [padded_offsets[e], padded_offsets[e+1]) of A are multiplied by expert e's
@@ -347,6 +413,50 @@ size_t mxg_mlp_saved_bytes(int T, int H, int I, int E, int k);
 size_t mxg_mlp_workspace_bytes(int T, int H, int I, int E, int k);
 int mxg_grouped_mlp_fwd(const mxg_mlp_fwd_args* args, void* stream);
 int mxg_grouped_mlp_bwd(const mxg_mlp_bwd_args* args, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * The grouped expert MLP on tokens that arrive already grouped by expert: the
+ * pages' GroupedLinear call, experts(tokens, split_sizes), one count per
+ * expert and one weight per expert ([Grouped] "Grouping fragmented expert
+ * workloads"), e.g. rows an expert-parallel dispatcher delivered or a caller
+ * that permuted them itself.  Same forward as mxg_grouped_mlp_fwd with each
+ * row its own token (T = R, k = 1) and its expert given by position:
+ *   x            bf16 [R][H]: expert e's rows are [sum_{e'<e} split_sizes[e'],
+ *                + split_sizes[e]) (empty experts allowed)
+ *   split_sizes  int32 [E] (device, input); negative sizes or a sum other
+ *                than R set MXG_ERR_OFFSETS in dev_status (rows no expert
+ *                covers are then skipped and reported as MXG_ERR_EXPERT_ID)
+ *   probs        fp32 [R]: each row's routing probability, applied once in
+ *                ScaledSwiGLU
+ *   y            bf16 [R][H] out: each row's expert output (not combined;
+ *                mxg_combine sums a token's rows)
+ *   saved        mxg_mlp_grouped_saved_bytes(R, H, I, E) bytes
+ *   workspace    mxg_mlp_grouped_workspace_bytes(R, H, I, E) bytes
+ *   w_gate_up, w_down, save_for_backward, dev_status, weight_cache: as
+ *                mxg_mlp_fwd_args.
+ * The backward is mxg_grouped_mlp_bwd with T = R, k = 1, this `saved`, and a
+ * workspace of the same size: dy [R][H] -> dx [R][H] (per row), dW, dprobs
+ * [R].  Same shape rules and errors as mxg_grouped_mlp_fwd. */
+typedef struct {
+  int32_t R, H, I, E;
+  const uint16_t* x;           /* bf16 [R][H], grouped by expert             */
+  const int32_t* split_sizes;  /* int32 [E] rows per expert (device, input)  */
+  const float* probs;          /* fp32 [R]                                   */
+  const uint16_t* w_gate_up;   /* bf16 [E][2I][H]                            */
+  const uint16_t* w_down;      /* bf16 [E][H][I]                             */
+  uint16_t* y;                 /* out bf16 [R][H]                            */
+  void* saved;
+  uint64_t saved_bytes;
+  void* workspace;
+  uint64_t workspace_bytes;
+  int32_t save_for_backward;
+  int32_t* dev_status;
+  const void* weight_cache;
+  uint64_t weight_cache_bytes;
+} mxg_mlp_grouped_fwd_args;
+size_t mxg_mlp_grouped_saved_bytes(int R, int H, int I, int E);
+size_t mxg_mlp_grouped_workspace_bytes(int R, int H, int I, int E);
+int mxg_grouped_mlp_fwd_grouped(const mxg_mlp_grouped_fwd_args* args, void* stream);
 
 /* Weight cache: the four MXFP8 weight tensors the MLP needs (W_gate_up
  * quantised along H and along 2I, W_down along I and along H, codes and

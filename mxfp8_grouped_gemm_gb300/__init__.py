@@ -9,5 +9,7 @@ from ._lib import (  # noqa: F401
     mxg_launch_count, mxg_mlp_group_align, mxg_mlp_row_capacity, mxg_mlp_saved_bytes, mxg_mlp_saved_view, mxg_mlp_workspace_bytes, mxg_mlp_workspace_view, mxg_mxfp8_quantize,
     mxg_route_permute, mxg_route_topk, mxg_router_bwd, mxg_router_bwd_workspace_bytes, mxg_router_fwd, status_string,
     WeightCache, mxg_mlp_quantize_weights, mxg_mlp_saved_bytes_cached, mxg_bench_mxfp8_mma_peak,
+    mxg_mxfp8_grouped_rows_capacity, mxg_mxfp8_quantize_grouped, mxg_gather_rows, mxg_combine,
+    mxg_mlp_grouped_saved_bytes, mxg_mlp_grouped_workspace_bytes, mxg_grouped_mlp_fwd_grouped,
 )
-from .layer import GroupedMLP  # noqa: F401
+from .layer import GroupedExperts, GroupedMLP  # noqa: F401

@@ -20,7 +20,7 @@ MXG_LAYOUT_MMA = 1
 STATUS = {
     0: "MXG_OK", 1: "MXG_ERR_ARG", 2: "MXG_ERR_SHAPE", 3: "MXG_ERR_ALIGN", 4: "MXG_ERR_ARCH",
     5: "MXG_ERR_WORKSPACE", 6: "MXG_ERR_CUDA", 16: "MXG_ERR_EXPERT_ID", 17: "MXG_ERR_OFFSETS",
-    18: "MXG_ERR_TIMEOUT",
+    18: "MXG_ERR_TIMEOUT", 19: "MXG_ERR_INDEX",
 }
 
 EXPORTS = [
@@ -36,6 +36,8 @@ EXPORTS = [
     "mxg_mlp_fp8_saved_bytes", "mxg_mlp_fp8_workspace_bytes", "mxg_grouped_mlp_fp8_fwd", "mxg_grouped_mlp_fp8_bwd",
     "mxg_grouped_mlp_fp8_fwd_stage", "mxg_grouped_mlp_fp8_bwd_stage", "mxg_mlp_fp8_saved_view",
     "mxg_mlp_workspace_view", "mxg_mlp_weight_cache_view", "mxg_bench_mxfp8_mma_peak",
+    "mxg_mxfp8_grouped_rows_capacity", "mxg_mxfp8_quantize_grouped", "mxg_gather_rows", "mxg_combine",
+    "mxg_mlp_grouped_saved_bytes", "mxg_mlp_grouped_workspace_bytes", "mxg_grouped_mlp_fwd_grouped",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -54,6 +56,16 @@ class MlpFwdArgs(ctypes.Structure):
                 ("probs", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
                 ("y", ctypes.c_void_p), ("split_sizes", ctypes.c_void_p), ("saved", ctypes.c_void_p),
                 ("saved_bytes", ctypes.c_uint64), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_uint64), ("save_for_backward", ctypes.c_int32),
+                ("dev_status", ctypes.c_void_p), ("weight_cache", ctypes.c_void_p),
+                ("weight_cache_bytes", ctypes.c_uint64)]
+
+
+class MlpGroupedFwdArgs(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("x", ctypes.c_void_p), ("split_sizes", ctypes.c_void_p), ("probs", ctypes.c_void_p),
+                ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("saved", ctypes.c_void_p), ("saved_bytes", ctypes.c_uint64), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_uint64), ("save_for_backward", ctypes.c_int32),
                 ("dev_status", ctypes.c_void_p), ("weight_cache", ctypes.c_void_p),
                 ("weight_cache_bytes", ctypes.c_uint64)]
@@ -80,7 +92,7 @@ def lib() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with `python -m mxfp8_grouped_gemm_gb300.build`")
     L = ctypes.CDLL(LIB_PATH)
-    I32, U64, SZ, P = ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t, ctypes.c_void_p
+    I32, I64, U64, SZ, P = ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t, ctypes.c_void_p
     sig = {
         "mxg_status_string": (ctypes.c_char_p, [I32]),
         "mxg_device_supported": (I32, []),
@@ -125,6 +137,13 @@ def lib() -> ctypes.CDLL:
         "mxg_mlp_workspace_view": (P, [P, I32, I32, I32, I32, I32, I32]),
         "mxg_mlp_weight_cache_view": (P, [P, I32, I32, I32, I32]),
         "mxg_bench_mxfp8_mma_peak": (I32, [I32, ctypes.POINTER(ctypes.c_double), P, P]),
+        "mxg_mxfp8_grouped_rows_capacity": (SZ, [I32, I32, I32]),
+        "mxg_mxfp8_quantize_grouped": (I32, [P, I32, I32, P, I32, P, P, P, P, P, I32, P, P]),
+        "mxg_gather_rows": (I32, [P, I64, I64, P, I32, I64, P, P, P]),
+        "mxg_combine": (I32, [P, I64, P, I32, I32, I32, P, P, P]),
+        "mxg_mlp_grouped_saved_bytes": (SZ, [I32, I32, I32, I32]),
+        "mxg_mlp_grouped_workspace_bytes": (SZ, [I32, I32, I32, I32]),
+        "mxg_grouped_mlp_fwd_grouped": (I32, [ctypes.POINTER(MlpGroupedFwdArgs), P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -430,3 +449,89 @@ def mxg_bench_mxfp8_mma_peak(steps: int, dev_status: torch.Tensor, stream=None) 
     _check("mxg_bench_mxfp8_mma_peak", lib().mxg_bench_mxfp8_mma_peak(
         int(steps), ctypes.byref(flops), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
     return float(flops.value)
+
+
+def mxg_mxfp8_grouped_rows_capacity(rows: int, groups: int, layout: int = MXG_LAYOUT_CANONICAL) -> int:
+    return int(lib().mxg_mxfp8_grouped_rows_capacity(rows, groups, layout))
+
+
+def mxg_mxfp8_quantize_grouped(x: torch.Tensor, group_offsets: torch.Tensor, dev_status: torch.Tensor,
+                               row: bool = True, col: bool = True, layout: int = MXG_LAYOUT_CANONICAL,
+                               stream=None) -> dict:
+    """x bf16 [rows, cols] in groups (group_offsets int32 [groups+1]) -> the
+    padded group layout: 'padded_offsets', and 'q_row','s_row' / 'q_col','s_col'."""
+    rows, cols = x.shape
+    groups = group_offsets.numel() - 1
+    cap = mxg_mxfp8_grouped_rows_capacity(rows, groups, layout)
+    if cap == 0:
+        raise ValueError(f"unsupported grouped quantisation rows={rows} groups={groups}")
+    dev = x.device
+    out = {"padded_offsets": torch.empty(groups + 1, dtype=torch.int32, device=dev), "capacity": cap}
+    if row:
+        out["q_row"] = torch.empty((cap, cols), dtype=torch.uint8, device=dev)
+        out["s_row"] = torch.empty(cap * cols // 32, dtype=torch.uint8, device=dev)
+    if col:
+        out["q_col"] = torch.empty((cols, cap), dtype=torch.uint8, device=dev)
+        out["s_col"] = torch.empty(cap * cols // 32, dtype=torch.uint8, device=dev)
+    _check("mxg_mxfp8_quantize_grouped", lib().mxg_mxfp8_quantize_grouped(
+        _ptr(_bits(x), None, "x"), rows, cols, _ptr(group_offsets, torch.int32, "group_offsets"), groups,
+        _ptr(out["padded_offsets"]), _ptr(out.get("q_row")), _ptr(out.get("s_row")), _ptr(out.get("q_col")),
+        _ptr(out.get("s_col")), layout, _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+    return out
+
+
+def mxg_gather_rows(src: torch.Tensor, index: torch.Tensor, dev_status: torch.Tensor, div: int = 1,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[r] = src[index[r] // div] (rows of src's trailing dimensions)."""
+    src_rows = src.shape[0]
+    row_bytes = src[0].numel() * src.element_size() if src.dim() > 1 else src.element_size()
+    rows = index.numel()
+    out = torch.empty((rows,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device) if out is None else out
+    _check("mxg_gather_rows", lib().mxg_gather_rows(
+        _ptr(src, None, "src"), src_rows, row_bytes, _ptr(index, torch.int32, "index"), div, rows,
+        _ptr(out, src.dtype, "out"), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+    return out
+
+
+def mxg_combine(rows: torch.Tensor, row_of_src: torch.Tensor, k: int, dev_status: torch.Tensor,
+                y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[t] = sum_j rows[row_of_src[t*k + j]] (fp32 sum in slot order, bf16 out)."""
+    src_rows, H = rows.shape
+    T = row_of_src.numel() // k
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=rows.device) if y is None else y
+    _check("mxg_combine", lib().mxg_combine(
+        _ptr(_bits(rows), torch.int16, "rows"), src_rows, _ptr(row_of_src, torch.int32, "row_of_src"), T, k, H,
+        _ptr(_bits(y), torch.int16, "y"), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+    return y
+
+
+def mxg_mlp_grouped_saved_bytes(R, H, I, E) -> int:
+    return int(lib().mxg_mlp_grouped_saved_bytes(R, H, I, E))
+
+
+def mxg_mlp_grouped_workspace_bytes(R, H, I, E) -> int:
+    return int(lib().mxg_mlp_grouped_workspace_bytes(R, H, I, E))
+
+
+def mxg_grouped_mlp_fwd_grouped(x, split_sizes, probs, w_gate_up, w_down, saved, workspace, dev_status, y=None,
+                                save_for_backward: bool = True, weight_cache: WeightCache | None = None,
+                                stream=None):
+    """Forward on rows already grouped by expert (split_sizes int32 [E] on the
+    device, probs fp32 [R]); returns the per-row outputs y [R, H]."""
+    R, H = x.shape
+    if weight_cache is not None:
+        E, I = weight_cache.E, weight_cache.I
+    else:
+        E, N2, _ = w_gate_up.shape
+        I = N2 // 2
+    y = torch.empty((R, H), dtype=torch.bfloat16, device=x.device) if y is None else y
+    a = MlpGroupedFwdArgs(R, H, I, E, _ptr(_bits(x), torch.int16, "x"), _ptr(split_sizes, torch.int32, "split_sizes"),
+                          _ptr(probs, torch.float32, "probs"), _ptr(_bits(w_gate_up), torch.int16, "w_gate_up"),
+                          _ptr(_bits(w_down), torch.int16, "w_down"), _ptr(_bits(y), torch.int16, "y"),
+                          _ptr(saved, torch.uint8, "saved"), saved.numel(), _ptr(workspace, torch.uint8, "workspace"),
+                          workspace.numel(), 1 if save_for_backward else 0,
+                          _ptr(dev_status, torch.int32, "dev_status"),
+                          None if weight_cache is None else _ptr(weight_cache.buffer, torch.uint8, "weight_cache"),
+                          0 if weight_cache is None else weight_cache.buffer.numel())
+    _check("mxg_grouped_mlp_fwd_grouped", lib().mxg_grouped_mlp_fwd_grouped(ctypes.byref(a), _stream(stream)))
+    return y

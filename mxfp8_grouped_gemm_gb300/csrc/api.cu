@@ -29,6 +29,9 @@ constexpr bool kUsePairTiles = true;
 // sum_e roundup(m_e, A) <= roundup(T*k, A) + A*E.
 constexpr int kMlpAlign = kUsePairTiles ? 256 : 128;
 inline int64_t row_cap(int64_t T, int64_t k, int64_t E) { return align_up(T * k, kMlpAlign) + kMlpAlign * E; }
+// The standalone grouped quantiser's group count limit (its padding kernel is
+// one block of 1024 threads, each taking a run of groups).
+constexpr int kMaxQuantGroups = 1 << 20;
 
 // Whether a bf16-output GEMM with contraction length K sums each token's k
 // rows in its epilogue (the tile that stores a token's last row reads the other
@@ -205,6 +208,7 @@ const char* mxg_status_string(int status) {
     case MXG_ERR_EXPERT_ID: return "expert id outside [0, E)";
     case MXG_ERR_OFFSETS: return "group offsets not monotone, not 128-aligned or beyond capacity";
     case MXG_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
+    case MXG_ERR_INDEX: return "a row index outside the buffer it indexes";
     default: return "unknown status";
   }
 }
@@ -293,6 +297,76 @@ int mxg_mxfp8_quantize(const uint16_t* x, int rows, int cols, uint8_t* q_row, ui
   p.sf_col_rows = cols;
   p.layout = layout;
   return cuda_status(launch_quant(p, static_cast<cudaStream_t>(stream)));
+}
+
+size_t mxg_mxfp8_grouped_rows_capacity(int rows, int groups, int layout) {
+  if (rows <= 0 || groups <= 0 || groups > kMaxQuantGroups) return 0;
+  if (layout != MXG_LAYOUT_CANONICAL && layout != MXG_LAYOUT_MMA) return 0;
+  const int64_t al = layout == MXG_LAYOUT_MMA ? 128 : 32;
+  const int64_t cap = align_up(rows, al) + al * groups;
+  return cap > INT32_MAX ? 0 : static_cast<size_t>(cap);
+}
+
+int mxg_mxfp8_quantize_grouped(const uint16_t* x, int rows, int cols, const int32_t* group_offsets, int groups,
+                               int32_t* padded_offsets, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                               uint8_t* s_col, int layout, int32_t* dev_status, void* stream) {
+  if (!x || !group_offsets || !padded_offsets || !dev_status || rows <= 0 || cols <= 0 || groups <= 0)
+    return MXG_ERR_ARG;
+  if (layout != MXG_LAYOUT_CANONICAL && layout != MXG_LAYOUT_MMA) return MXG_ERR_ARG;
+  if ((q_row == nullptr) != (s_row == nullptr) || (q_col == nullptr) != (s_col == nullptr)) return MXG_ERR_ARG;
+  if (!q_row && !q_col) return MXG_ERR_ARG;
+  if (cols % 128 || groups > kMaxQuantGroups) return MXG_ERR_SHAPE;
+  const int64_t cap = static_cast<int64_t>(mxg_mxfp8_grouped_rows_capacity(rows, groups, layout));
+  if (cap == 0) return MXG_ERR_SHAPE;
+  if (!aligned32(x) || !aligned32(group_offsets) || !aligned32(padded_offsets) || (q_row && !aligned32(q_row)) ||
+      (q_col && !aligned32(q_col)))
+    return MXG_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int al = layout == MXG_LAYOUT_MMA ? 128 : 32;
+  MXG_TRY(launch_group_pad(group_offsets, groups, rows, al, cap, padded_offsets, dev_status, s));
+  QuantParams p{};
+  p.x = x;
+  p.ld_x = cols;
+  p.src_div = 1;
+  p.rows = static_cast<int32_t>(cap);
+  p.cols = cols;
+  p.batch = 1;
+  p.rows_valid = padded_offsets + groups;
+  p.grp_off = group_offsets;
+  p.grp_poff = padded_offsets;
+  p.groups = groups;
+  p.q_row = q_row;
+  p.s_row = s_row;
+  p.sf_row_rows = cap;
+  p.q_col = q_col;
+  p.s_col = s_col;
+  p.ld_col = cap;
+  p.sf_col_rows = cols;
+  p.layout = layout;
+  return cuda_status(launch_quant(p, s));
+}
+
+int mxg_gather_rows(const void* src, int64_t src_rows, int64_t row_bytes, const int32_t* index, int div,
+                    int64_t rows, void* dst, int32_t* dev_status, void* stream) {
+  if (!src || !index || !dst || !dev_status || src_rows <= 0 || row_bytes <= 0 || div <= 0 || rows <= 0)
+    return MXG_ERR_ARG;
+  if (row_bytes % 4) return MXG_ERR_SHAPE;
+  if (src_rows > static_cast<int64_t>(INT32_MAX) * div || rows > INT32_MAX) return MXG_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(index) |
+       reinterpret_cast<uintptr_t>(dev_status)) & 3u)
+    return MXG_ERR_ALIGN;
+  return cuda_status(launch_gather_rows(src, src_rows, row_bytes, index, div, rows, dst, dev_status,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int mxg_combine(const uint16_t* rows, int64_t src_rows, const int32_t* row_of_src, int T, int k, int H, uint16_t* y,
+                int32_t* dev_status, void* stream) {
+  if (!rows || !row_of_src || !y || !dev_status || src_rows <= 0 || T <= 0 || k <= 0 || H <= 0) return MXG_ERR_ARG;
+  if (H % 8 || k > 32) return MXG_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(rows) | reinterpret_cast<uintptr_t>(y)) & 15u) return MXG_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(row_of_src) | reinterpret_cast<uintptr_t>(dev_status)) & 3u) return MXG_ERR_ALIGN;
+  return cuda_status(launch_combine(rows, row_of_src, T, k, H, y, static_cast<cudaStream_t>(stream), src_rows,
+                                    dev_status));
 }
 
 int mxg_grouped_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
@@ -845,6 +919,58 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
 }
 
 int mxg_grouped_mlp_bwd(const mxg_mlp_bwd_args* A, void* stream) { return bwd_impl(A, -1, stream); }
+
+// Pre-grouped tokens: the layer with T = R rows, k = 1 and each row's expert
+// given by split_sizes.  The rows are already in expert order, so the
+// permute's stable counting sort leaves them in place; the k = 1 combine is
+// the scatter of each row back to its own position.
+static int64_t grouped_tail(int64_t R, int64_t E) { return align_up(4 * R, kAlign) + align_up(4 * E, kAlign); }
+
+size_t mxg_mlp_grouped_saved_bytes(int R, int H, int I, int E) { return mxg_mlp_saved_bytes(R, H, I, E, 1); }
+
+size_t mxg_mlp_grouped_workspace_bytes(int R, int H, int I, int E) {
+  if (!mlp_shape_ok(R, H, I, E, 1)) return 0;
+  return static_cast<size_t>(Plan(R, H, I, E, 1).ws_bytes() + grouped_tail(R, E));
+}
+
+int mxg_grouped_mlp_fwd_grouped(const mxg_mlp_grouped_fwd_args* G, void* stream) {
+  if (!G) return MXG_ERR_ARG;
+  const int R = G->R, H = G->H, I = G->I, E = G->E;
+  if (R <= 0 || H <= 0 || I <= 0 || E <= 0) return MXG_ERR_ARG;
+  if (!mlp_shape_ok(R, H, I, E, 1)) return MXG_ERR_SHAPE;
+  if (!G->split_sizes || !G->workspace || !G->dev_status) return MXG_ERR_ARG;
+  if (!aligned32(G->split_sizes) || !aligned32(G->workspace)) return MXG_ERR_ALIGN;
+  const Plan pl(R, H, I, E, 1);
+  if (G->workspace_bytes < static_cast<uint64_t>(pl.ws_bytes() + grouped_tail(R, E))) return MXG_ERR_WORKSPACE;
+  int32_t* ids = at<int32_t>(G->workspace, pl.ws_bytes());
+  int32_t* split_out = at<int32_t>(G->workspace, pl.ws_bytes() + align_up(4 * static_cast<int64_t>(R), kAlign));
+  mxg_mlp_fwd_args A{};
+  A.T = R;
+  A.H = H;
+  A.I = I;
+  A.E = E;
+  A.k = 1;
+  A.x = G->x;
+  A.ids = ids;
+  A.probs = G->probs;
+  A.w_gate_up = G->w_gate_up;
+  A.w_down = G->w_down;
+  A.y = G->y;
+  A.split_sizes = split_out;
+  A.saved = G->saved;
+  A.saved_bytes = G->saved_bytes;
+  A.workspace = G->workspace;
+  A.workspace_bytes = static_cast<uint64_t>(pl.ws_bytes());
+  A.save_for_backward = G->save_for_backward;
+  A.dev_status = G->dev_status;
+  A.weight_cache = G->weight_cache;
+  A.weight_cache_bytes = G->weight_cache_bytes;
+  // every other argument is checked by the forward before anything is launched
+  const int pre = fwd_impl(&A, MXG_FWD_NUM_STAGES, stream);
+  if (pre != MXG_OK) return pre;
+  MXG_TRY(launch_expand_splits(G->split_sizes, E, R, ids, G->dev_status, static_cast<cudaStream_t>(stream)));
+  return fwd_impl(&A, -1, stream);
+}
 
 int mxg_grouped_mlp_bwd_stage(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   if (stage < 0 || stage >= MXG_BWD_NUM_STAGES) return MXG_ERR_ARG;

@@ -15,7 +15,8 @@ namespace {
 // One thread per 8 consecutive columns (16-byte vectors) of one token.
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ src,
                                                       const int32_t* __restrict__ prow_of_src, int T, int k,
-                                                      int H, uint16_t* __restrict__ out) {
+                                                      int H, uint16_t* __restrict__ out, int64_t src_rows,
+                                                      int32_t* status) {
   const int vecs = H >> 3;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<int64_t>(T) * vecs) return;
@@ -27,6 +28,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   for (int j = 0; j < k; ++j) {
     const int pr = prow_of_src[static_cast<int64_t>(t) * k + j];
     if (pr < 0) continue;
+    if (pr >= src_rows) {
+      if (v == 0) report(status, MXG_ERR_INDEX);
+      continue;
+    }
     const uint4 q = *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(pr) * H + v * 8);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -59,11 +64,11 @@ __global__ void __launch_bounds__(256) dprob_kernel(const float* __restrict__ pa
 }  // namespace
 
 cudaError_t launch_combine(const uint16_t* src, const int32_t* prow_of_src, int T, int k, int H, uint16_t* out,
-                           cudaStream_t s) {
+                           cudaStream_t s, int64_t src_rows, int32_t* status) {
   const int64_t n = static_cast<int64_t>(T) * (H / 8);
   const int64_t grid = (n + 255) / 256;
   if (grid == 0) return cudaSuccess;
-  combine_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(src, prow_of_src, T, k, H, out);
+  combine_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(src, prow_of_src, T, k, H, out, src_rows, status);
   count_launch();
   return cudaGetLastError();
 }

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 namespace mxg {
@@ -39,8 +40,23 @@ struct QuantParams {
   const float* pt_amax;
   const int32_t* pt_group_off;
   int32_t pt_groups;
+  // grouped rows without a row map (the standalone grouped quantiser): padded
+  // row p of group g (grp_poff[g] <= p < grp_poff[g+1]) reads source row
+  // grp_off[g] + (p - grp_poff[g]) while that is below grp_off[g+1], else it
+  // is a zero padding row; set rows_valid = grp_poff + groups
+  const int32_t* grp_off;
+  const int32_t* grp_poff;
+  int32_t groups;
 };
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
+
+// Padded layout of grouped rows: poff[g] = sum over g' < g of the group sizes
+// off[g'+1] - off[g'] each rounded up to `align`.  off must start at 0, be
+// monotone and end at `rows`, and the padded total must fit `cap` rows;
+// otherwise MXG_ERR_OFFSETS goes to status and poff is all zeros (nothing is
+// then quantised).
+cudaError_t launch_group_pad(const int32_t* off, int groups, int rows, int align, int64_t cap, int32_t* poff,
+                             int32_t* status, cudaStream_t s);
 
 // Largest magnitude of each tensor of a bf16 matrix batch (per-tensor FP8):
 // rows optionally gathered like QuantParams; a tensor is a row group of
@@ -84,8 +100,20 @@ int permute_num_blocks(int R);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ combine
+// y[t] = sum_j src[prow_of_src[t*k + j]] (fp32 in slot order, one bf16
+// rounding).  Negative entries are skipped; entries >= src_rows are skipped
+// and reported as MXG_ERR_INDEX through status (nullable).
 cudaError_t launch_combine(const uint16_t* src, const int32_t* prow_of_src, int T, int k, int H, uint16_t* out,
-                           cudaStream_t s);
+                           cudaStream_t s, int64_t src_rows = INT64_MAX, int32_t* status = nullptr);
+// dst row r = src row index[r] / div (rows of row_bytes bytes, a multiple of
+// 4); an index outside [0, src_rows * div) gives a zero row and MXG_ERR_INDEX.
+cudaError_t launch_gather_rows(const void* src, int64_t src_rows, int64_t row_bytes, const int32_t* index, int div,
+                               int64_t rows, void* dst, int32_t* status, cudaStream_t s);
+// ids[r] = the group of row r, from split sizes [E] (rows of group e follow
+// those of e - 1); sizes that are negative or do not sum to R give
+// MXG_ERR_OFFSETS and ids -1 for the rows no group covers.
+cudaError_t launch_expand_splits(const int32_t* split_sizes, int E, int64_t R, int32_t* ids, int32_t* status,
+                                 cudaStream_t s);
 cudaError_t launch_dprob(const float* part, int ld, const int32_t* prow_of_src, int R, float* dprobs,
                          cudaStream_t s);
 

@@ -163,7 +163,7 @@ constexpr int kTilesPerCta = 4;      // 32-row tiles walked by one CTA
 // Stage one 32 x 128 tile (gathered rows: s_src holds the source row of each
 // of the CTA's rows, -1 for padding) into shared memory asynchronously.
 __device__ __forceinline__ void stage_tile(const QuantParams& P, const uint16_t* xb, int p0, int c0, uint16_t* buf,
-                                           int tid, const int* s_src, int first) {
+                                           int tid, const int* s_src, int first, bool gathered) {
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const int i = tid + it * 128;
@@ -171,7 +171,7 @@ __device__ __forceinline__ void stage_tile(const QuantParams& P, const uint16_t*
     const int pp = p0 + rr;
     int64_t srow = pp;
     bool zero = false;
-    if (P.src_rows != nullptr) {
+    if (gathered) {
       const int f = s_src[pp - first];
       if (f < 0) zero = true;
       else srow = f;
@@ -201,19 +201,36 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
   if (ntiles <= 0) return;
   const uint16_t* xb = P.x + static_cast<int64_t>(b) * P.x_batch_stride;
   // gathered rows: the CTA's 128 source rows resolved once (one load and one
-  // division per row) instead of in every staging pass
+  // division per row, or a search of the group offsets) instead of in every
+  // staging pass
   __shared__ int s_src[kTilesPerCta * kRows];
-  if (P.src_rows != nullptr) {
-    const int f = first + tid < P.rows ? P.src_rows[first + tid] : -1;
-    s_src[tid] = f < 0 ? -1 : f / P.src_div;
+  const bool gathered = P.src_rows != nullptr || P.grp_off != nullptr;
+  if (gathered) {
+    const int p = first + tid;
+    int f = -1;
+    if (P.src_rows != nullptr) {
+      const int v = p < P.rows ? P.src_rows[p] : -1;
+      f = v < 0 ? -1 : v / P.src_div;
+    } else if (p < limit) {
+      // the group holding padded row p: the last g with grp_poff[g] <= p
+      int lo = 0, hi = P.groups - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.grp_poff[mid] <= p) lo = mid;
+        else hi = mid - 1;
+      }
+      const int src = P.grp_off[lo] + (p - P.grp_poff[lo]);
+      f = src < P.grp_off[lo + 1] ? src : -1;
+    }
+    s_src[tid] = f;
     __syncthreads();
   }
 
-  stage_tile(P, xb, first, c0, tile[0], tid, s_src, first);
+  stage_tile(P, xb, first, c0, tile[0], tid, s_src, first, gathered);
   for (int t = 0; t < ntiles; ++t) {
     const int p0 = first + t * kRows;
     if (t + 1 < ntiles) {
-      stage_tile(P, xb, p0 + kRows, c0, tile[(t + 1) & 1], tid, s_src, first);
+      stage_tile(P, xb, p0 + kRows, c0, tile[(t + 1) & 1], tid, s_src, first, gathered);
       asm volatile("cp.async.wait_group 1;" ::: "memory");
     } else {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -323,7 +340,56 @@ __global__ void __launch_bounds__(256) amax_kernel(const AmaxParams P) {
   }
 }
 
+// Padded offsets of grouped rows, one block: every thread takes a contiguous
+// run of groups, checks them, sums their padded sizes; a block-wide scan of
+// the run totals gives each run's start.
+__global__ void __launch_bounds__(1024) group_pad_kernel(const int32_t* __restrict__ off, int groups, int rows,
+                                                         int align, int64_t cap, int32_t* __restrict__ poff,
+                                                         int32_t* status) {
+  __shared__ int64_t s_tot[1024];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_bad = (off[0] != 0 || off[groups] != rows) ? 1 : 0;
+  const int per = (groups + blockDim.x - 1) / blockDim.x;
+  const int g0 = min(groups, tid * per), g1 = min(groups, g0 + per);
+  int64_t tot = 0;
+  bool bad = false;
+  for (int g = g0; g < g1; ++g) {
+    const int a = off[g], b = off[g + 1];
+    if (b < a) bad = true;
+    tot += (static_cast<int64_t>(b - a) + align - 1) / align * align;
+  }
+  s_tot[tid] = tot;
+  __syncthreads();
+  if (bad) s_bad = 1;
+  for (int d = 1; d < static_cast<int>(blockDim.x); d <<= 1) {      // inclusive scan of the run totals
+    const int64_t v = tid >= d ? s_tot[tid - d] : 0;
+    __syncthreads();
+    s_tot[tid] += v;
+    __syncthreads();
+  }
+  const bool fail = s_bad != 0 || s_tot[blockDim.x - 1] > cap;
+  if (fail) {
+    for (int g = tid; g <= groups; g += blockDim.x) poff[g] = 0;
+    if (tid == 0) report(status, MXG_ERR_OFFSETS);
+    return;
+  }
+  int64_t run = s_tot[tid] - tot;
+  for (int g = g0; g < g1; ++g) {
+    poff[g] = static_cast<int32_t>(run);
+    run += (static_cast<int64_t>(off[g + 1] - off[g]) + align - 1) / align * align;
+  }
+  if (tid == blockDim.x - 1) poff[groups] = static_cast<int32_t>(s_tot[tid]);
+}
+
 }  // namespace
+
+cudaError_t launch_group_pad(const int32_t* off, int groups, int rows, int align, int64_t cap, int32_t* poff,
+                             int32_t* status, cudaStream_t s) {
+  group_pad_kernel<<<1, 1024, 0, s>>>(off, groups, rows, align, cap, poff, status);
+  count_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_amax(const AmaxParams& p, cudaStream_t s) {
   dim3 grid((p.rows + 31) / 32, p.cols / 256, p.batch);

@@ -115,3 +115,57 @@ class GroupedMLP:
 
     def padded_rows_capacity(self) -> int:
         return _lib.mxg_mlp_row_capacity(self.T, self.k, self.E)
+
+
+class GroupedExperts:
+    """The expert MLP on rows that arrive already grouped by expert (the
+    GroupedLinear call with split_sizes: an expert-parallel dispatcher's
+    output, or rows the caller permuted).  Buffers are sized for up to
+    ``max_rows`` rows; each call passes its own row count."""
+
+    def __init__(self, max_rows: int, H: int, I: int, E: int, device="cuda"):
+        self.R_max, self.H, self.I, self.E = max_rows, H, I, E
+        self.device = torch.device(device)
+        saved = _lib.mxg_mlp_grouped_saved_bytes(max_rows, H, I, E)
+        ws = _lib.mxg_mlp_grouped_workspace_bytes(max_rows, H, I, E)
+        if saved == 0 or ws == 0:
+            raise ValueError(f"unsupported grouped shape R={max_rows} H={H} I={I} E={E}")
+        self.saved = torch.empty(saved, dtype=torch.uint8, device=self.device)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.weight_cache = None
+        self._R = 0
+        self._cached = False
+
+    def quantize_weights(self, w_gate_up, w_down, stream=None):
+        self.weight_cache = _lib.mxg_mlp_quantize_weights(w_gate_up, w_down, self.weight_cache, stream=stream)
+        return self.weight_cache
+
+    def forward(self, x, split_sizes, probs, w_gate_up=None, w_down=None, save_for_backward=True, y=None,
+                stream=None):
+        """x bf16 [R, H] grouped by expert, split_sizes int32 [E] (device),
+        probs fp32 [R] -> per-row outputs y [R, H]."""
+        R = x.shape[0]
+        if R > self.R_max:
+            raise ValueError(f"{R} rows exceed the buffers' {self.R_max}")
+        cached = w_gate_up is None and w_down is None
+        if cached and self.weight_cache is None:
+            raise ValueError("no weights given and no weight cache: call quantize_weights first")
+        self._R, self._cached = R, cached
+        return _lib.mxg_grouped_mlp_fwd_grouped(x, split_sizes, probs.reshape(R), w_gate_up, w_down, self.saved,
+                                                self.workspace, self.dev_status, y=y,
+                                                save_for_backward=save_for_backward,
+                                                weight_cache=self.weight_cache if cached else None, stream=stream)
+
+    def backward(self, dy, dx=None, dw_gate_up=None, dw_down=None, dprobs=None, main_grad=None, stream=None):
+        """dy bf16 [R, H] (per row) -> dx [R, H], dW_gate_up, dW_down, dprobs [R, 1]."""
+        R = dy.shape[0]
+        if R != self._R:
+            raise ValueError("backward rows differ from the forward's")
+        return _lib.mxg_grouped_mlp_bwd(dy, self.saved, self.workspace, self.dev_status, self.E, self.I, 1, dx=dx,
+                                        dw_gate_up=dw_gate_up, dw_down=dw_down, dprobs=dprobs, stream=stream,
+                                        weight_cache=self.weight_cache if self._cached else None,
+                                        main_grad=main_grad)
+
+    def status(self) -> int:
+        return int(self.dev_status.item())

@@ -36,28 +36,6 @@ def mma_to_canonical(s: torch.Tensor, rows: int, nblocks: int) -> np.ndarray:
     return flat[mma_index(rows, nblocks)]
 
 
-def assert_rms_close(a, r, frac=2e-2, name="", guard=0.5):
-    """The stated tolerance read as a relative RMS error: ||a - r||_2 <= frac *
-    ||r||_2 (the error is at most `frac` of the output RMS).  A per-element
-    guard |a - r| <= guard * RMS(r) + 2^-7 |r| catches localised faults (a
-    wrong row or tile) that an RMS can hide; it sits above the largest single
-    re-quantisation flip of a heavy-tailed product (one E4M3 step of the largest
-    dGU value of an expert times a large x, measured up to ~0.35 RMS on few-token
-    experts).  Returns (max|a-r| / RMS, rel RMS)."""
-    a = np.asarray(a, dtype=np.float64)
-    r = np.asarray(r, dtype=np.float64)
-    if r.size == 0:
-        return 0.0, 0.0
-    rms = float(np.sqrt(np.mean(r * r)))
-    diff = np.abs(a - r)
-    err = float(np.max(diff))
-    rel_rms = float(np.sqrt(np.mean(diff ** 2)) / rms) if rms > 0 else float(np.sqrt(np.mean(diff ** 2)))
-    assert rel_rms <= frac, f"{name}: relative RMS error {rel_rms:.4g} > {frac} (max|a-r|/RMS {err / rms:.3g})"
-    bad = diff > guard * rms + 2.0 ** -7 * np.abs(r)
-    assert not bad.any(), f"{name}: {int(bad.sum())} elements beyond the per-element guard (max|a-r|/RMS {err / rms:.3g})"
-    return (err / rms if rms else 0.0), rel_rms
-
-
 def assert_rel_close(a, r, tol=1e-2, floor=1.0, name=""):
     a = np.asarray(a, dtype=np.float64)
     r = np.asarray(r, dtype=np.float64)

@@ -22,11 +22,19 @@ to a different E4M3 code only if v lies within delta |v| of a rounding
 midpoint.  Midpoints are one grid step u(v) apart and u(v) >= 2^-4 |v| for
 normal E4M3 codes, so (v spread evenly within its grid cell) the chance of a
 flip is p <= 2 delta |v| / u(v) <= 32 delta.  A flip moves the dequantised
-value by one step u.  For an output C = sum_n A_n B_n whose A is re-quantised,
-the flips add independent terms +-u_n B_n, so
-    sigma^2 <= p * sum_n u_n^2 B_n^2,
-computed from the oracle's own operands and grid steps; Z = 6 (a normal tail
-of 2e-9 per element).
+value by one step u.  For an output C = sum_n A_n B_n (n over a contraction
+of length K) whose A is re-quantised, the flips add independent terms
++-u_n B_n.  The expected number of flips per output is lambda = p K, and:
+  * lambda >= 50: their sum is close to normal, with
+        sigma^2 <= p * sum_n u_n^2 B_n^2,
+    computed from the oracle's own operands and grid steps; the term is
+    Z * sigma with Z = 6 (a normal tail of 2e-9 per element);
+  * lambda < 50 (rare flips, e.g. of h, whose delta is tiny): at most
+    n(lambda) flips happen, n the count a Poisson(lambda) variable (whose
+    tail bounds the binomial's) exceeds with chance below 1e-10, and
+    each moves C by at most max_n u_n * max_n |B_n|; the term is their
+    product.  (One flip of h moves a dW_down element by ~3 % of its RMS: a
+    normal 6 sigma with p ~ 3e-5 would understate that.)
 
 delta per re-quantised tensor:
   h   : the GPU computes h = p SiLU(g) u in fp32 from fp32 accumulators; a
@@ -86,6 +94,33 @@ def mx_steps_group_columns(a: np.ndarray) -> np.ndarray:
 def flip_sigma2(u: np.ndarray, b: np.ndarray, delta: float) -> np.ndarray:
     """sigma^2 of C = A B^T (A [m, K] re-quantised with steps u, B [N, K])."""
     return flip_prob(delta) * ((u * u) @ (b * b).T)
+
+
+LAMBDA_NORMAL = 50.0
+TAIL = 1e-10
+
+
+def rare_flips(lam: float) -> int:
+    """Smallest n with P(Poisson(lam) > n) <= 1e-10: more than n flips in one
+    output has a negligible chance."""
+    if lam <= 0:
+        return 0
+    term = np.exp(-lam)            # P(N = 0)
+    cdf = term
+    n = 0
+    while 1.0 - cdf > TAIL:
+        n += 1
+        term *= lam / n
+        cdf += term
+    return n
+
+
+def flip_term(var: np.ndarray, m_outer: np.ndarray, lam: float) -> np.ndarray:
+    """Per-element flip allowance: Z * sqrt(var) when lam >= 50 flips are
+    expected, else n(lam) single-flip maxima (see the module docstring)."""
+    if lam >= LAMBDA_NORMAL:
+        return Z * np.sqrt(var)
+    return rare_flips(lam) * m_outer
 
 
 def storage(r: np.ndarray, rows_abs_sum: np.ndarray | None = None) -> np.ndarray:
@@ -148,7 +183,10 @@ def write_record(rec: dict):
 #     most 2 delta_h / 2^-8 = 2^-11 and such a difference flips the E4M3 code
 #     with chance at most 32 * 2^-7, so p <= 2^-13.  dGU: a relative
 #     perturbation of delta_dGU before and one bf16 unit (2^-8) after the
-#     bf16 rounding, delta = delta_dGU + 2^-8.
+#     bf16 rounding, delta = delta_dGU + 2^-8.  The tensor's one scale moves
+#     by a factor two when its largest magnitude, perturbed by delta, can
+#     cross a power of two; for such a tensor every code may change, by at
+#     most one step of the coarser grid: p = 1 and steps doubled.
 
 DELTA_BF16_H = 2.0 ** -8
 DELTA_BF16_DGU = 2.0 ** -8 + 3 * 2.0 ** -9
@@ -168,23 +206,37 @@ def fp8_steps(v: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, np.maximum(fl, mx.E4M3_EMIN) - mx.E4M3_MBITS + e)
 
 
-def _sig2(mode: str, which: str, a: np.ndarray, b: np.ndarray, col: bool) -> np.ndarray:
-    """sigma^2 of a GEMM over the re-quantised (or re-rounded) operand a [m, K]
-    against b [N, K] (col: a and b are [tokens, .] and the GEMM contracts the
-    tokens, giving [a-cols, b-cols])."""
-    if mode == "mxfp8":
-        delta = DELTA_H if which == "h" else DELTA_DGU
-        u = mx_steps_group_columns(a) if col else mx_steps(a)
-        p = flip_prob(delta)
-        var = p * u * u
-    elif mode == "fp8":
-        u = fp8_steps(moe.bf16_round(a))
-        p = P_FP8_H if which == "h" else flip_prob(DELTA_FP8_DGU)
-        var = p * u * u
-    else:
+def flip_allowance(mode: str, which: str, a: np.ndarray, b: np.ndarray, col: bool) -> np.ndarray:
+    """Per-element flip (or rounding) allowance of a GEMM over the re-quantised
+    (or re-rounded) operand a [m, K] against b [N, K] (col: a and b are
+    [tokens, .] and the GEMM contracts the tokens, giving [a-cols, b-cols])."""
+    K = a.shape[0] if col else a.shape[1]
+    if mode == "bf16":
+        # every element rounded: an error uniform within +-delta |v|, no flips
         delta = DELTA_BF16_H if which == "h" else DELTA_BF16_DGU
         var = (delta * a) ** 2 / 3.0
-    return var.T @ (b * b) if col else var @ (b * b).T
+        return Z * np.sqrt(var.T @ (b * b) if col else var @ (b * b).T)
+    if mode == "mxfp8":
+        u = mx_steps_group_columns(a) if col else mx_steps(a)
+        p = flip_prob(DELTA_H if which == "h" else DELTA_DGU)
+    else:
+        v = moe.bf16_round(a)
+        u = fp8_steps(v)
+        p = P_FP8_H if which == "h" else flip_prob(DELTA_FP8_DGU)
+        delta = DELTA_H if which == "h" else DELTA_FP8_DGU
+        amax = float(np.max(np.abs(v))) if v.size else 0.0
+        if amax > 0 and np.floor(np.log2(amax * (1 - delta))) != np.floor(np.log2(amax * (1 + delta))):
+            p, u = 1.0, 2.0 * u                       # the scale itself may differ by a factor two
+    lam = p * K
+    if lam >= LAMBDA_NORMAL:
+        var = p * u * u
+        return flip_term(var.T @ (b * b) if col else var @ (b * b).T, None, lam)
+    ab = np.abs(b)
+    if col:
+        m_outer = np.outer(u.max(axis=0), ab.max(axis=0))
+    else:
+        m_outer = np.outer(u.max(axis=1), ab.max(axis=1))
+    return flip_term(None, m_outer, lam)
 
 
 def full_bounds(ctx: dict, g: dict | None, weights: dict, dy: np.ndarray | None = None, mode: str = "mxfp8",
@@ -205,12 +257,12 @@ def full_bounds(ctx: dict, g: dict | None, weights: dict, dy: np.ndarray | None 
     quantised = mode != "bf16"
     col_in = (lambda v: mx.fake_quant_group_columns(v)) if mode == "mxfp8" else \
         ((lambda v: moe._fq(v, "fp8")) if mode == "fp8" else (lambda v: np.asarray(v, dtype=np.float64)))
-    s2_y = np.zeros((R, H))
+    f_y = np.zeros((R, H))
     if bwd:
-        s2_dx = np.zeros((R, H))
+        f_dx = np.zeros((R, H))
         dp_sig = np.zeros(R)
-        s2_dwgu = np.zeros((E, 2 * I, H))
-        s2_dwd = np.zeros((E, H, I))
+        f_dwgu = np.zeros((E, 2 * I, H))
+        f_dwd = np.zeros((E, H, I))
     tok = perm["src_of_row"] // k
     dp_delta = DELTA_DGU if quantised else 3 * 2.0 ** -9
     for e in range(E):
@@ -219,26 +271,24 @@ def full_bounds(ctx: dict, g: dict | None, weights: dict, dy: np.ndarray | None 
             continue
         w = weights[e]
         h = ctx["h"][a:b]
-        s2_y[a:b] = _sig2(mode, "h", h, w["wd"], False)
+        f_y[a:b] = flip_allowance(mode, "h", h, w["wd"], False)
         if not bwd:
             continue
         dgu, x_perm = g["dgu"][a:b], ctx["x_perm"][a:b]
-        s2_dx[a:b] = _sig2(mode, "dgu", dgu, w["wguT"], False)
+        f_dx[a:b] = flip_allowance(mode, "dgu", dgu, w["wguT"], False)
         gu = ctx["gu"][a:b]
         _, _, terms = moe.dscaled_swiglu(g["dh"][a:b], gu[:, :I], gu[:, I:], ctx["p_perm"][a:b, None])
         dp_sig[a:b] = dp_delta * np.sqrt(np.sum(terms * terms, axis=1))
-        s2_dwgu[e] = _sig2(mode, "dgu", dgu, col_in(x_perm), True)
+        f_dwgu[e] = flip_allowance(mode, "dgu", dgu, col_in(x_perm), True)
         dyc = col_in(np.asarray(dy, dtype=np.float64)[tok[a:b]])
-        s2_dwd[e] = _sig2(mode, "h", h, dyc, True).T
+        f_dwd[e] = flip_allowance(mode, "h", h, dyc, True).T
     row = perm["row_of_src"].reshape(T, k)
     y_rows_abs = sum(np.abs(ctx["y_perm"][row[:, j]]) for j in range(k))
-    sig_y = np.sqrt(sum(s2_y[row[:, j]] for j in range(k)))
-    out = {"y": bound(ctx["y"], storage(ctx["y"], y_rows_abs) + Z * sig_y, frac)}
+    out = {"y": bound(ctx["y"], storage(ctx["y"], y_rows_abs) + sum(f_y[row[:, j]] for j in range(k)), frac)}
     if bwd:
         dx_rows_abs = sum(np.abs(g["dx_perm"][row[:, j]]) for j in range(k))
-        sig_dx = np.sqrt(sum(s2_dx[row[:, j]] for j in range(k)))
-        out["dx"] = bound(g["dx"], storage(g["dx"], dx_rows_abs) + Z * sig_dx, frac)
+        out["dx"] = bound(g["dx"], storage(g["dx"], dx_rows_abs) + sum(f_dx[row[:, j]] for j in range(k)), frac)
         out["dprobs"] = bound(g["dprobs"], Z * dp_sig[row], frac)
-        out["dw_gate_up"] = bound(g["dw_gate_up"], storage(g["dw_gate_up"]) + Z * np.sqrt(s2_dwgu), frac)
-        out["dw_down"] = bound(g["dw_down"], storage(g["dw_down"]) + Z * np.sqrt(s2_dwd), frac)
+        out["dw_gate_up"] = bound(g["dw_gate_up"], storage(g["dw_gate_up"]) + f_dwgu, frac)
+        out["dw_down"] = bound(g["dw_down"], storage(g["dw_down"]) + f_dwd, frac)
     return out

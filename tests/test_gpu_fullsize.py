@@ -4,20 +4,29 @@ times: the whole route -> forward -> backward runs on the GPU; the oracle
 checks the integer outputs in full and the floating-point outputs on seeded
 samples it can evaluate exactly (oracle.sampled):
   * ids, split_sizes, padded offsets and the padded row map: bit-exact, all;
-  * gate-up outputs of the sampled tokens' rows: 1e-2 relative (floor 1);
-  * y, dx, dprobs of the sampled tokens and sampled columns of dW_down / rows of
-    dW_gate_up: error at most 2e-2 of the reference RMS (relative RMS error over
-    the sample, plus the per-element guard);
-  * dW of every empty expert: exactly zero."""
+  * sampled rows: for every expert with tokens, 8 of its rows, half of them in
+    the expert's last 256-row tile (the ragged tile when the split is not a
+    multiple of 256); the tokens owning them bring all their k rows;
+  * gate-up outputs of those rows: 1e-2 relative (floor 1);
+  * y, dx, dprobs of those tokens and, for every expert with tokens, sampled
+    columns of dW_down and rows of dW_gate_up: relative RMS error at most 2e-2
+    over the sample and every element within the bound tests/parity_bounds.py
+    derives (the RMS being the sample's);
+  * dW of every empty expert: exactly zero.
+The oracle holds one expert's weights at a time."""
 import numpy as np
 import pytest
 import torch
 
+import parity_bounds as pb
 import synthetic
-from gpu_helpers import assert_rel_close, assert_rms_close, np_, require_gpu
+from gpu_helpers import assert_rel_close, np_, require_gpu
 from oracle import moe, sampled
 
 pytestmark = pytest.mark.gpu
+
+ROWS_PER_EXPERT = 8
+DW_SLICES_PER_EXPERT = 8
 
 
 @pytest.fixture(scope="module")
@@ -28,17 +37,18 @@ def pool():
     p.close()
 
 
-def _pick(wl, ids, split, rng):
-    """Sampled tokens and the experts their rows use."""
-    if wl.k == 2:
-        # tokens routed to the two most loaded experts (both of their rows)
-        S = np.argsort(-split, kind="stable")[:2]
-        cand = np.nonzero(np.isin(ids[:, 0], S) & np.isin(ids[:, 1], S))[0]
-        tokens = np.sort(rng.choice(cand, size=min(24, cand.size), replace=False))
-    else:
-        tokens = np.sort(rng.choice(wl.T, size=6, replace=False))
-    experts = np.unique(ids[tokens])
-    return tokens, experts
+def _pick_rows(perm, split, align, rng):
+    """Permuted rows to sample: per non-empty expert, half from its last tile."""
+    rows = []
+    for e in np.nonzero(split > 0)[0]:
+        a, b = int(perm["offsets"][e]), int(perm["offsets"][e + 1])
+        last0 = a + ((b - a - 1) // align) * align
+        n_last = min(ROWS_PER_EXPERT // 2, b - last0)
+        last = rng.choice(np.arange(last0, b), size=n_last, replace=False)
+        rest = np.setdiff1d(np.arange(a, b), last)
+        rows.append(last)
+        rows.append(rng.choice(rest, size=min(ROWS_PER_EXPERT - n_last, rest.size), replace=False))
+    return np.sort(np.concatenate(rows))
 
 
 @pytest.mark.parametrize("name", ["mixtral", "skew", "fine"])
@@ -64,7 +74,8 @@ def test_fullsize_sampled(name, pool):
     # --- integer outputs, in full
     ids, probs = moe.route_topk(inp["logits"].numpy(), k)
     assert np.array_equal(np_(ids_g), ids)
-    perm = moe.permute(ids, E, pad=m.mxg_mlp_group_align())
+    align = m.mxg_mlp_group_align()
+    perm = moe.permute(ids, E, pad=align)
     split = perm["split_sizes"]
     assert np.array_equal(np_(layer.split_sizes), split)
     assert np.array_equal(np_(poff_g), perm["padded_offsets"])
@@ -73,35 +84,77 @@ def test_fullsize_sampled(name, pool):
     prow = perm["padded_offsets"][expert_of_row[rows]] + (rows - perm["offsets"][expert_of_row[rows]])
     assert np.array_equal(np_(prow_g), prow)
 
-    # --- sampled floating-point outputs
+    # --- sampled tokens: every non-empty expert, its last tile included
     rng = np.random.default_rng(4242 + wl.index)
-    tokens, experts = _pick(wl, ids, split, rng)
-    W = {int(e): pool.expert_weights(inp["w_gate_up"][e], inp["w_down"][e]) for e in experts}
+    tokens = np.unique(perm["src_of_row"][_pick_rows(perm, split, align, rng)] // k)
     x, dy = inp["x"].double().numpy(), inp["dy"].double().numpy()
-    s = sampled.rows_forward_backward(tokens, x, dy, probs, rows, expert_of_row, k, W)
-    tt = torch.from_numpy(tokens).cuda()
-    assert_rms_close(np_(layer.y[tt]), s["y"], 2e-2, f"{name} y")
-    assert_rms_close(np_(layer.dx[tt]), s["dx"], 2e-2, f"{name} dx")
-    assert_rms_close(np_(layer.dprobs[tt]), s["dprobs"], 2e-2, f"{name} dprobs")
-    # padded row of each permuted row r (the map above is indexed by flat index)
-    prow_of_row = perm["padded_offsets"][expert_of_row] + (np.arange(T * k) - perm["offsets"][expert_of_row])
-    pr = prow_of_row[s["rows"].reshape(-1)]
-    gu = np_(gu_g[torch.from_numpy(pr).cuda()])
-    assert_rel_close(gu, s["gu"].reshape(-1, 2 * I), tol=1e-2, floor=1.0, name=f"{name} gate-up")
-
     tok = perm["src_of_row"] // k
     p_perm = probs.reshape(-1)[perm["src_of_row"]]
-    for e in [int(v) for v in experts[:2] if split[v] > 0]:
-        a, b = perm["offsets"][e], perm["offsets"][e + 1]
-        xe, dye, pe = x[tok[a:b]], dy[tok[a:b]], p_perm[a:b]
-        cols = np.sort(rng.choice(I, size=12, replace=False))
-        ref = sampled.dw_down_columns(xe, dye, pe, inp["w_gate_up"][e].double().numpy(), cols)
-        got = np_(layer.dw_down[e][:, torch.from_numpy(cols).cuda()])
-        assert_rms_close(got, ref, 2e-2, f"{name} dW_down[{e}]")
-        rows_n = np.sort(np.concatenate([rng.choice(I, 6, replace=False), I + rng.choice(I, 6, replace=False)]))
-        ref = sampled.dw_gate_up_rows(xe, dye, pe, inp["w_gate_up"][e].double().numpy(),
-                                      inp["w_down"][e].double().numpy(), rows_n)
-        got = np_(layer.dw_gate_up[e][torch.from_numpy(rows_n).cuda()])
-        assert_rms_close(got, ref, 2e-2, f"{name} dW_gate_up[{e}]")
+    n = tokens.size
+    acc = {"y": np.zeros((n, H)), "dx": np.zeros((n, H)), "dprobs": np.zeros((n, k)), "gu": np.zeros((n, k, 2 * I))}
+    extra = {"y_rows": np.zeros((n, H)), "dx_rows": np.zeros((n, H)), "f_y": np.zeros((n, H)),
+             "f_dx": np.zeros((n, H)), "dp_sig": np.zeros((n, k))}
+    done = np.zeros((n, k), dtype=bool)
+    dwd_got, dwd_ref, dwd_extra = [], [], []
+    dwgu_got, dwgu_ref, dwgu_extra = [], [], []
+    for e in [int(v) for v in np.nonzero(split > 0)[0]]:
+        W = pool.expert_weights(inp["w_gate_up"][e], inp["w_down"][e])
+        s = sampled.rows_forward_backward(tokens, x, dy, probs, rows, expert_of_row, k, {e: W})
+        for key in acc:
+            acc[key] = acc[key] + s[key]
+        done |= s["done"]
+        for a, j in zip(*np.nonzero(s["done"])):
+            extra["y_rows"][a] += np.abs(s["y_rows"][a, j])
+            extra["dx_rows"][a] += np.abs(s["dx_rows"][a, j])
+            extra["f_y"][a] += pb.flip_allowance("mxfp8", "h", s["h"][a, j][None], W["wd"], False)[0]
+            extra["f_dx"][a] += pb.flip_allowance("mxfp8", "dgu", s["dgu"][a, j][None], W["wguT"], False)[0]
+            g_, u_ = s["gu"][a, j, :I], s["gu"][a, j, I:]
+            _, _, terms = moe.dscaled_swiglu(s["dh"][a, j], g_, u_, probs[tokens[a], j])
+            extra["dp_sig"][a, j] = pb.DELTA_DGU * np.sqrt(np.sum(terms * terms))
+        del W
+        # weight-gradient slices of this expert
+        a0, b0 = perm["offsets"][e], perm["offsets"][e + 1]
+        xe, dye, pe = x[tok[a0:b0]], dy[tok[a0:b0]], p_perm[a0:b0]
+        cols = np.sort(rng.choice(I, size=DW_SLICES_PER_EXPERT, replace=False))
+        ref, parts = sampled.dw_down_columns(xe, dye, pe, inp["w_gate_up"][e].double().numpy(), cols, parts=True)
+        dwd_ref.append(ref)
+        dwd_got.append(np_(layer.dw_down[e][:, torch.from_numpy(cols).cuda()]))
+        dwd_extra.append(pb.storage(ref) + pb.flip_allowance("mxfp8", "h", parts["h"], parts["dyc"], True).T)
+        half = DW_SLICES_PER_EXPERT // 2
+        rows_n = np.sort(np.concatenate([rng.choice(I, half, replace=False), I + rng.choice(I, half, replace=False)]))
+        ref, parts = sampled.dw_gate_up_rows(xe, dye, pe, inp["w_gate_up"][e].double().numpy(),
+                                             inp["w_down"][e].double().numpy(), rows_n, parts=True)
+        dwgu_ref.append(ref)
+        dwgu_got.append(np_(layer.dw_gate_up[e][torch.from_numpy(rows_n).cuda()]))
+        dwgu_extra.append(pb.storage(ref) + pb.flip_allowance("mxfp8", "dgu", parts["dgu"], parts["xc"], True))
+    assert done.all()
+
+    rec = {"test": "fullsize_sampled", "workload": name, "precision": "mxfp8", "sampled_tokens": int(n)}
+    tt = torch.from_numpy(tokens).cuda()
+    y_ref, dx_ref = acc["y"], acc["dx"]
+    pb.check(np_(layer.y[tt]), y_ref,
+             pb.bound(y_ref, pb.storage(y_ref, extra["y_rows"]) + extra["f_y"]), "y", rec)
+    pb.check(np_(layer.dx[tt]), dx_ref,
+             pb.bound(dx_ref, pb.storage(dx_ref, extra["dx_rows"]) + extra["f_dx"]), "dx", rec)
+    pb.check(np_(layer.dprobs[tt]), acc["dprobs"], pb.bound(acc["dprobs"], pb.Z * extra["dp_sig"]), "dprobs", rec)
+    dwd_ref_all = np.concatenate([r.ravel() for r in dwd_ref])
+    pb.check(np.concatenate([g_.ravel() for g_ in dwd_got]), dwd_ref_all,
+             pb.bound(dwd_ref_all, np.concatenate([b_.ravel() for b_ in dwd_extra])), "dw_down", rec)
+    dwgu_ref_all = np.concatenate([r.ravel() for r in dwgu_ref])
+    pb.check(np.concatenate([g_.ravel() for g_ in dwgu_got]), dwgu_ref_all,
+             pb.bound(dwgu_ref_all, np.concatenate([b_.ravel() for b_ in dwgu_extra])), "dw_gate_up", rec)
+
+    # gate-up rows of the sampled tokens (padded row layout)
+    srows = perm["row_of_src"].reshape(T, k)[tokens]                  # permuted rows [n, k]
+    pr = perm["padded_offsets"][expert_of_row[srows]] + (srows - perm["offsets"][expert_of_row[srows]])
+    gu = np_(gu_g[torch.from_numpy(pr.reshape(-1)).cuda()])
+    assert_rel_close(gu, acc["gu"].reshape(-1, 2 * I), tol=1e-2, floor=1.0, name=f"{name} gate-up")
+    # the sample reached every non-empty expert's last tile
+    last_tile_rows = 0
+    for e in np.nonzero(split > 0)[0]:
+        a0, b0 = perm["offsets"][e], perm["offsets"][e + 1]
+        last_tile_rows += int(np.sum((srows >= a0 + ((b0 - a0 - 1) // align) * align) & (srows < b0)) > 0)
+    assert last_tile_rows == int(np.sum(split > 0))
+    pb.write_record(dict(rec, tensor="coverage", experts=int(np.sum(split > 0)), last_tiles=last_tile_rows))
     for e in np.nonzero(split == 0)[0]:
         assert not bool(layer.dw_gate_up[int(e)].any()) and not bool(layer.dw_down[int(e)].any())

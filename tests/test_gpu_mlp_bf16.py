@@ -4,13 +4,15 @@ MLP): seeded inputs spanning several tiles, ragged group tails and an empty
 expert.  The only rounding on the GPU side is bf16 storage (h, dGU, the
 gate-up output kept for the backward, the outputs) and fp32 accumulation, so
 the errors are far inside the 2e-2 relative-RMS bar; the test states the
-tighter bound it expects (5e-3)."""
+tighter bound it expects (5e-3 relative RMS) and checks every element against
+the bound tests/parity_bounds.py derives for bf16 storage."""
 import numpy as np
 import pytest
 import torch
 
 import synthetic
-from gpu_helpers import assert_rms_close, np_, require_gpu
+import parity_bounds as pb
+from gpu_helpers import np_, require_gpu
 from oracle import moe
 
 pytestmark = pytest.mark.gpu
@@ -48,13 +50,15 @@ def test_bf16_mlp_fwd_bwd_matches_exact_oracle(name):
     g = moe.mlp_bwd(ctx, inp["dy"].double().numpy())
     assert np.array_equal(np_(ids), rids)
     assert np.array_equal(np_(split), ctx["perm"]["split_sizes"])
-    report = {
-        "y": assert_rms_close(np_(y), ctx["y"], 5e-3, "y"),
-        "dx": assert_rms_close(np_(dx), g["dx"], 5e-3, "dx"),
-        "dprobs": assert_rms_close(np_(dprobs), g["dprobs"], 5e-3, "dprobs"),
-        "dw_gate_up": assert_rms_close(np_(dwgu), g["dw_gate_up"], 5e-3, "dW_gate_up"),
-        "dw_down": assert_rms_close(np_(dwd), g["dw_down"], 5e-3, "dW_down"),
-    }
+    W = {e: moe.expert_weights(inp["w_gate_up"][e].double().numpy(), inp["w_down"][e].double().numpy(), quant=False)
+         for e in range(E) if ctx["perm"]["split_sizes"][e] > 0}
+    bnd = pb.full_bounds(ctx, g, W, inp["dy"].double().numpy(), mode="bf16", frac=5e-3)
+    rec = {"test": "mlp_bf16", "workload": name, "precision": "bf16"}
+    report = {}
+    for key, got, ref in (("y", y, ctx["y"]), ("dx", dx, g["dx"]), ("dprobs", dprobs, g["dprobs"]),
+                          ("dw_gate_up", dwgu, g["dw_gate_up"]), ("dw_down", dwd, g["dw_down"])):
+        o = pb.check(np_(got), ref, bnd[key], key, rec, frac=5e-3)
+        report[key] = (o["max_err_over_rms"], o["rel_rms"])
     for e in np.nonzero(ctx["perm"]["split_sizes"] == 0)[0]:
         assert not np_(dwgu)[e].any() and not np_(dwd)[e].any()
     print(name, {n: (round(a, 5), round(b, 6)) for n, (a, b) in report.items()})

@@ -8,8 +8,9 @@ oracle's fp8 mode (oracle/fp8.py: one power-of-two scale per expert tensor,
   (scaling by a power of two is exact on both sides);
 - amax of h: within 1e-2 relative (h comes out of an fp32 GEMM on one side and
   fp64 on the other);
-- y, dx, dW_gate_up, dW_down, dprobs: within 2e-2 of the reference RMS
-  (relative RMS error plus the per-element guard), as for the MXFP8 path;
+- y, dx, dW_gate_up, dW_down, dprobs: relative RMS error within 2e-2 and
+  every element within the bound tests/parity_bounds.py derives for the
+  per-tensor FP8 path;
 - experts without tokens: dW exactly 0."""
 import ctypes
 
@@ -18,7 +19,8 @@ import pytest
 import torch
 
 import synthetic
-from gpu_helpers import assert_rms_close, np_, require_gpu
+import parity_bounds as pb
+from gpu_helpers import np_, require_gpu
 from oracle import fp8, moe
 
 pytestmark = pytest.mark.gpu
@@ -88,13 +90,15 @@ def test_fp8_mlp_matches_oracle(name):
             ref = np.max(np.abs(ctx["h"][a:b]))
             assert abs(amax["h"][e] - ref) <= 1e-2 * ref, (e, amax["h"][e], ref)
     assert np.array_equal(np_(split), perm["split_sizes"])
-    report = {
-        "y": assert_rms_close(np_(y), ctx["y"], 2e-2, "y"),
-        "dx": assert_rms_close(np_(dx), g["dx"], 2e-2, "dx"),
-        "dprobs": assert_rms_close(np_(dprobs), g["dprobs"], 2e-2, "dprobs"),
-        "dw_gate_up": assert_rms_close(np_(dwgu), g["dw_gate_up"], 2e-2, "dW_gate_up"),
-        "dw_down": assert_rms_close(np_(dwd), g["dw_down"], 2e-2, "dW_down"),
-    }
+    W = {e: moe.expert_weights(inp["w_gate_up"][e].double().numpy(), inp["w_down"][e].double().numpy(), quant="fp8")
+         for e in range(E) if perm["split_sizes"][e] > 0}
+    bnd = pb.full_bounds(ctx, g, W, inp["dy"].double().numpy(), mode="fp8")
+    rec = {"test": "mlp_fp8", "workload": name, "precision": "fp8"}
+    report = {}
+    for key, got, ref in (("y", y, ctx["y"]), ("dx", dx, g["dx"]), ("dprobs", dprobs, g["dprobs"]),
+                          ("dw_gate_up", dwgu, g["dw_gate_up"]), ("dw_down", dwd, g["dw_down"])):
+        o = pb.check(np_(got), ref, bnd[key], key, rec)
+        report[key] = (o["max_err_over_rms"], o["rel_rms"])
     for e in np.nonzero(perm["split_sizes"] == 0)[0]:
         assert not np_(dwgu)[e].any() and not np_(dwd)[e].any()
     print(name, {n: (round(a, 5), round(b, 6)) for n, (a, b) in report.items()})

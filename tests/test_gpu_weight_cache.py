@@ -11,14 +11,20 @@ ABI.
   of the uncached run, so (main_grad - start) differs from 2 dW by at most two
   bf16 roundings (2^-8 relative each) plus two fp32 additions; slices of
   experts without tokens stay bit-identical; against the oracle, (main_grad -
-  start) / 2 is within the MLP's 2e-2 relative-RMS bar of dW."""
+  start) / 2 meets the MLP's parity bounds for dW (tests/parity_bounds.py)."""
 import numpy as np
 import pytest
 import torch
 
 import synthetic
-from gpu_helpers import assert_rms_close, np_, require_gpu
+import parity_bounds as pb
+from gpu_helpers import np_, require_gpu
 from oracle import moe
+
+
+def _weights(inp, split):
+    return {e: moe.expert_weights(inp["w_gate_up"][e].double().numpy(), inp["w_down"][e].double().numpy())
+            for e in range(len(split)) if split[e] > 0}
 
 pytestmark = pytest.mark.gpu
 
@@ -68,7 +74,8 @@ def test_cached_weights_bit_identical(name):
     rids, rprobs = moe.route_topk(inp["logits"].numpy(), k)
     ctx = moe.mlp_fwd(inp["x"].double().numpy(), rids, rprobs, inp["w_gate_up"].double().numpy(),
                       inp["w_down"].double().numpy())
-    assert_rms_close(np_(y), ctx["y"], 2e-2, "y")
+    bnd = pb.full_bounds(ctx, None, _weights(inp, ctx["perm"]["split_sizes"]))
+    pb.check(np_(y), ctx["y"], bnd["y"], "y", {"test": "weight_cache", "workload": name, "precision": "mxfp8"})
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -96,8 +103,9 @@ def test_main_grad_accumulates_fp32(name):
     ctx = moe.mlp_fwd(inp["x"].double().numpy(), rids, rprobs, inp["w_gate_up"].double().numpy(),
                       inp["w_down"].double().numpy())
     gr = moe.mlp_bwd(ctx, inp["dy"].double().numpy())
-    for got, start, dw, oracle_dw, nm in ((mg_gu, mg0_gu, ref["dwgu"], gr["dw_gate_up"], "dW_gate_up"),
-                                          (mg_d, mg0_d, ref["dwd"], gr["dw_down"], "dW_down")):
+    bnd = pb.full_bounds(ctx, gr, _weights(inp, ctx["perm"]["split_sizes"]), inp["dy"].double().numpy())
+    for got, start, dw, oracle_dw, nm, key in ((mg_gu, mg0_gu, ref["dwgu"], gr["dw_gate_up"], "dW_gate_up", "dw_gate_up"),
+                                               (mg_d, mg0_d, ref["dwd"], gr["dw_down"], "dW_down", "dw_down")):
         a, s0, w = np_(got).astype(np.float64), start.numpy().astype(np.float64), np_(dw)
         inc = a - s0
         bound = 2.0 ** -7 * 1.01 * np.abs(w) + 2.0 ** -22 * (np.abs(s0) + 2 * np.abs(w)) + 1e-30
@@ -105,7 +113,7 @@ def test_main_grad_accumulates_fp32(name):
         assert worst <= 1.0, f"{nm}: main_grad increment off 2 dW by {worst:.3g}x the rounding bound"
         for e in np.nonzero(split == 0)[0]:
             assert np.array_equal(a[e], s0[e]), f"{nm}: expert {e} without tokens changed"
-        assert_rms_close(inc / 2, oracle_dw, 2e-2, nm)
+        pb.check(inc / 2, oracle_dw, bnd[key], nm, {"test": "main_grad", "workload": name, "precision": "mxfp8"})
 
 
 def test_weight_cache_holds_the_oracles_codes():

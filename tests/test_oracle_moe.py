@@ -248,6 +248,20 @@ def test_sampled_evaluation_equals_full_oracle():
     np.testing.assert_allclose(s["dx"], g["dx"][tokens], rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(s["dprobs"], g["dprobs"][tokens], rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(s["gu"], ctx["gu"][s["rows"]], rtol=1e-11, atol=1e-13)
+    # one expert at a time, summed: the same outputs (the full-size tests hold
+    # one expert's weights in memory at a time)
+    acc = {n: 0.0 for n in ("y", "dx", "dprobs")}
+    done = np.zeros_like(s["done"])
+    for e in W:
+        part = sampled.rows_forward_backward(tokens, c["x"], c["dy"], probs, perm["row_of_src"], expert_of_row, k,
+                                             {e: W[e]})
+        for n in acc:
+            acc[n] = acc[n] + part[n]
+        assert not (done & part["done"]).any()
+        done |= part["done"]
+    assert done.all()
+    for n in acc:
+        np.testing.assert_allclose(acc[n], s[n], rtol=1e-12, atol=1e-14)
     tok = perm["src_of_row"] // k
     for e in (0, 3):
         a, b = perm["offsets"][e], perm["offsets"][e + 1]
