@@ -225,6 +225,7 @@ int mxg_device_supported(void) {
 uint64_t mxg_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int mxg_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* probs, void* stream) {
+  NvtxRange nvtx("mxg.route_topk");
   if (!logits || !ids || !probs) return MXG_ERR_ARG;
   if (T <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
   if (k > E || E > 256 || k > 32) return MXG_ERR_SHAPE;
@@ -243,6 +244,7 @@ size_t mxg_route_permute_workspace_bytes(int T, int k, int E) {
 int mxg_route_permute(const int32_t* ids, int T, int k, int E, int32_t* split_sizes, int32_t* src_of_row,
                       int32_t* row_of_src, int32_t* padded_offsets, void* ws, size_t ws_bytes,
                       int32_t* dev_status, void* stream) {
+  NvtxRange nvtx("mxg.route_permute");
   if (!ids || !split_sizes || !src_of_row || !row_of_src || !padded_offsets || !ws || !dev_status)
     return MXG_ERR_ARG;
   if (T <= 0 || k <= 0 || E <= 0) return MXG_ERR_ARG;
@@ -272,6 +274,7 @@ int mxg_route_permute(const int32_t* ids, int T, int k, int E, int32_t* split_si
 
 int mxg_mxfp8_quantize(const uint16_t* x, int rows, int cols, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                        uint8_t* s_col, int layout, void* stream) {
+  NvtxRange nvtx("mxg.mxfp8_quantize");
   if (!x || rows <= 0 || cols <= 0) return MXG_ERR_ARG;
   if (layout != MXG_LAYOUT_CANONICAL && layout != MXG_LAYOUT_MMA) return MXG_ERR_ARG;
   if ((q_row == nullptr) != (s_row == nullptr) || (q_col == nullptr) != (s_col == nullptr)) return MXG_ERR_ARG;
@@ -310,6 +313,7 @@ size_t mxg_mxfp8_grouped_rows_capacity(int rows, int groups, int layout) {
 int mxg_mxfp8_quantize_grouped(const uint16_t* x, int rows, int cols, const int32_t* group_offsets, int groups,
                                int32_t* padded_offsets, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                                uint8_t* s_col, int layout, int32_t* dev_status, void* stream) {
+  NvtxRange nvtx("mxg.mxfp8_quantize_grouped");
   if (!x || !group_offsets || !padded_offsets || !dev_status || rows <= 0 || cols <= 0 || groups <= 0)
     return MXG_ERR_ARG;
   if (layout != MXG_LAYOUT_CANONICAL && layout != MXG_LAYOUT_MMA) return MXG_ERR_ARG;
@@ -348,6 +352,7 @@ int mxg_mxfp8_quantize_grouped(const uint16_t* x, int rows, int cols, const int3
 
 int mxg_gather_rows(const void* src, int64_t src_rows, int64_t row_bytes, const int32_t* index, int div,
                     int64_t rows, void* dst, int32_t* dev_status, void* stream) {
+  NvtxRange nvtx("mxg.gather_rows");
   if (!src || !index || !dst || !dev_status || src_rows <= 0 || row_bytes <= 0 || div <= 0 || rows <= 0)
     return MXG_ERR_ARG;
   if (row_bytes % 4) return MXG_ERR_SHAPE;
@@ -361,6 +366,7 @@ int mxg_gather_rows(const void* src, int64_t src_rows, int64_t row_bytes, const 
 
 int mxg_combine(const uint16_t* rows, int64_t src_rows, const int32_t* row_of_src, int T, int k, int H, uint16_t* y,
                 int32_t* dev_status, void* stream) {
+  NvtxRange nvtx("mxg.combine");
   if (!rows || !row_of_src || !y || !dev_status || src_rows <= 0 || T <= 0 || k <= 0 || H <= 0) return MXG_ERR_ARG;
   if (H % 8 || k > 32) return MXG_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(rows) | reinterpret_cast<uintptr_t>(y)) & 15u) return MXG_ERR_ALIGN;
@@ -372,6 +378,7 @@ int mxg_combine(const uint16_t* rows, int64_t src_rows, const int32_t* row_of_sr
 int mxg_grouped_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                      const int32_t* padded_offsets, int E, int m_cap, int N, int K, uint16_t* d,
                      int32_t* dev_status, void* stream) {
+  NvtxRange nvtx("mxg.grouped_gemm");
   if (!a || !sa || !b || !sb || !padded_offsets || !d || !dev_status) return MXG_ERR_ARG;
   if (E <= 0 || m_cap <= 0 || N <= 0 || K <= 0) return MXG_ERR_ARG;
   if (E > 256 || K % 128 || N % 128 || m_cap % 128) return MXG_ERR_SHAPE;
@@ -439,6 +446,7 @@ int mxg_debug_grouped_gemm_stall(const uint8_t* a, const uint8_t* sa, const uint
 int mxg_grouped_gemm_wgrad(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                            const int32_t* padded_offsets, int E, int M, int N, int t_cap, uint16_t* d,
                            int32_t* dev_status, void* stream) {
+  NvtxRange nvtx("mxg.grouped_gemm_wgrad");
   if (!a || !sa || !b || !sb || !padded_offsets || !d || !dev_status) return MXG_ERR_ARG;
   if (E <= 0 || M <= 0 || N <= 0 || t_cap <= 0) return MXG_ERR_ARG;
   if (E > 256 || M % 128 || N % 128 || t_cap % 128) return MXG_ERR_SHAPE;
@@ -512,6 +520,7 @@ const void* mxg_mlp_weight_cache_view(const void* cache, int H, int I, int E, in
 
 int mxg_mlp_quantize_weights(const uint16_t* w_gate_up, const uint16_t* w_down, int H, int I, int E, void* cache,
                              size_t cache_bytes, void* stream) {
+  NvtxRange nvtx("mxg.quantize_weights");
   if (!w_gate_up || !w_down || !cache) return MXG_ERR_ARG;
   if (H <= 0 || I <= 0 || E <= 0) return MXG_ERR_ARG;
   if (!mlp_shape_ok(1, H, I, E, 1)) return MXG_ERR_SHAPE;
@@ -588,6 +597,7 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
 
   // F2: permute (histogram -> scan -> stable scatter) into the padded layout
   if (run(MXG_FWD_PERMUTE)) {
+  NvtxRange nvtx("mxg.fwd.permute");
   MXG_TRY(cudaMemsetAsync(at<int32_t>(sv, pl.prow_src), 0xFF, 4 * pl.Rc, s));
   PermuteParams pp{};
   pp.ids = A->ids;
@@ -607,15 +617,18 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
 
   // F4: weights, both orientations in one pass (the transposed ones only for
   // backward); nothing to do with a weight cache
-  if (run(MXG_FWD_QUANT_WEIGHTS) && !cached)
+  if (run(MXG_FWD_QUANT_WEIGHTS) && !cached) {
+    NvtxRange nvtx("mxg.fwd.quant_weights");
     MXG_TRY(launch_weight_quant(A->w_gate_up, A->w_down, H, I, E, at<uint8_t>(ws, pl.wgu), at<uint8_t>(ws, pl.swgu),
                                 save ? at<uint8_t>(sv, pl.wguT) : nullptr, at<uint8_t>(sv, pl.swguT),
                                 at<uint8_t>(ws, pl.wd), at<uint8_t>(ws, pl.swd),
                                 save ? at<uint8_t>(sv, pl.wdT) : nullptr, at<uint8_t>(sv, pl.swdT), s));
+  }
 
   // F3: gather x into the padded per-expert layout and quantise (row-wise along
   // H for the gate-up GEMM; token-column-wise for the gate-up weight gradient)
   if (run(MXG_FWD_QUANT_X)) {
+  NvtxRange nvtx("mxg.fwd.quant_x");
   QuantParams xq{};
   xq.x = A->x;
   xq.ld_x = H;
@@ -642,6 +655,7 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
 
   // F5: gate-up grouped GEMM + ScaledSwiGLU + MXFP8 re-quantisation of h
   if (run(MXG_FWD_GATE_UP)) {
+  NvtxRange nvtx("mxg.fwd.gate_up");
   GemmArgs g{};
   g.epi = EPI_SWIGLU;
   g.pair = kUsePairTiles;
@@ -679,6 +693,7 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
 
   // F6: down grouped GEMM
   if (run(MXG_FWD_DOWN)) {
+  NvtxRange nvtx("mxg.fwd.down");
   GemmArgs d{};
   d.epi = EPI_BF16;
   d.pair = kUsePairTiles && H % 256 == 0;
@@ -713,9 +728,11 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
   }
 
   // F7: y[t] = sum_j Y[row(t, j)] (fused into the down GEMM above for long contractions)
-  if (run(MXG_FWD_COMBINE) && !fuse_combine(k, I, pl.R))
+  if (run(MXG_FWD_COMBINE) && !fuse_combine(k, I, pl.R)) {
+    NvtxRange nvtx("mxg.fwd.combine");
     MXG_TRY(launch_combine(at<uint16_t>(ws, pl.yperm), at<int32_t>(sv, pl.prow_of_src), static_cast<int>(pl.T),
                            static_cast<int>(k), static_cast<int>(H), A->y, s));
+  }
   return MXG_OK;
 }
 
@@ -762,6 +779,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
 
   // B1: gather dy and quantise (row-wise along H for dgrad, token-column-wise for wgrad)
   if (run(MXG_BWD_QUANT_DY)) {
+  NvtxRange nvtx("mxg.bwd.quant_dy");
   QuantParams yq{};
   yq.x = A->dy;
   yq.ld_x = H;
@@ -784,6 +802,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
 
   // B2: dH = dY W_down (MX along H) with fused dSwiGLU -> dGU (both orientations), d(prob) partials
   if (run(MXG_BWD_DGRAD_DOWN)) {
+  NvtxRange nvtx("mxg.bwd.dgrad_down");
   GemmArgs g{};
   g.epi = EPI_DSWIGLU;
   g.pair = kUsePairTiles && I % 256 == 0;
@@ -821,6 +840,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
 
   // B3: dW_down[e] = dYc^T Hc over the tokens of e (or added into main_grad_down)
   if (run(MXG_BWD_WGRAD_DOWN)) {
+  NvtxRange nvtx("mxg.bwd.wgrad_down");
   GemmArgs w{};
   w.epi = main_grad ? EPI_ACC_F32 : EPI_BF16;
   w.kgroup = true;
@@ -847,6 +867,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
 
   // B4: dX_perm = dGU W_gate_up (MX along 2I)
   if (run(MXG_BWD_DGRAD_GATE_UP)) {
+  NvtxRange nvtx("mxg.bwd.dgrad_gate_up");
   GemmArgs x{};
   x.epi = EPI_BF16;
   x.pair = kUsePairTiles && H % 256 == 0;
@@ -882,6 +903,7 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
 
   // B5: dW_gate_up[e] = dGUc^T Xc over the tokens of e (or added into main_grad_gate_up)
   if (run(MXG_BWD_WGRAD_GATE_UP)) {
+  NvtxRange nvtx("mxg.bwd.wgrad_gate_up");
   GemmArgs v{};
   v.epi = main_grad ? EPI_ACC_F32 : EPI_BF16;
   v.kgroup = true;
@@ -909,12 +931,16 @@ static int bwd_impl(const mxg_mlp_bwd_args* A, int stage, void* stream) {
   // B6, B7: combine dx, reduce d(prob)
   const int32_t* prow_of_src = at<int32_t>(sv, pl.prow_of_src);
   // B6: dx[t] = sum_j dX[row(t, j)] (fused into the dgrad-gate-up GEMM above for long contractions)
-  if (run(MXG_BWD_COMBINE_DX) && !fuse_combine(k, 2 * I, pl.R))
+  if (run(MXG_BWD_COMBINE_DX) && !fuse_combine(k, 2 * I, pl.R)) {
+    NvtxRange nvtx("mxg.bwd.combine_dx");
     MXG_TRY(launch_combine(at<uint16_t>(ws, pl.dxperm), prow_of_src, static_cast<int>(pl.T), static_cast<int>(k),
                            static_cast<int>(H), A->dx, s));
-  if (run(MXG_BWD_DPROBS))
+  }
+  if (run(MXG_BWD_DPROBS)) {
+    NvtxRange nvtx("mxg.bwd.dprobs");
     MXG_TRY(launch_dprob(at<float>(ws, pl.dp), static_cast<int>(pl.dp_ld), prow_of_src, static_cast<int>(pl.R),
                          A->dprobs, s));
+  }
   return MXG_OK;
 }
 

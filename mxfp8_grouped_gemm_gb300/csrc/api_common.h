@@ -3,6 +3,7 @@
 // alignment checks and CUDA-error propagation.
 #pragma once
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdint>
 
@@ -39,6 +40,17 @@ inline const T* at(const void* base, int64_t off) {
 }
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA; }
+
+// An NVTX range around the host code that enqueues one stage's launches, so a
+// profiler's timeline names every kernel by its stage ("mxg.fwd.gate_up", ...).
+// NVTX v3 is header-only: without a profiler attached a range costs a few
+// nanoseconds and loads nothing.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 }  // namespace api
 }  // namespace mxg
