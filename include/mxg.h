@@ -96,16 +96,35 @@ int mxg_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float
  * Router front end: logits = x W_r^T (one linear layer H -> E, no bias) and the
  * top-k route of mxg_route_topk on them, in one kernel.  [Grouped] Fig. 1 (a
  * router picks two of eight experts per token); the page does not spell the
- * router out, the single bias-free linear layer is the reading taken.
+ * router out, the single bias-free linear layer is the reading taken.  The
+ * contraction runs on the tensor cores (bf16 operands, fp32 accumulators,
+ * 128 tokens per CTA); the route is taken on the fp32 logits.
  *   x         bf16 [T][H] (device)
  *   w_router  bf16 [E][H] (device)
  *   logits    fp32 [T][E] out, accumulated in fp32 from the bf16 products
  *   ids, probs  as mxg_route_topk
  * Requires H % 128 == 0, 1 <= k <= E <= 256, k <= 32.  x, w_router 32-byte
- * aligned.
+ * aligned.  A kernel wait that gives up (no status word here) leaves the
+ * affected tokens' ids at -1, which a following permute reports.
  */
 int mxg_router_fwd(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, float* logits,
                    int32_t* ids, float* probs, void* stream);
+
+/* Router front end fused with the permute: the logits and route of
+ * mxg_router_fwd, and the permute of mxg_route_permute on the chosen ids, with
+ * the permute's per-chunk expert histogram accumulated by the router kernel
+ * itself (the route output feeds the histogram without a second pass over the
+ * ids).  [Grouped] Fig. 1 (router, top-2 of 8) and "Grouping fragmented expert
+ * workloads" (split_sizes).
+ *   x, w_router, logits, ids, probs   as mxg_router_fwd
+ *   split_sizes, src_of_row, row_of_src, padded_offsets, ws, ws_bytes,
+ *   dev_status                        as mxg_route_permute (ws sized by
+ *                                     mxg_route_permute_workspace_bytes)
+ * Results equal mxg_router_fwd followed by mxg_route_permute, bit for bit.
+ * Requires H % 128 == 0, 1 <= k <= E <= 256, k <= 32. */
+int mxg_router_fwd_permute(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, float* logits,
+                           int32_t* ids, float* probs, int32_t* split_sizes, int32_t* src_of_row, int32_t* row_of_src,
+                           int32_t* padded_offsets, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* Scratch for mxg_router_bwd (bytes). */
 size_t mxg_router_bwd_workspace_bytes(int T, int H, int E, int k);

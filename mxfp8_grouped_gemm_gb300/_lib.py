@@ -38,6 +38,7 @@ EXPORTS = [
     "mxg_mlp_workspace_view", "mxg_mlp_weight_cache_view", "mxg_bench_mxfp8_mma_peak",
     "mxg_mxfp8_grouped_rows_capacity", "mxg_mxfp8_quantize_grouped", "mxg_gather_rows", "mxg_combine",
     "mxg_mlp_grouped_saved_bytes", "mxg_mlp_grouped_workspace_bytes", "mxg_grouped_mlp_fwd_grouped",
+    "mxg_router_fwd_permute",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -144,6 +145,7 @@ def lib() -> ctypes.CDLL:
         "mxg_mlp_grouped_saved_bytes": (SZ, [I32, I32, I32, I32]),
         "mxg_mlp_grouped_workspace_bytes": (SZ, [I32, I32, I32, I32]),
         "mxg_grouped_mlp_fwd_grouped": (I32, [ctypes.POINTER(MlpGroupedFwdArgs), P]),
+        "mxg_router_fwd_permute": (I32, [P, P, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -535,3 +537,26 @@ def mxg_grouped_mlp_fwd_grouped(x, split_sizes, probs, w_gate_up, w_down, saved,
                           0 if weight_cache is None else weight_cache.buffer.numel())
     _check("mxg_grouped_mlp_fwd_grouped", lib().mxg_grouped_mlp_fwd_grouped(ctypes.byref(a), _stream(stream)))
     return y
+
+
+def mxg_router_fwd_permute(x: torch.Tensor, w_router: torch.Tensor, k: int, dev_status: torch.Tensor, stream=None):
+    """Router logits + route + permute in one call; returns (logits, ids,
+    probs, permute dict as mxg_route_permute)."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    probs = torch.empty((T, k), dtype=torch.float32, device=dev)
+    ws_bytes = int(lib().mxg_route_permute_workspace_bytes(T, k, E))
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    out = {"split_sizes": torch.empty(E, dtype=torch.int32, device=dev),
+           "src_of_row": torch.empty(T * k, dtype=torch.int32, device=dev),
+           "row_of_src": torch.empty(T * k, dtype=torch.int32, device=dev),
+           "padded_offsets": torch.empty(E + 1, dtype=torch.int32, device=dev)}
+    _check("mxg_router_fwd_permute", lib().mxg_router_fwd_permute(
+        _ptr(x, torch.bfloat16, "x"), _ptr(w_router, torch.bfloat16, "w_router"), T, H, E, k,
+        _ptr(logits), _ptr(ids), _ptr(probs), _ptr(out["split_sizes"]), _ptr(out["src_of_row"]),
+        _ptr(out["row_of_src"]), _ptr(out["padded_offsets"]), _ptr(ws), ws_bytes,
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+    return logits, ids, probs, out

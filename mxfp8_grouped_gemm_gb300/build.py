@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmxg.so")
-SOURCES = ["api.cu", "api_bf16.cu", "api_fp8.cu", "route.cu", "router.cu", "quant.cu", "combine.cu", "gemm.cu", "noalloc.cu", "peak.cu", "rows.cu"]
+SOURCES = ["api.cu", "api_bf16.cu", "api_fp8.cu", "route.cu", "router.cu", "quant.cu", "combine.cu", "gemm.cu", "noalloc.cu", "peak.cu", "rows.cu", "router_mma.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",

@@ -1131,6 +1131,10 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
 
 }  // namespace
 
+bool tma_map_bf16(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, uint32_t box_rows) {
+  return encode_bf16(m, base, cols, rows, box_rows);
+}
+
 int gemm_pick_bn(int epi, int N) {
   if (epi == EPI_SWIGLU) return 256;
   return N % 256 == 0 ? 256 : 128;

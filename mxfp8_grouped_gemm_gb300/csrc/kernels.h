@@ -1,5 +1,6 @@
 // Internal launchers shared by the C-ABI layer (api.cu) and the kernel files.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -98,6 +99,22 @@ struct PermuteParams {
 };
 int permute_num_blocks(int R);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
+
+// 2-D TMA map over a bf16 matrix [rows][cols] (row stride cols * 2 bytes):
+// boxes of 64 columns (one 128-byte swizzled row) x box_rows rows; reads
+// past the matrix's edges fill zeros.
+bool tma_map_bf16(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, uint32_t box_rows);
+
+// Router logits on the tensor cores and the top-k route (router_mma.cu):
+// logits fp32 [T][E] = x [T][H] W_r [E][H]^T, then ids / probs as the route.
+// When counts is given (zeroed by the caller), every CTA also adds its
+// tokens' expert counts into counts[f / kPermuteChunk][e] (f = t*k + j): the
+// permute's histogram, so the permute can start from its scan.
+cudaError_t launch_router_mma(const uint16_t* x, const uint16_t* w, int T, int H, int E, int k, float* logits,
+                              int32_t* ids, float* probs, int32_t* counts, int32_t* status, cudaStream_t s);
+constexpr int kPermuteChunk = 4096;
+// The permute's scan and scatter after an external histogram (counts filled).
+cudaError_t launch_permute_from_counts(const PermuteParams& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ combine
 // y[t] = sum_j src[prow_of_src[t*k + j]] (fp32 in slot order, one bf16

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 }
 
 // --------------------------------------------------------------- permute ----
-constexpr int kChunk = 4096;     // flat entries per CTA
+constexpr int kChunk = kPermuteChunk;     // flat entries per CTA
 constexpr int kThreads = 256;
 constexpr int kMaxE = 256;
 
@@ -142,6 +142,16 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, 
 }
 
 int permute_num_blocks(int R) { return (R + kChunk - 1) / kChunk; }
+
+cudaError_t launch_permute_from_counts(const PermuteParams& p, cudaStream_t s) {
+  const int nblk = permute_num_blocks(p.R);
+  if (nblk == 0) return cudaSuccess;
+  scan_kernel<<<1, kThreads, 0, s>>>(p, nblk);
+  count_launch();
+  scatter_kernel<<<nblk, kThreads, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s) {
   const int nblk = permute_num_blocks(p.R);

@@ -72,6 +72,10 @@ WORKLOADS = {
     # one expert of the Mixtral layer at its uniform load (4096 rows): the same
     # per-tile work as "mixtral" with ~1.5 GB on the device, for profiler captures
     "mixtral_e1": Workload("mixtral_e1", 6, T=4096, H=4096, I=14336, E=1, k=1),
+    # the Mixtral layer's tokens (x and dy at full size, top-2 of 8 experts)
+    # with a narrow intermediate dimension: the activation quantisers' full
+    # work with ~3 GB on the device, for profiler captures
+    "mixtral_tokens": Workload("mixtral_tokens", 7, T=16384, H=4096, I=1024, E=8, k=2),
 }
 
 

@@ -111,3 +111,24 @@ def test_router_bwd_reports_bad_expert_id():
     m.mxg_router_bwd(x.cuda(), w.cuda(), ids.cuda(), probs.cuda(), dprobs.cuda(), dx, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 16                               # MXG_ERR_EXPERT_ID
+
+
+@pytest.mark.parametrize("T,H,E,k", CASES + [(20000, 256, 16, 3)])
+def test_router_fwd_permute_equals_router_then_permute(T, H, E, k):
+    """The fused call (the router kernel feeds the permute's histogram) gives
+    the same logits, route, split sizes, maps and padded offsets, bit for bit,
+    as mxg_router_fwd followed by mxg_route_permute (k = 3: a CTA's entries
+    straddle a histogram chunk)."""
+    m = require_gpu()
+    x, w = _inputs(T, H, E, 200 + E)
+    xc, wc = x.cuda(), w.cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lo, ids, probs, pm = m.mxg_router_fwd_permute(xc, wc, k, st)
+    lo2, ids2, probs2 = m.mxg_router_fwd(xc, wc, k)
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pm2 = m.mxg_route_permute(ids2, E, st2)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(st2.item()) == 0
+    assert torch.equal(lo, lo2) and torch.equal(ids, ids2) and torch.equal(probs, probs2)
+    for name in pm2:
+        assert torch.equal(pm[name], pm2[name]), name
