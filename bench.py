@@ -240,6 +240,55 @@ def split_stats(split) -> dict:
             "not_multiple_of_128": int((nz % 128 != 0).sum())}
 
 
+def time_router(m, x, k: int, E: int, dev, stream, reps: int = 20) -> dict:
+    """The router front end on the workload's tokens, outside the MLP step:
+    logits on the tensor cores + route (fwd), the same fused with the permute
+    (fwd_permute), and the backward; events on the stream."""
+    import torch
+
+    import synthetic
+    T, H = x.shape
+    peaks, _ = load_peaks()
+    w_r = synthetic.random_bf16((E, H), 4242, std=0.02).to(dev)
+    dprobs = torch.randn(T, k, device=dev, generator=torch.Generator(device=dev).manual_seed(5))
+    dx_r = torch.zeros((T, H), dtype=torch.bfloat16, device=dev)
+    st_r = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_r = torch.empty(m.mxg_router_bwd_workspace_bytes(T, H, E, k), dtype=torch.uint8, device=dev)
+    dw_r = torch.empty((E, H), dtype=torch.float32, device=dev)
+    lo, ri, rp = m.mxg_router_fwd(x, w_r, k)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(3):
+        m.mxg_router_fwd(x, w_r, k, logits=lo, ids=ri, probs=rp)
+        m.mxg_router_fwd_permute(x, w_r, k, st_r)
+        m.mxg_router_bwd(x, w_r, ri, rp, dprobs, dx_r, st_r, dw_router=dw_r, workspace=ws_r)
+    torch.cuda.synchronize(dev)
+    ev[0].record(stream)
+    for _ in range(reps):
+        m.mxg_router_fwd(x, w_r, k, logits=lo, ids=ri, probs=rp)
+    ev[1].record(stream)
+    for _ in range(reps):
+        m.mxg_router_fwd_permute(x, w_r, k, st_r)
+    ev[2].record(stream)
+    for _ in range(reps):
+        m.mxg_router_bwd(x, w_r, ri, rp, dprobs, dx_r, st_r, dw_router=dw_r, workspace=ws_r)
+    ev[3].record(stream)
+    torch.cuda.synchronize(dev)
+    if int(st_r.item()) != 0:
+        raise SystemExit(f"bench: router status {m.status_string(int(st_r.item()))}")
+    f_ms, fp_ms, b_ms = (ev[i].elapsed_time(ev[i + 1]) / reps for i in range(3))
+    # algorithmic bytes: fwd reads x (and W_r), writes logits, ids, probs; bwd
+    # reads probs, dprobs, ids, x, reads and writes dx, writes dW_r
+    fb = T * H * 2 + E * H * 2 + T * E * 4 + T * k * 8
+    bb = T * k * 12 + T * H * 2 + 2 * T * H * 2 + E * H * 4
+    flops = 2.0 * T * H * E
+    return {"T": T, "H": H, "E": E, "k": k, "fwd_ms": round(f_ms, 4), "fwd_permute_ms": round(fp_ms, 4),
+            "bwd_ms": round(b_ms, 4), "fwd_gbs": round(fb / (f_ms * 1e-3) / 1e9, 1),
+            "fwd_frac_of_hbm": round(fb / (f_ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 3),
+            "fwd_tflops": round(flops / (f_ms * 1e-3) / 1e12, 1),
+            "fwd_frac_of_bf16": round(flops / (f_ms * 1e-3) / 1e12 / float(peaks["bf16_tflops"]), 4),
+            "bwd_gbs": round(bb / (b_ms * 1e-3) / 1e9, 1), "note": "not part of the MLP step"}
+
+
 def time_workload(m, name: str, steps: int, warmup: int, dev, stream, precision: str, p_mx: float) -> dict:
     """One more workload through the same calls as the main step (device-resident
     inputs, route + forward + backward per step, events on the stream)."""
@@ -269,11 +318,13 @@ def time_workload(m, name: str, steps: int, warmup: int, dev, stream, precision:
     if layer.status() != 0:
         raise SystemExit(f"bench: {name} device status {m.status_string(layer.status())}")
     ms = a.elapsed_time(b) / steps
+    router = time_router(m, d["x"], wl.k, wl.E, dev, stream) if wl.H % 128 == 0 else None
     flops = wl.gemm_flops(True)
     tf = flops / (ms * 1e-3) / 1e12
     out = {"workload": workload_config(wl, precision, 1)["workload"], "ms_per_step": round(ms, 4),
            "tflops": round(tf, 2), "tokens_per_s": round(wl.T / (ms * 1e-3), 1), "frac_of_mxfp8_peak": round(tf / p_mx, 4),
-           "steps": steps, "warmup": warmup, "split_sizes": split_stats(layer.split_sizes.cpu().numpy())}
+           "steps": steps, "warmup": warmup, "split_sizes": split_stats(layer.split_sizes.cpu().numpy()),
+           "router": router}
     del layer, d
     torch.cuda.empty_cache()
     return out
@@ -396,37 +447,7 @@ def run_ours(args, rank, world):
     # the same tokens, outside the MLP step: reported beside it ----
     router = None
     if not args.no_router and H % 128 == 0:
-        w_r = synthetic.random_bf16((E, H), 4242, std=0.02).to(dev)
-        dprobs = torch.randn(T, k, device=dev, generator=torch.Generator(device=dev).manual_seed(5))
-        dx_r = torch.zeros((T, H), dtype=torch.bfloat16, device=dev)
-        st_r = torch.zeros(1, dtype=torch.int32, device=dev)
-        ws_r = torch.empty(m.mxg_router_bwd_workspace_bytes(T, H, E, k), dtype=torch.uint8, device=dev)
-        dw_r = torch.empty((E, H), dtype=torch.float32, device=dev)
-        lo, ri, rp = m.mxg_router_fwd(d["x"], w_r, k)
-        reps = 20
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        for _ in range(3):
-            m.mxg_router_fwd(d["x"], w_r, k, logits=lo, ids=ri, probs=rp)
-            m.mxg_router_bwd(d["x"], w_r, ri, rp, dprobs, dx_r, st_r, dw_router=dw_r, workspace=ws_r)
-        torch.cuda.synchronize(dev)
-        ev[0].record(stream)
-        for _ in range(reps):
-            m.mxg_router_fwd(d["x"], w_r, k, logits=lo, ids=ri, probs=rp)
-        ev[1].record(stream)
-        for _ in range(reps):
-            m.mxg_router_bwd(d["x"], w_r, ri, rp, dprobs, dx_r, st_r, dw_router=dw_r, workspace=ws_r)
-        ev[2].record(stream)
-        torch.cuda.synchronize(dev)
-        if int(st_r.item()) != 0:
-            raise SystemExit(f"bench: router status {m.status_string(int(st_r.item()))}")
-        f_ms, b_ms = ev[0].elapsed_time(ev[1]) / reps, ev[1].elapsed_time(ev[2]) / reps
-        # algorithmic bytes: fwd reads x, writes logits, ids, probs; bwd reads
-        # probs, dprobs, ids, x, reads and writes dx, writes dW_r
-        fb = T * H * 2 + T * E * 4 + T * k * 8
-        bb = T * k * 12 + T * H * 2 + 2 * T * H * 2 + E * H * 4
-        router = {"fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4),
-                  "fwd_gbs": round(fb / (f_ms * 1e-3) / 1e9, 1), "bwd_gbs": round(bb / (b_ms * 1e-3) / 1e9, 1),
-                  "note": "not part of the MLP step above"}
+        router = time_router(m, d["x"], k, E, dev, stream)
     # ---- gradient accumulation (MXFP8 path): the weights quantised once into
     # a weight cache per optimizer step, then micro-batches whose weight
     # gradients are added into fp32 main_grad buffers; reported beside the step

@@ -96,6 +96,15 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b) {
   return r;
 }
 
+// Four fp32 -> four E4M3 codes in one word (a in the lowest byte).
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{.reg .b16 lo, hi;\n cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+      " mov.b32 %0, {lo, hi};}"
+      : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+
 // 32 values already multiplied by the inverse scale -> 32 codes in 8 words.
 __device__ __forceinline__ void encode32(const float (&v)[32], uint32_t (&w)[8]) {
 #pragma unroll
@@ -104,6 +113,13 @@ __device__ __forceinline__ void encode32(const float (&v)[32], uint32_t (&w)[8])
     const uint32_t hi = cvt_e4m3x2(v[4 * i + 2], v[4 * i + 3]);
     w[i] = lo | (hi << 16);
   }
+}
+
+// The same codes with each word packed by one move (the quantiser's form:
+// measured faster there, a little slower inside the GEMM epilogues).
+__device__ __forceinline__ void encode32_x4(const float (&v)[32], uint32_t (&w)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = cvt_e4m3x4(v[4 * i + 0], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
 // ----------------------------------------------------------------- top-k

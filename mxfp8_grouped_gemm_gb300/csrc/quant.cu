@@ -51,7 +51,7 @@ __device__ __forceinline__ void quant_store32(float (&v)[32], uint8_t* dst, uint
     v[i + 1] = t.y;
   }
   uint32_t w[8];
-  encode32(v, w);
+  encode32_x4(v, w);
   uint4* d = reinterpret_cast<uint4*>(dst);
   d[0] = make_uint4(w[0], w[1], w[2], w[3]);
   d[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -63,7 +63,7 @@ __device__ __forceinline__ void quant_store32_pt(float (&v)[32], uint8_t* dst, f
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] *= s;
   uint32_t w[8];
-  encode32(v, w);
+  encode32_x4(v, w);
   uint4* d = reinterpret_cast<uint4*>(dst);
   d[0] = make_uint4(w[0], w[1], w[2], w[3]);
   d[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -90,6 +90,7 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t (&r)[4]) 
 // permuted so that matrix m's fragment rows 2j, 2j+1 are tile rows 8j+2m,
 // 8j+2m+1); the quad reduces the block maximum with two shuffles and each lane
 // writes its 8 codes as one 8-byte store.
+template <bool PT>
 __device__ __forceinline__ void quant_col_block(const QuantParams& P, const uint16_t* buf, int col0, int64_t gcol0,
                                                 int p0, int lane, float pt_s) {
   const int m = lane >> 3, i = lane & 7;
@@ -102,7 +103,7 @@ __device__ __forceinline__ void quant_col_block(const QuantParams& P, const uint
   const int64_t gc = gcol0 + (lane >> 2);
   uint8_t* qdst = P.q_col + gc * P.ld_col + p0 + 8 * j;
   const int64_t qstep = 8 * P.ld_col;
-  const bool store_scale = j == 0 && P.pt_amax == nullptr;
+  const bool store_scale = j == 0 && !PT;
   int64_t soff = 0, sstep = 0;
   if (store_scale) {
     soff = sf_offset(P.layout, gc, p0 >> 5, P.sf_col_rows, P.ld_col >> 5);
@@ -120,7 +121,7 @@ __device__ __forceinline__ void quant_col_block(const QuantParams& P, const uint
     }
     uint32_t sb = 0;
     float inv = pt_s;                         // per-tensor FP8: the tensor's scale
-    if (P.pt_amax == nullptr) {               // MX: the block's own scale
+    if constexpr (!PT) {                      // MX: the block's own scale
       uint32_t amax = pair_max_bits(r, 4);
       amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
@@ -133,7 +134,7 @@ __device__ __forceinline__ void quant_col_block(const QuantParams& P, const uint
     for (int q = 0; q < 2; ++q) {
       const float2 lo = mul2(make_float2(v[4 * q], v[4 * q + 1]), inv2);
       const float2 hi = mul2(make_float2(v[4 * q + 2], v[4 * q + 3]), inv2);
-      w[q] = cvt_e4m3x2(lo.x, lo.y) | (cvt_e4m3x2(hi.x, hi.y) << 16);
+      w[q] = cvt_e4m3x4(lo.x, lo.y, hi.x, hi.y);
     }
     *reinterpret_cast<uint2*>(qdst + ct * qstep) = make_uint2(w[0], w[1]);
     if (store_scale) P.s_col[soff + ct * sstep] = static_cast<uint8_t>(sb);
@@ -158,39 +159,44 @@ __device__ __forceinline__ void copy_col_block(const QuantParams& P, const uint1
   }
 }
 
-constexpr int kTilesPerCta = 4;      // 32-row tiles walked by one CTA
+constexpr int kTilesPerCta = 8;      // 32-row tiles walked by one CTA
 
-// Stage one 32 x 128 tile (gathered rows: s_src holds the source row of each
-// of the CTA's rows, -1 for padding) into shared memory asynchronously.
-__device__ __forceinline__ void stage_tile(const QuantParams& P, const uint16_t* xb, int p0, int c0, uint16_t* buf,
-                                           int tid, const int* s_src, int first, bool gathered) {
+// Stage one 32 x 128 tile into shared memory asynchronously.  Thread tid
+// copies 16-byte chunk tid % 16 of rows tid / 16 + 8 i (i < 4).  Gathered
+// rows: s_off holds each of the CTA's rows' element offset from x (-1: a zero
+// padding row), so a copy is one shared load, one add and the copy.
+template <bool GATHER>
+__device__ __forceinline__ void stage_tile(const uint16_t* xc, int64_t ld_x, int p0, int rel0, uint16_t* buf, int tid,
+                                           const int64_t* s_off) {
+  const int vv = tid & 15;
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
-    const int i = tid + it * 128;
-    const int rr = i >> 4, vv = i & 15;
-    const int pp = p0 + rr;
-    int64_t srow = pp;
-    bool zero = false;
-    if (gathered) {
-      const int f = s_src[pp - first];
-      if (f < 0) zero = true;
-      else srow = f;
-    }
+    const int rr = (tid >> 4) + it * 8;
     uint16_t* dst = buf + rr * kStride + chunk_pos(rr, vv) * 8;
-    if (zero) *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    else cp_async16(dst, xb + srow * P.ld_x + c0 + vv * 8);
+    if constexpr (GATHER) {
+      const int64_t off = s_off[rel0 + rr];
+      if (off < 0) *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      else cp_async16(dst, xc + off);
+    } else {
+      cp_async16(dst, xc + static_cast<int64_t>(p0 + rr) * ld_x);
+    }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// One CTA walks kTilesPerCta tiles of 32 rows x 128 columns, loading tile t+1
-// (asynchronous 16-byte copies into the other shared buffer) while it
+// One CTA walks up to kTilesPerCta tiles of 32 rows x 128 columns, loading
+// tile t+1 (asynchronous 16-byte copies into the other shared buffer) while it
 // quantises tile t.  Row-wise: thread t quantises the 32-value block (row t/4,
 // columns 32*(t%4)..) read back with 16-byte loads.  Column-wise: warp w
 // quantises columns 32w..32w+31 over the tile's 32 rows from transposed
-// matrix loads (quant_col_block).
-__global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
+// matrix loads (quant_col_block).  The mode (gathered rows, row-wise and
+// column-wise outputs, per-tensor scale) is a template argument, so the tile
+// loop carries no run-time mode tests; the bf16 pass-through outputs of the
+// BF16 path stay run-time options.
+template <bool GATHER, bool ROW, bool COL, bool PT>
+__global__ void __launch_bounds__(128, 8) quant_kernel(const QuantParams P) {
   __shared__ __align__(16) uint16_t tile[2][kRows * kStride];
+  __shared__ int64_t s_off[GATHER ? kTilesPerCta * kRows : 1];
   const int c0 = blockIdx.y * kCols;
   const int b = blockIdx.z;
   const int tid = threadIdx.x;
@@ -200,37 +206,43 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
   const int ntiles = min(kTilesPerCta, (limit - first + kRows - 1) / kRows);
   if (ntiles <= 0) return;
   const uint16_t* xb = P.x + static_cast<int64_t>(b) * P.x_batch_stride;
-  // gathered rows: the CTA's 128 source rows resolved once (one load and one
-  // division per row, or a search of the group offsets) instead of in every
-  // staging pass
-  __shared__ int s_src[kTilesPerCta * kRows];
-  const bool gathered = P.src_rows != nullptr || P.grp_off != nullptr;
-  if (gathered) {
-    const int p = first + tid;
-    int f = -1;
-    if (P.src_rows != nullptr) {
-      const int v = p < P.rows ? P.src_rows[p] : -1;
-      f = v < 0 ? -1 : v / P.src_div;
-    } else if (p < limit) {
-      // the group holding padded row p: the last g with grp_poff[g] <= p
-      int lo = 0, hi = P.groups - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (P.grp_poff[mid] <= p) lo = mid;
-        else hi = mid - 1;
+  const uint16_t* xc = xb + c0 + (tid & 15) * 8;      // this thread's 16-byte column chunk
+  if constexpr (GATHER) {
+    // the CTA's source rows resolved once: a row map entry divided by the
+    // number of rows per source row, or a search of the group offsets
+    for (int i = tid; i < ntiles * kRows; i += 128) {
+      const int p = first + i;
+      int f = -1;
+      if (P.src_rows != nullptr) {
+        const int v = P.src_rows[p];
+        f = v < 0 ? -1 : (P.src_div == 1 ? v : v / P.src_div);
+      } else if (p < limit) {
+        int lo = 0, hi = P.groups - 1;     // the last group g with grp_poff[g] <= p
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (P.grp_poff[mid] <= p) lo = mid;
+          else hi = mid - 1;
+        }
+        const int src = P.grp_off[lo] + (p - P.grp_poff[lo]);
+        f = src < P.grp_off[lo + 1] ? src : -1;
       }
-      const int src = P.grp_off[lo] + (p - P.grp_poff[lo]);
-      f = src < P.grp_off[lo + 1] ? src : -1;
+      s_off[i] = f < 0 ? int64_t{-1} : static_cast<int64_t>(f) * P.ld_x;
     }
-    s_src[tid] = f;
     __syncthreads();
+    if (P.probs_perm != nullptr && blockIdx.y == 0 && b == 0) {
+      for (int i = tid; i < ntiles * kRows; i += 128) {
+        const int pp = first + i;
+        const int f = P.src_rows != nullptr ? P.src_rows[pp] : pp;
+        P.probs_perm[pp] = f < 0 ? 0.f : P.probs[f];
+      }
+    }
   }
 
-  stage_tile(P, xb, first, c0, tile[0], tid, s_src, first, gathered);
+  stage_tile<GATHER>(xc, P.ld_x, first, 0, tile[0], tid, s_off);
   for (int t = 0; t < ntiles; ++t) {
     const int p0 = first + t * kRows;
     if (t + 1 < ntiles) {
-      stage_tile(P, xb, p0 + kRows, c0, tile[(t + 1) & 1], tid, s_src, first, gathered);
+      stage_tile<GATHER>(xc, P.ld_x, p0 + kRows, (t + 1) * kRows, tile[(t + 1) & 1], tid, s_off);
       asm volatile("cp.async.wait_group 1;" ::: "memory");
     } else {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -238,7 +250,7 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
     __syncthreads();
     const uint16_t* buf = tile[t & 1];
     float pt_s = 1.f;
-    if (P.pt_amax != nullptr) {
+    if constexpr (PT) {
       int g = b;
       if (P.pt_group_off != nullptr) {      // the row group holding this tile (groups are 32-row aligned)
         g = 0;
@@ -246,12 +258,7 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
       }
       pt_s = fp8_scale(P.pt_amax[g]);
     }
-    if (P.probs_perm != nullptr && blockIdx.y == 0 && b == 0 && tid < kRows) {
-      const int pp = p0 + tid;
-      const int f = P.src_rows != nullptr ? P.src_rows[pp] : pp;
-      P.probs_perm[pp] = f < 0 ? 0.f : P.probs[f];
-    }
-    if (P.q_row != nullptr) {
+    if constexpr (ROW) {
       const int r = tid >> 2, j = tid & 3;
       const int p = p0 + r;
       float v[32];
@@ -265,23 +272,23 @@ __global__ void __launch_bounds__(128) quant_kernel(const QuantParams P) {
         wv[4 * i + 2] = q.z;
         wv[4 * i + 3] = q.w;
       }
-      const uint32_t blk_max = pair_max_bits(wv, 16);
+      const uint32_t blk_max = PT ? 0u : pair_max_bits(wv, 16);
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
         v[2 * h] = __uint_as_float(wv[h] << 16);
         v[2 * h + 1] = __uint_as_float(wv[h] & 0xffff0000u);
       }
       const int64_t grow = static_cast<int64_t>(b) * P.rows + p;
-      if (P.pt_amax != nullptr)
+      if constexpr (PT)
         quant_store32_pt(v, P.q_row + grow * P.cols + c0 + j * 32, pt_s);
       else
         quant_store32(v, P.q_row + grow * P.cols + c0 + j * 32,
                       P.s_row + sf_offset(P.layout, grow, (c0 >> 5) + j, P.sf_row_rows, P.cols >> 5),
                       blk_max);
     }
-    if (P.q_col != nullptr) {
+    if constexpr (COL) {
       const int warp = tid >> 5;
-      quant_col_block(P, buf, warp * 32, static_cast<int64_t>(b) * P.cols + c0 + warp * 32, p0, tid & 31, pt_s);
+      quant_col_block<PT>(P, buf, warp * 32, static_cast<int64_t>(b) * P.cols + c0 + warp * 32, p0, tid & 31, pt_s);
     }
     if (P.b_row != nullptr) {
       const int r = tid >> 2, j = tid & 3;
@@ -399,10 +406,33 @@ cudaError_t launch_amax(const AmaxParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <bool G, bool R, bool C, bool PT>
+void launch_mode(const QuantParams& p, dim3 grid, cudaStream_t s) {
+  quant_kernel<G, R, C, PT><<<grid, 128, 0, s>>>(p);
+}
+
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s) {
   dim3 grid((p.rows / kRows + kTilesPerCta - 1) / kTilesPerCta, p.cols / kCols, p.batch);
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
-  quant_kernel<<<grid, 128, 0, s>>>(p);
+  const int mode = (p.src_rows != nullptr || p.grp_off != nullptr ? 1 : 0) | (p.q_row != nullptr ? 2 : 0) |
+                   (p.q_col != nullptr ? 4 : 0) | (p.pt_amax != nullptr ? 8 : 0);
+  switch (mode) {
+    case 0: launch_mode<false, false, false, false>(p, grid, s); break;
+    case 1: launch_mode<true, false, false, false>(p, grid, s); break;
+    case 2: launch_mode<false, true, false, false>(p, grid, s); break;
+    case 3: launch_mode<true, true, false, false>(p, grid, s); break;
+    case 4: launch_mode<false, false, true, false>(p, grid, s); break;
+    case 5: launch_mode<true, false, true, false>(p, grid, s); break;
+    case 6: launch_mode<false, true, true, false>(p, grid, s); break;
+    case 7: launch_mode<true, true, true, false>(p, grid, s); break;
+    case 10: launch_mode<false, true, false, true>(p, grid, s); break;
+    case 11: launch_mode<true, true, false, true>(p, grid, s); break;
+    case 12: launch_mode<false, false, true, true>(p, grid, s); break;
+    case 13: launch_mode<true, false, true, true>(p, grid, s); break;
+    case 14: launch_mode<false, true, true, true>(p, grid, s); break;
+    case 15: launch_mode<true, true, true, true>(p, grid, s); break;
+    default: return cudaErrorInvalidValue;   // a per-tensor scale without any code output
+  }
   count_launch();
   return cudaGetLastError();
 }
