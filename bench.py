@@ -256,23 +256,35 @@ def time_router(m, x, k: int, E: int, dev, stream, reps: int = 20) -> dict:
     ws_r = torch.empty(m.mxg_router_bwd_workspace_bytes(T, H, E, k), dtype=torch.uint8, device=dev)
     dw_r = torch.empty((E, H), dtype=torch.float32, device=dev)
     lo, ri, rp = m.mxg_router_fwd(x, w_r, k)
+    # the calls are recorded in CUDA graphs and the replays timed: each call
+    # is a few tens of microseconds of GPU work, shorter than its host-side
+    # launch path, so back-to-back eager calls would time the host
+    fp_out = m.mxg_router_fwd_permute(x, w_r, k, st_r)
+    graphs = []
+    side = torch.cuda.Stream(dev)
+    with torch.cuda.stream(side):
+        for _ in range(2):       # warm-up (module loading, function attributes) before capture
+            m.mxg_router_fwd(x, w_r, k, logits=lo, ids=ri, probs=rp)
+            m.mxg_router_bwd(x, w_r, ri, rp, dprobs, dx_r, st_r, dw_router=dw_r, workspace=ws_r)
+    torch.cuda.synchronize(dev)
+    for call in (lambda: m.mxg_router_fwd(x, w_r, k, logits=lo, ids=ri, probs=rp),
+                 lambda: m.mxg_router_fwd_permute(x, w_r, k, st_r),
+                 lambda: m.mxg_router_bwd(x, w_r, ri, rp, dprobs, dx_r, st_r, dw_router=dw_r, workspace=ws_r)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                call()
+        graphs.append(g)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize(dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    for _ in range(3):
-        m.mxg_router_fwd(x, w_r, k, logits=lo, ids=ri, probs=rp)
-        m.mxg_router_fwd_permute(x, w_r, k, st_r)
-        m.mxg_router_bwd(x, w_r, ri, rp, dprobs, dx_r, st_r, dw_router=dw_r, workspace=ws_r)
-    torch.cuda.synchronize(dev)
     ev[0].record(stream)
-    for _ in range(reps):
-        m.mxg_router_fwd(x, w_r, k, logits=lo, ids=ri, probs=rp)
-    ev[1].record(stream)
-    for _ in range(reps):
-        m.mxg_router_fwd_permute(x, w_r, k, st_r)
-    ev[2].record(stream)
-    for _ in range(reps):
-        m.mxg_router_bwd(x, w_r, ri, rp, dprobs, dx_r, st_r, dw_router=dw_r, workspace=ws_r)
-    ev[3].record(stream)
+    for i, g in enumerate(graphs):
+        g.replay()
+        ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
+    del fp_out
     if int(st_r.item()) != 0:
         raise SystemExit(f"bench: router status {m.status_string(int(st_r.item()))}")
     f_ms, fp_ms, b_ms = (ev[i].elapsed_time(ev[i + 1]) / reps for i in range(3))

@@ -477,6 +477,39 @@ size_t mxg_mlp_grouped_saved_bytes(int R, int H, int I, int E);
 size_t mxg_mlp_grouped_workspace_bytes(int R, int H, int I, int E);
 int mxg_grouped_mlp_fwd_grouped(const mxg_mlp_grouped_fwd_args* args, void* stream);
 
+/* The same forward on grouped rows that arrive already quantised: row-wise
+ * MXFP8 codes and E8M0 scales (blocks of 32 along H), e.g. what an
+ * expert-parallel dispatcher shipped instead of bf16 rows (about half the
+ * bytes).  Inference only: the weight gradient of W_gate_up needs x quantised
+ * in blocks of 32 tokens of each expert's group, which row-wise codes cannot
+ * give, so there is no backward for this call.  [Grouped] "Reducing memory
+ * pressure with MXFP8" (MXFP8 operands) and "Grouping fragmented expert
+ * workloads" (tokens grouped with split_sizes).
+ *   xq   uint8 [R][H] E4M3 codes (device, 32-byte aligned)
+ *   xs   uint8 [R][H/32] E8M0 scales, canonical layout (device, 4-byte aligned)
+ *   the rest as mxg_mlp_grouped_fwd_args without x and save_for_backward;
+ *   saved and workspace sized by the mxg_mlp_grouped_* queries.
+ * Given the codes and scales mxg_mxfp8_quantize writes for x's rows, y equals
+ * mxg_grouped_mlp_fwd_grouped's bit for bit. */
+typedef struct {
+  int32_t R, H, I, E;
+  const uint8_t* xq;           /* E4M3 codes [R][H], grouped by expert       */
+  const uint8_t* xs;           /* E8M0 scales [R][H/32]                      */
+  const int32_t* split_sizes;  /* int32 [E] (device, input)                  */
+  const float* probs;          /* fp32 [R]                                   */
+  const uint16_t* w_gate_up;   /* bf16 [E][2I][H]                            */
+  const uint16_t* w_down;      /* bf16 [E][H][I]                             */
+  uint16_t* y;                 /* out bf16 [R][H]                            */
+  void* saved;
+  uint64_t saved_bytes;
+  void* workspace;
+  uint64_t workspace_bytes;
+  int32_t* dev_status;
+  const void* weight_cache;
+  uint64_t weight_cache_bytes;
+} mxg_mlp_grouped_fwd_mx_args;
+int mxg_grouped_mlp_fwd_grouped_mx(const mxg_mlp_grouped_fwd_mx_args* args, void* stream);
+
 /* Weight cache: the four MXFP8 weight tensors the MLP needs (W_gate_up
  * quantised along H and along 2I, W_down along I and along H, codes and
  * tensor-core scale layout), written once per weight update and reused by

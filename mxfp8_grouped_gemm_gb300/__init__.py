@@ -11,6 +11,6 @@ from ._lib import (  # noqa: F401
     WeightCache, mxg_mlp_quantize_weights, mxg_mlp_saved_bytes_cached, mxg_bench_mxfp8_mma_peak,
     mxg_mxfp8_grouped_rows_capacity, mxg_mxfp8_quantize_grouped, mxg_gather_rows, mxg_combine,
     mxg_mlp_grouped_saved_bytes, mxg_mlp_grouped_workspace_bytes, mxg_grouped_mlp_fwd_grouped,
-    mxg_router_fwd_permute,
+    mxg_router_fwd_permute, mxg_grouped_mlp_fwd_grouped_mx,
 )
 from .layer import GroupedExperts, GroupedMLP  # noqa: F401

@@ -38,7 +38,7 @@ EXPORTS = [
     "mxg_mlp_workspace_view", "mxg_mlp_weight_cache_view", "mxg_bench_mxfp8_mma_peak",
     "mxg_mxfp8_grouped_rows_capacity", "mxg_mxfp8_quantize_grouped", "mxg_gather_rows", "mxg_combine",
     "mxg_mlp_grouped_saved_bytes", "mxg_mlp_grouped_workspace_bytes", "mxg_grouped_mlp_fwd_grouped",
-    "mxg_router_fwd_permute",
+    "mxg_router_fwd_permute", "mxg_grouped_mlp_fwd_grouped_mx",
 ]
 
 FWD_STAGES = ["permute", "quant_weights", "quant_x", "gate_up", "down", "combine"]
@@ -70,6 +70,15 @@ class MlpGroupedFwdArgs(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_uint64), ("save_for_backward", ctypes.c_int32),
                 ("dev_status", ctypes.c_void_p), ("weight_cache", ctypes.c_void_p),
                 ("weight_cache_bytes", ctypes.c_uint64)]
+
+
+class MlpGroupedFwdMxArgs(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("xq", ctypes.c_void_p), ("xs", ctypes.c_void_p), ("split_sizes", ctypes.c_void_p),
+                ("probs", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("saved", ctypes.c_void_p), ("saved_bytes", ctypes.c_uint64),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_uint64), ("dev_status", ctypes.c_void_p),
+                ("weight_cache", ctypes.c_void_p), ("weight_cache_bytes", ctypes.c_uint64)]
 
 
 class MlpBwdArgs(ctypes.Structure):
@@ -146,6 +155,7 @@ def lib() -> ctypes.CDLL:
         "mxg_mlp_grouped_workspace_bytes": (SZ, [I32, I32, I32, I32]),
         "mxg_grouped_mlp_fwd_grouped": (I32, [ctypes.POINTER(MlpGroupedFwdArgs), P]),
         "mxg_router_fwd_permute": (I32, [P, P, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P]),
+        "mxg_grouped_mlp_fwd_grouped_mx": (I32, [ctypes.POINTER(MlpGroupedFwdMxArgs), P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -560,3 +570,26 @@ def mxg_router_fwd_permute(x: torch.Tensor, w_router: torch.Tensor, k: int, dev_
         _ptr(out["row_of_src"]), _ptr(out["padded_offsets"]), _ptr(ws), ws_bytes,
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
     return logits, ids, probs, out
+
+
+def mxg_grouped_mlp_fwd_grouped_mx(xq, xs, split_sizes, probs, w_gate_up, w_down, saved, workspace, dev_status,
+                                   H: int, y=None, weight_cache: WeightCache | None = None, stream=None):
+    """Inference forward on grouped rows given as row-wise MXFP8: codes xq uint8
+    [R, H] and canonical scales xs uint8 [R, H/32]; returns y [R, H]."""
+    R = xq.shape[0]
+    if weight_cache is not None:
+        E, I = weight_cache.E, weight_cache.I
+    else:
+        E, N2, _ = w_gate_up.shape
+        I = N2 // 2
+    y = torch.empty((R, H), dtype=torch.bfloat16, device=xq.device) if y is None else y
+    a = MlpGroupedFwdMxArgs(R, H, I, E, _ptr(xq, torch.uint8, "xq"), _ptr(xs, torch.uint8, "xs"),
+                            _ptr(split_sizes, torch.int32, "split_sizes"), _ptr(probs, torch.float32, "probs"),
+                            _ptr(_bits(w_gate_up), torch.int16, "w_gate_up"), _ptr(_bits(w_down), torch.int16, "w_down"),
+                            _ptr(_bits(y), torch.int16, "y"), _ptr(saved, torch.uint8, "saved"), saved.numel(),
+                            _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+                            _ptr(dev_status, torch.int32, "dev_status"),
+                            None if weight_cache is None else _ptr(weight_cache.buffer, torch.uint8, "weight_cache"),
+                            0 if weight_cache is None else weight_cache.buffer.numel())
+    _check("mxg_grouped_mlp_fwd_grouped_mx", lib().mxg_grouped_mlp_fwd_grouped_mx(ctypes.byref(a), _stream(stream)))
+    return y

@@ -563,13 +563,20 @@ const void* mxg_mlp_workspace_view(const void* workspace, int T, int H, int I, i
   }
 }
 
-static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
+// xq_pre / xs_pre (nullable): x already quantised row-wise (codes [T][H] and
+// canonical scales [T][H/32], one row per token; used with k = 1); the x stage
+// then places those rows into the padded layout instead of quantising
+// (inference only: no token-column codes of x exist for a backward).
+static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream, const uint8_t* xq_pre = nullptr,
+                    const uint8_t* xs_pre = nullptr) {
   if (!A) return MXG_ERR_ARG;
   const int T = A->T, H = A->H, I = A->I, E = A->E, k = A->k;
   if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MXG_ERR_ARG;
   if (!mlp_shape_ok(T, H, I, E, k)) return MXG_ERR_SHAPE;
   const bool cached = A->weight_cache != nullptr;
-  if (!A->x || !A->ids || !A->probs || (!cached && (!A->w_gate_up || !A->w_down)) || !A->y || !A->split_sizes ||
+  const bool pre = xq_pre != nullptr;
+  if (pre && (xs_pre == nullptr || A->save_for_backward != 0)) return MXG_ERR_ARG;
+  if ((!A->x && !pre) || !A->ids || !A->probs || (!cached && (!A->w_gate_up || !A->w_down)) || !A->y || !A->split_sizes ||
       !A->saved || !A->workspace || !A->dev_status)
     return MXG_ERR_ARG;
   if (!aligned32(A->x) || !aligned32(A->ids) || !aligned32(A->probs) || !aligned32(A->w_gate_up) ||
@@ -627,7 +634,13 @@ static int fwd_impl(const mxg_mlp_fwd_args* A, int stage, void* stream) {
 
   // F3: gather x into the padded per-expert layout and quantise (row-wise along
   // H for the gate-up GEMM; token-column-wise for the gate-up weight gradient)
-  if (run(MXG_FWD_QUANT_X)) {
+  if (run(MXG_FWD_QUANT_X) && pre) {
+    NvtxRange nvtx("mxg.fwd.place_x");
+    MXG_TRY(launch_place_rows(xq_pre, xs_pre, static_cast<int64_t>(T) * k, at<int32_t>(sv, pl.prow_src), pl.Rc,
+                              poff + E, H, at<uint8_t>(ws, pl.xq), at<uint8_t>(ws, pl.sxq), pl.Rc, A->probs,
+                              at<float>(sv, pl.probs_perm), st, s));
+  }
+  if (run(MXG_FWD_QUANT_X) && !pre) {
   NvtxRange nvtx("mxg.fwd.quant_x");
   QuantParams xq{};
   xq.x = A->x;
@@ -957,6 +970,46 @@ size_t mxg_mlp_grouped_saved_bytes(int R, int H, int I, int E) { return mxg_mlp_
 size_t mxg_mlp_grouped_workspace_bytes(int R, int H, int I, int E) {
   if (!mlp_shape_ok(R, H, I, E, 1)) return 0;
   return static_cast<size_t>(Plan(R, H, I, E, 1).ws_bytes() + grouped_tail(R, E));
+}
+
+int mxg_grouped_mlp_fwd_grouped_mx(const mxg_mlp_grouped_fwd_mx_args* G, void* stream) {
+  if (!G) return MXG_ERR_ARG;
+  const int R = G->R, H = G->H, I = G->I, E = G->E;
+  if (R <= 0 || H <= 0 || I <= 0 || E <= 0) return MXG_ERR_ARG;
+  if (!mlp_shape_ok(R, H, I, E, 1)) return MXG_ERR_SHAPE;
+  if (!G->xq || !G->xs || !G->split_sizes || !G->workspace || !G->dev_status) return MXG_ERR_ARG;
+  if (!aligned32(G->xq) || !aligned32(G->split_sizes) || !aligned32(G->workspace)) return MXG_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(G->xs) & 3u) return MXG_ERR_ALIGN;
+  const Plan pl(R, H, I, E, 1);
+  if (G->workspace_bytes < static_cast<uint64_t>(pl.ws_bytes() + grouped_tail(R, E))) return MXG_ERR_WORKSPACE;
+  NvtxRange nvtx("mxg.grouped_mlp_fwd_grouped_mx");
+  int32_t* ids = at<int32_t>(G->workspace, pl.ws_bytes());
+  int32_t* split_out = at<int32_t>(G->workspace, pl.ws_bytes() + align_up(4 * static_cast<int64_t>(R), kAlign));
+  mxg_mlp_fwd_args A{};
+  A.T = R;
+  A.H = H;
+  A.I = I;
+  A.E = E;
+  A.k = 1;
+  A.x = nullptr;
+  A.ids = ids;
+  A.probs = G->probs;
+  A.w_gate_up = G->w_gate_up;
+  A.w_down = G->w_down;
+  A.y = G->y;
+  A.split_sizes = split_out;
+  A.saved = G->saved;
+  A.saved_bytes = G->saved_bytes;
+  A.workspace = G->workspace;
+  A.workspace_bytes = static_cast<uint64_t>(pl.ws_bytes());
+  A.save_for_backward = 0;
+  A.dev_status = G->dev_status;
+  A.weight_cache = G->weight_cache;
+  A.weight_cache_bytes = G->weight_cache_bytes;
+  const int pre = fwd_impl(&A, MXG_FWD_NUM_STAGES, stream, G->xq, G->xs);
+  if (pre != MXG_OK) return pre;
+  MXG_TRY(launch_expand_splits(G->split_sizes, E, R, ids, G->dev_status, static_cast<cudaStream_t>(stream)));
+  return fwd_impl(&A, -1, stream, G->xq, G->xs);
 }
 
 int mxg_grouped_mlp_fwd_grouped(const mxg_mlp_grouped_fwd_args* G, void* stream) {

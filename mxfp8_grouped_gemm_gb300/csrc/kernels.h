@@ -126,6 +126,14 @@ cudaError_t launch_combine(const uint16_t* src, const int32_t* prow_of_src, int 
 // 4); an index outside [0, src_rows * div) gives a zero row and MXG_ERR_INDEX.
 cudaError_t launch_gather_rows(const void* src, int64_t src_rows, int64_t row_bytes, const int32_t* index, int div,
                                int64_t rows, void* dst, int32_t* status, cudaStream_t s);
+// Pre-quantised rows into the padded row layout: padded row p takes codes
+// row f = src[p] of q (cols bytes) and its cols/32 canonical scale bytes,
+// written as codes [rows][cols] and tensor-core-layout scales (sf_rows rows);
+// f < 0 (padding) gives zero codes and scales.  probs_perm[p] = probs[f]
+// (0 for padding) when probs is given.
+cudaError_t launch_place_rows(const uint8_t* q, const uint8_t* s, int64_t src_rows, const int32_t* src, int64_t rows,
+                              const int32_t* rows_valid, int cols, uint8_t* q_out, uint8_t* s_out, int64_t sf_rows,
+                              const float* probs, float* probs_perm, int32_t* status, cudaStream_t st);
 // ids[r] = the group of row r, from split sizes [E] (rows of group e follow
 // those of e - 1); sizes that are negative or do not sum to R give
 // MXG_ERR_OFFSETS and ids -1 for the rows no group covers.

@@ -5,7 +5,9 @@
 // eight experts per token.  Read as one bias-free linear layer H -> E on the
 // token's hidden state, the logits are a [T, H] x [H, E] contraction: one CTA
 // takes 128 tokens, TMA streams its x rows and the router rows 64 columns at
-// a time into a shared-memory ring, one thread issues tcgen05.mma kind::f16
+// a time into a shared-memory ring (each CTA starting at its own column so
+// the CTAs do not all read the same router rows at once), one thread issues
+// tcgen05.mma kind::f16
 // (bf16 operands, fp32 accumulators; M = 128 tokens, N = E rounded up to a
 // multiple of 16, the extra router rows read as zeros), and the accumulators
 // land in TMEM with one token per lane.  Four epilogue warps read them back
@@ -55,6 +57,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * kRtM;
   const int nk = H / kRtK;
+  // Every CTA reads the same router rows: started at the same contraction
+  // step, all of them would ask for the same few L2 lines at once.  Each CTA
+  // starts at its own step and wraps around.
+  const int kb0 = static_cast<int>((static_cast<int64_t>(blockIdx.x) * 5) % nk);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -92,9 +98,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
           break;
         }
         uint8_t* sA = sm + st * C::kStageBytes;
+        const int kc = (kb0 + kb) % nk * kRtK;
         mbar_arrive_expect_tx(&full[st], C::kStageBytes);
-        tma_load_2d(sA, &tmX, kb * kRtK, t0, &full[st]);
-        tma_load_2d(sA + C::kABytes, &tmW, kb * kRtK, 0, &full[st]);
+        tma_load_2d(sA, &tmX, kc, t0, &full[st]);
+        tma_load_2d(sA + C::kABytes, &tmW, kc, 0, &full[st]);
       }
       if (*abort_flag) {  // let copies already in flight land before the CTA exits
         const uint64_t g0 = globaltimer_ns();

@@ -77,7 +77,42 @@ __global__ void __launch_bounds__(1024) expand_splits_kernel(const int32_t* __re
   }
 }
 
+// One CTA per padded row: 16-byte code chunks by the threads, then the
+// row's scale bytes, each to its tensor-core-layout position.
+__global__ void __launch_bounds__(128) place_rows_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
+                                                         int64_t src_rows, const int32_t* __restrict__ src,
+                                                         const int32_t* rows_valid, int cols,
+                                                         uint8_t* __restrict__ q_out, uint8_t* __restrict__ s_out,
+                                                         int64_t sf_rows, const float* __restrict__ probs,
+                                                         float* __restrict__ probs_perm, int32_t* status) {
+  const int64_t p = blockIdx.x;
+  if (rows_valid != nullptr && p >= *rows_valid) return;
+  int f = src[p];
+  if (f >= src_rows) {
+    if (threadIdx.x == 0) report(status, MXG_ERR_INDEX);
+    f = -1;
+  }
+  const int chunks = cols / 16;
+  uint4* dq = reinterpret_cast<uint4*>(q_out + p * cols);
+  const uint4* sq = f >= 0 ? reinterpret_cast<const uint4*>(q + static_cast<int64_t>(f) * cols) : nullptr;
+  for (int c = threadIdx.x; c < chunks; c += blockDim.x) dq[c] = f >= 0 ? __ldg(sq + c) : make_uint4(0u, 0u, 0u, 0u);
+  const int nb = cols / 32;
+  for (int b = threadIdx.x; b < nb; b += blockDim.x)
+    s_out[sf_mma_offset(p, b, sf_rows)] = f >= 0 ? s[static_cast<int64_t>(f) * nb + b] : uint8_t{0};
+  if (probs_perm != nullptr && threadIdx.x == 0) probs_perm[p] = f >= 0 ? probs[f] : 0.f;
+}
+
 }  // namespace
+
+cudaError_t launch_place_rows(const uint8_t* q, const uint8_t* s, int64_t src_rows, const int32_t* src, int64_t rows,
+                              const int32_t* rows_valid, int cols, uint8_t* q_out, uint8_t* s_out, int64_t sf_rows,
+                              const float* probs, float* probs_perm, int32_t* status, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  place_rows_kernel<<<static_cast<unsigned>(rows), 128, 0, st>>>(q, s, src_rows, src, rows_valid, cols, q_out, s_out,
+                                                                 sf_rows, probs, probs_perm, status);
+  count_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather_rows(const void* src, int64_t src_rows, int64_t row_bytes, const int32_t* index, int div,
                                int64_t rows, void* dst, int32_t* status, cudaStream_t s) {

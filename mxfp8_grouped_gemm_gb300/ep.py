@@ -26,11 +26,14 @@ The backward mirrors it: dy rows go out like x rows (step 3-4), dx rows and the
 per-row d(probability) come back (6-7); each rank keeps its own experts'
 weight gradients.
 
-The dispatched payload is the bf16 rows, not MXFP8 codes: the wgrad operand
-of W_gate_up is x quantised in blocks of 32 tokens of an expert's group, and
+The dispatched payload for training is the bf16 rows: the wgrad operand of
+W_gate_up is x quantised in blocks of 32 tokens of an expert's group, and
 that group is only complete on the receiving rank, so the quantisation has
-to happen there from the bf16 values (row-wise codes shipped from the source
-could serve the forward GEMM, but not the token-column blocks).
+to happen there from the bf16 values.  An inference forward (payload
+"mxfp8") ships the F3 output instead: each token's row-wise MXFP8 codes and
+E8M0 scales (H + H/32 bytes instead of 2H), quantised once per token on the
+source rank; row-wise blocks lie inside a row, so these are the codes the
+receiving rank would have computed, and the forward is the same bit for bit.
 
 The exchange runs through a communicator object (TorchComm wraps a
 torch.distributed process group: NCCL for CUDA tensors, gloo for CPU ones);
@@ -86,6 +89,14 @@ class CudaOps:
     def permute(self, ids: torch.Tensor, E: int) -> dict:
         return _lib.mxg_route_permute(ids, E, self.status)
 
+    def quantize_rows(self, x: torch.Tensor):
+        """Row-wise MXFP8 of x [T, H] (blocks of 32 along H): codes uint8
+        [T, H] and canonical scales uint8 [T, H/32]."""
+        T, H = x.shape
+        off = torch.tensor([0, T], dtype=torch.int32, device=self.device)
+        q = _lib.mxg_mxfp8_quantize_grouped(x, off, self.status, row=True, col=False)
+        return q["q_row"][:T], q["s_row"].view(-1, H // 32)[:T]
+
     def counts_to_host(self, split_sizes: torch.Tensor) -> np.ndarray:
         return split_sizes.cpu().numpy().astype(np.int64)
 
@@ -109,6 +120,13 @@ class CudaOps:
             return x_rows.new_empty((0, self.H))
         split = torch.from_numpy(split_local.astype(np.int32)).to(self.device)
         return self.experts.forward(x_rows, split, probs_rows, w_gate_up, w_down).clone()
+
+    def experts_forward_mx(self, xq_rows, xs_rows, split_local: np.ndarray, probs_rows, w_gate_up, w_down):
+        self._R = -1                                  # inference: nothing saved for a backward
+        if xq_rows.shape[0] == 0:
+            return torch.empty((0, self.H), dtype=torch.bfloat16, device=self.device)
+        split = torch.from_numpy(split_local.astype(np.int32)).to(self.device)
+        return self.experts.forward_mx(xq_rows, xs_rows, split, probs_rows, w_gate_up, w_down).clone()
 
     def experts_backward(self, dy_rows):
         if self._R == 0:
@@ -173,7 +191,11 @@ class ExpertParallelMLP:
         self.ops = ops if ops is not None else CudaOps(self.max_rows, H, I, self.E_local, device=device)
 
     # ---------------------------------------------------------------- forward
-    def forward(self, x, ids, probs, w_gate_up, w_down):
+    def forward(self, x, ids, probs, w_gate_up, w_down, payload: str = "bf16"):
+        """payload "bf16": the rows as bf16 (training); "mxfp8": each token's
+        row-wise codes and scales (inference: no backward after it)."""
+        if payload not in ("bf16", "mxfp8"):
+            raise ValueError(f"payload must be 'bf16' or 'mxfp8', got {payload!r}")
         ops, G, n, k = self.ops, self.G, self.E_local, self.k
         perm = ops.permute(ids, self.E)
         split = ops.counts_to_host(perm["split_sizes"])                 # [E] rows per expert, this rank's tokens
@@ -181,27 +203,37 @@ class ExpertParallelMLP:
         counts_recv = self.comm.all_to_all_counts(counts_send)          # [G, n]: from source s, per local expert
         send_splits = counts_send.sum(axis=1).tolist()
         recv_splits = counts_recv.sum(axis=1).tolist()
-        x_rows = ops.gather(x, perm["src_of_row"], div=k)               # permuted order = destination order
-        p_rows = ops.gather(probs.reshape(-1), perm["src_of_row"])
-        x_recv = self.comm.all_to_all_rows(x_rows, send_splits, recv_splits)
+        p_rows = ops.gather(probs.reshape(-1), perm["src_of_row"])    # permuted order = destination order
         p_recv = self.comm.all_to_all_rows(p_rows, send_splits, recv_splits)
         order = receive_order(counts_recv)
         order_t = ops.index(order)
-        x_g = ops.gather(x_recv, order_t)
         p_g = ops.gather(p_recv, order_t)
         split_local = counts_recv.sum(axis=0)                           # rows per local expert
-        y_g = ops.experts_forward(x_g, split_local, p_g, w_gate_up, w_down)
+        x_g = None
+        if payload == "bf16":
+            x_rows = ops.gather(x, perm["src_of_row"], div=k)
+            x_g = ops.gather(self.comm.all_to_all_rows(x_rows, send_splits, recv_splits), order_t)
+            y_g = ops.experts_forward(x_g, split_local, p_g, w_gate_up, w_down)
+        else:
+            xq_tok, xs_tok = ops.quantize_rows(x)                      # once per token, on the source rank
+            q_rows = ops.gather(xq_tok, perm["src_of_row"], div=k)
+            s_rows = ops.gather(xs_tok, perm["src_of_row"], div=k)
+            q_g = ops.gather(self.comm.all_to_all_rows(q_rows, send_splits, recv_splits), order_t)
+            s_g = ops.gather(self.comm.all_to_all_rows(s_rows, send_splits, recv_splits), order_t)
+            y_g = ops.experts_forward_mx(q_g, s_g, split_local, p_g, w_gate_up, w_down)
         back_t = ops.index(inverse(order))
         y_back = self.comm.all_to_all_rows(ops.gather(y_g, back_t), recv_splits, send_splits)
         y = ops.combine(y_back, perm["row_of_src"], k)
         self._ctx = {"perm": perm, "send_splits": send_splits, "recv_splits": recv_splits, "order_t": order_t,
                      "back_t": back_t, "split": split, "counts_recv": counts_recv, "x_grouped": x_g,
-                     "split_local": split_local}
+                     "split_local": split_local, "payload": payload}
         return y
 
     # --------------------------------------------------------------- backward
     def backward(self, dy):
         ops, c, k = self.ops, self._ctx, self.k
+        if c["payload"] != "bf16":
+            raise RuntimeError("a forward with the mxfp8 payload is inference only: it has no backward")
         perm = c["perm"]
         dy_rows = ops.gather(dy, perm["src_of_row"], div=k)
         dy_recv = self.comm.all_to_all_rows(dy_rows, c["send_splits"], c["recv_splits"])

@@ -157,6 +157,21 @@ class GroupedExperts:
                                                 save_for_backward=save_for_backward,
                                                 weight_cache=self.weight_cache if cached else None, stream=stream)
 
+    def forward_mx(self, xq, xs, split_sizes, probs, w_gate_up=None, w_down=None, y=None, stream=None):
+        """Inference forward on grouped rows given as row-wise MXFP8 (codes xq
+        uint8 [R, H], canonical scales xs uint8 [R, H/32]); no backward."""
+        R = xq.shape[0]
+        if R > self.R_max:
+            raise ValueError(f"{R} rows exceed the buffers' {self.R_max}")
+        cached = w_gate_up is None and w_down is None
+        if cached and self.weight_cache is None:
+            raise ValueError("no weights given and no weight cache: call quantize_weights first")
+        self._R = -1                                   # nothing saved for a backward
+        return _lib.mxg_grouped_mlp_fwd_grouped_mx(xq, xs, split_sizes, probs.reshape(R), w_gate_up, w_down,
+                                                   self.saved, self.workspace, self.dev_status, self.H, y=y,
+                                                   weight_cache=self.weight_cache if cached else None,
+                                                   stream=stream)
+
     def backward(self, dy, dx=None, dw_gate_up=None, dw_down=None, dprobs=None, main_grad=None, stream=None):
         """dy bf16 [R, H] (per row) -> dx [R, H], dW_gate_up, dW_down, dprobs [R, 1]."""
         R = dy.shape[0]

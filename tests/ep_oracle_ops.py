@@ -57,6 +57,17 @@ class OracleOps:
                                   for e in range(self.E_local)]
         return torch.from_numpy(self.ctx["y"])
 
+    def quantize_rows(self, x):
+        c, s = mx.quantize_blocks(x.numpy())
+        return torch.from_numpy(c), torch.from_numpy(s)
+
+    def experts_forward_mx(self, xq_rows, xs_rows, split_local, probs_rows, w_gate_up, w_down):
+        # the dequantised rows lie on the MX grid with the same block maxima,
+        # so the oracle's quantisation reproduces exactly these codes
+        x = mx.dequantize_blocks(xq_rows.numpy(), xs_rows.numpy())
+        self.seen_mx = {"codes": xq_rows.numpy().copy(), "scales": xs_rows.numpy().copy()}
+        return self.experts_forward(torch.from_numpy(x), split_local, probs_rows, w_gate_up, w_down)
+
     def experts_backward(self, dy_rows):
         g = moe.mlp_bwd(self.ctx, dy_rows.numpy())
         return (torch.from_numpy(g["dx"]), torch.from_numpy(g["dw_gate_up"]), torch.from_numpy(g["dw_down"]),

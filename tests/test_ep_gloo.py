@@ -38,7 +38,7 @@ def _case(G, T_loc, H, I, E, k, seed):
             if isinstance(v, torch.Tensor)}
 
 
-def _rank(rank, G, port, shape, seed, out_q):
+def _rank(rank, G, port, shape, seed, out_q, payload="bf16"):
     import sys
     sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
     from ep_oracle_ops import OracleOps
@@ -55,7 +55,10 @@ def _rank(rank, G, port, shape, seed, out_q):
         layer = ep.ExpertParallelMLP(comm, T_loc, H, I, E, k, ops=OracleOps(H, I, n))
         mine = slice(rank * n, (rank + 1) * n)
         y = layer.forward(torch.from_numpy(c["x"][sl]), torch.from_numpy(ids), torch.from_numpy(probs),
-                          c["w_gate_up"][mine], c["w_down"][mine])
+                          c["w_gate_up"][mine], c["w_down"][mine], payload=payload)
+        if payload == "mxfp8":
+            out_q.put((rank, {"y": y.numpy(), "split": layer._ctx["split"], **layer.ops.seen_mx}))
+            return
         dx, dwgu, dwd, dprobs = layer.backward(torch.from_numpy(c["dy"][sl]))
         seen = layer.ops.seen
         out_q.put((rank, {"y": y.numpy(), "dx": dx.numpy(), "dwgu": dwgu.numpy(), "dwd": dwd.numpy(),
@@ -65,14 +68,11 @@ def _rank(rank, G, port, shape, seed, out_q):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("G", [2, 4])
-def test_expert_parallel_equals_single_rank(G):
-    T_loc, H, I, E, k = 96, 64, 96, 8, 2
-    seed = 40 + G
+def _run_ranks(G, shape, seed, payload="bf16"):
     ctx_mp = mp.get_context("spawn")
     q = ctx_mp.Queue()
     port = _port()
-    procs = [ctx_mp.Process(target=_rank, args=(r, G, port, (T_loc, H, I, E, k), seed, q)) for r in range(G)]
+    procs = [ctx_mp.Process(target=_rank, args=(r, G, port, shape, seed, q, payload)) for r in range(G)]
     for p in procs:
         p.start()
     res = {}
@@ -90,6 +90,14 @@ def test_expert_parallel_equals_single_rank(G):
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
+    return res
+
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_expert_parallel_equals_single_rank(G):
+    T_loc, H, I, E, k = 96, 64, 96, 8, 2
+    seed = 40 + G
+    res = _run_ranks(G, (T_loc, H, I, E, k), seed)
 
     c = _case(G, T_loc, H, I, E, k, seed)
     ids, probs = moe.route_topk(c["logits"], k)
@@ -134,3 +142,25 @@ def test_receive_order_and_partition():
     # received: s0: e0 e0 e2 | s1: e0 e1 e1 e1 -> grouped: e0 (s0 s0 s1), e1 (s1 s1 s1), e2 (s0)
     assert order.tolist() == [0, 1, 3, 4, 5, 6, 2]
     assert np.array_equal(ep.inverse(order)[order], np.arange(7))
+
+
+def test_expert_parallel_mxfp8_payload_inference():
+    """The inference forward that ships each token's row-wise MXFP8 codes and
+    scales: every rank receives, bit for bit, the codes and scales the single
+    rank computes for its experts' grouped rows, and y equals the single-rank
+    oracle's."""
+    G, T_loc, H, I, E, k = 2, 96, 64, 96, 8, 2
+    seed = 47
+    res = _run_ranks(G, (T_loc, H, I, E, k), seed, payload="mxfp8")
+    c = _case(G, T_loc, H, I, E, k, seed)
+    ids, probs = moe.route_topk(c["logits"], k)
+    ctx = moe.mlp_fwd(c["x"], ids, probs, c["w_gate_up"], c["w_down"])
+    perm = ctx["perm"]
+    n = E // G
+    for r in range(G):
+        o = res[r]
+        a, b = perm["offsets"][r * n], perm["offsets"][(r + 1) * n]
+        codes, scales = mx.quantize_blocks(ctx["x_perm"][a:b])
+        assert np.array_equal(o["codes"], codes) and np.array_equal(o["scales"], scales)
+        sl = slice(r * T_loc, (r + 1) * T_loc)
+        np.testing.assert_allclose(o["y"], ctx["y"][sl], rtol=1e-12, atol=1e-14)

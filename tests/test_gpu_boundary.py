@@ -198,3 +198,28 @@ def test_pregrouped_reports_bad_split_sizes():
                w["w_gate_up"].cuda(), w["w_down"].cuda())                 # sums to 255, not 256
     torch.cuda.synchronize()
     assert ex.status() == 17                                              # MXG_ERR_OFFSETS
+
+
+def test_pregrouped_mx_forward_equals_the_bf16_rows_forward():
+    """The inference forward on grouped rows given as row-wise MXFP8 codes and
+    scales (mxg_grouped_mlp_fwd_grouped_mx) gives the same y, bit for bit, as
+    the forward on the bf16 rows those codes come from."""
+    m = require_gpu()
+    T, H, I, E, k = 300, 256, 384, 6, 2
+    inp = synthetic.make_case(T, H, I, E, k, seed=35, empty_experts=(2,))
+    d = {n: inp[n].cuda() for n in ("logits", "x", "w_gate_up", "w_down")}
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ids, probs = m.mxg_route_topk(d["logits"], k)
+    pm = m.mxg_route_permute(ids, E, st)
+    R = T * k
+    x_g = m.mxg_gather_rows(d["x"], pm["src_of_row"], st, div=k)
+    p_g = m.mxg_gather_rows(probs.reshape(-1), pm["src_of_row"], st)
+    off = torch.tensor([0, R], dtype=torch.int32, device="cuda")
+    q = m.mxg_mxfp8_quantize_grouped(x_g, off, st, row=True, col=False)
+    xq, xs = q["q_row"][:R], q["s_row"].view(-1, H // 32)[:R]
+    ex = m.GroupedExperts(R, H, I, E)
+    y_ref = ex.forward(x_g, pm["split_sizes"], p_g, d["w_gate_up"], d["w_down"], save_for_backward=False).clone()
+    y_mx = ex.forward_mx(xq, xs, pm["split_sizes"], p_g, d["w_gate_up"], d["w_down"]).clone()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and ex.status() == 0
+    assert torch.equal(y_mx, y_ref)
