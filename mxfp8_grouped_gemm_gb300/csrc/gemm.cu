@@ -27,7 +27,8 @@
 //                 With BN = 256 the accumulator is single-buffered, so dH is
 //                 first parked as bf16 pairs in spare TMEM columns and the
 //                 accumulator released; the math then overlaps the next
-//                 tile's MMAs.
+//                 tile's MMAs, and the dGU codes leave through per-warp
+//                 shared tiles by TMA stores.
 //
 // CTA = 12 warps: warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs,
 // warp 2 copies each stage's scale factors into TMEM, warps 4-11 run the
@@ -81,9 +82,15 @@ struct Cfg {
   // leaves free); BN = 128 dSwiGLU keeps a 32 x 33 fp32 transpose tile per warp.
   static constexpr bool kDsTmem = EPI == 2 && BN == 256;
   static constexpr uint32_t kDsCol = 384;
-  static constexpr int kXposeBytes = EPI == 2 && BN == 128 ? 8 * 32 * 33 * 4
+  // MXFP8 dSwiGLU at BN = 256 stores its dGU codes by TMA through a 4 KB
+  // shared tile per epilogue warp (epi_dswiglu_tma), beside the 2.5 KB
+  // scratch: a five-stage ring.
+  static constexpr bool kDsTma = EPI == 2 && BN == 256 && OPK == OPK_MX;
+  static constexpr int kDsWarpBytes = 4096 + 32 * 20 * 4;
+  static constexpr int kXposeBytes = kDsTma                                    ? 8 * kDsWarpBytes
+                                     : EPI == 2 && BN == 128                   ? 8 * 32 * 33 * 4
                                      : (EPI == 1 || EPI == 2) && OPK == OPK_MX ? 8 * 32 * 20 * 4
-                                                                             : 0;
+                                                                               : 0;
   static constexpr int kCtrlBytes = 2048;
   static constexpr int kStages = (232448 - 1024 - kCtrlBytes - kXposeBytes) / kStageBytes > 8
                                      ? 8
@@ -144,6 +151,32 @@ __device__ __forceinline__ uint32_t row_quant32(const float (&h)[32], uint8_t* d
   return sb;
 }
 
+// Row-wise MX of one thread's 32 values into a 32-row x 32-byte shared tile
+// for a TMA store: row `lane` at lane·32, its two 16-byte halves swapped when
+// bit 2 of the row is set (the tensor map's 32-byte swizzle: conflict-free).
+// Returns the scale byte.
+__device__ __forceinline__ uint32_t row_quant32_staged(const float (&h)[32], uint8_t* tile, int lane) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+  const uint32_t sb = mx_scale_byte(f2u(amax));
+  const float2 inv = make_float2(mx_inv_scale(sb), mx_inv_scale(sb));
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float2 t = mul2(make_float2(h[i], h[i + 1]), inv);
+    v[i] = t.x;
+    v[i + 1] = t.y;
+  }
+  uint32_t w[8];
+  encode32(v, w);
+  const int sw = (lane >> 2) & 1;
+  uint8_t* row = tile + lane * 32;
+  *reinterpret_cast<uint4*>(row + (sw << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(row + ((sw ^ 1) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+  return sb;
+}
+
 // Column-wise MX of the warp's 32 x 32 block (lane l holds row tok0 + l; for
 // each column col0 + i the 32 rows form one block, tok0 32-aligned and inside
 // one expert group; codes go to qc[(col0 + i) * ld + tok0 + row]) through a
@@ -187,6 +220,12 @@ __device__ __forceinline__ void col_quant32_xpose(const float (&h)[32], float* x
 // half-warps cover the 32 banks once.  The halves' maxima meet in one shuffle
 // and each lane stores its 16 codes as one 16-byte run of the transposed
 // output (lanes l and l + 16 fill one 32-byte sector).
+//
+// STAGED: the codes go to a 32-column x 32-byte shared tile for a TMA store
+// instead (column c = 16·pass + cl at c·32, its two 16-byte halves swapped
+// when bit 2 of c is set: the tensor map's 32-byte swizzle, so the eight lanes
+// of each store phase cover the 32 banks once); qc and ld are then unused.
+template <bool STAGED = false>
 __device__ __forceinline__ void col_quant32_slots(const float (&h)[32], float* slot, int pitch, uint8_t* qc,
                                                   uint8_t* sc, int64_t ld, int64_t sc_rows, int64_t col0,
                                                   int64_t tok0, int lane) {
@@ -223,7 +262,12 @@ __device__ __forceinline__ void col_quant32_slots(const float (&h)[32], float* s
     // v[j] holds row j ^ (4g): for g = 1 the words of rows 0-3 / 4-7 (and 8-11 / 12-15) trade places
     const uint4 out = g ? make_uint4(w[1], w[0], w[3], w[2]) : make_uint4(w[0], w[1], w[2], w[3]);
     const int64_t col = col0 + 16 * pass + cl;
-    *reinterpret_cast<uint4*>(qc + col * ld + tok0 + 16 * g) = out;
+    if constexpr (STAGED) {
+      const int c = 16 * pass + cl;
+      *reinterpret_cast<uint4*>(qc + c * 32 + ((g ^ ((c >> 2) & 1)) << 4)) = out;
+    } else {
+      *reinterpret_cast<uint4*>(qc + col * ld + tok0 + 16 * g) = out;
+    }
     if (g == 0) sc[sf_mma_offset(col, tok0 >> 5, sc_rows)] = static_cast<uint8_t>(sb);
   }
 }
@@ -518,18 +562,14 @@ __device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& 
 }
 
 
-// BN = 256: drain the thread's 128 dH columns, park them as 64 packed bf16
-// pairs in the warp's own TMEM columns (tstage: this warp's lanes, columns
-// kDsCol + 64·hf ..), release the accumulator, then run the dSwiGLU epilogue
-// from there while the next tile's MMAs fill the accumulator.  `slots` is the
-// warp's 32 x 20-word scratch for the column-wise quantiser.
+// BN = 256: drain the thread's 128 dH columns and park them as 64 packed
+// bf16 pairs in the warp's own TMEM columns (tstage: this warp's lanes,
+// columns kDsCol + 64·hf ..), then release the accumulator, so the dSwiGLU
+// math runs from there while the next tile's MMAs fill the accumulator.
 template <int OPK>
-__device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q,
-                                                   int lane, int hf, const AccRelease& tempty, uint32_t tstage,
-                                                   float* slots) {
+__device__ __forceinline__ void park_dh(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int hf, int lane,
+                                        const AccRelease& tempty, uint32_t tstage) {
   constexpr int COLS = 128;
-  const int64_t tok0 = tc.m0 + q * 32;
-  const int64_t r = tok0 + lane;
   const float f = tile_scale<OPK>(P, tc);         // per-tensor FP8: accumulators -> dH
 #pragma unroll
   for (int c = 0; c < COLS / 32; c += 2) {
@@ -554,70 +594,146 @@ __device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const Tile
   }
   tmem_st_wait();
   release_acc(tempty, lane);
+}
+
+// The parked dH of 32-column chunk c as fp32.
+__device__ __forceinline__ void unpark_dh(uint32_t tstage, int c, float (&dh)[32]) {
+  uint32_t w[16];
+  tmem_ld_32x32b_x16(tstage + 16 * c, w);
+  tmem_ld_wait();
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    dh[2 * m] = u2f(w[m] << 16);
+    dh[2 * m + 1] = u2f(w[m] & 0xffff0000u);
+  }
+}
+
+// dSwiGLU of 32 columns of one row: dg, du (into u) and the d(prob) partial
+// sum_i dH g s u.  s = sigmoid(g), sl = silu(g) = g s,
+// d silu(g)/dg = s (1 + g (1 - s)) = s + sl (1 - s); pairs of columns as
+// packed fp32 pairs.
+__device__ __forceinline__ void dswiglu32(const float (&dh)[32], const float (&g)[32], float (&u)[32], float p,
+                                          float2& dp2, float (&dg)[32]) {
+  const float2 one2 = make_float2(1.f, 1.f), p2 = make_float2(p, p);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float2 g2 = make_float2(g[i], g[i + 1]), u2 = make_float2(u[i], u[i + 1]);
+    const float2 dh2 = make_float2(dh[i], dh[i + 1]);
+    const float2 d2 = add2(one2, make_float2(__expf(-g2.x), __expf(-g2.y)));
+    const float2 s2 = make_float2(__fdividef(1.f, d2.x), __fdividef(1.f, d2.y));
+    const float2 sl2 = mul2(g2, s2);
+    const float2 t2 = mul2(dh2, u2);
+    dp2 = fma2(t2, sl2, dp2);
+    const float2 dg2 = mul2(mul2(t2, p2), fma2(sl2, sub2(one2, s2), s2));
+    const float2 du2 = mul2(mul2(dh2, p2), sl2);
+    dg[i] = dg2.x;
+    dg[i + 1] = dg2.y;
+    u[i] = du2.x;
+    u[i + 1] = du2.y;
+  }
+}
+
+// BF16 and per-tensor FP8 dgrad-down at BN = 256: dH parked in TMEM, the
+// saved g|u read with plain loads, dGU written in bf16 (row-major, and
+// transposed for the weight gradient; FP8: with the expert's amax).
+template <int OPK>
+__device__ __forceinline__ void epi_dswiglu_staged(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q,
+                                                   int lane, int hf, const AccRelease& tempty, uint32_t tstage) {
+  constexpr int COLS = 128;
+  const int64_t tok0 = tc.m0 + q * 32;
+  const int64_t r = tok0 + lane;
+  park_dh<OPK>(P, tc, tb, hf, lane, tempty, tstage);
   const float p = P.probs_perm[r];
   const int64_t I = P.I;
   const int j0 = tc.nt * 256 + hf * COLS;
   float2 dp2 = make_float2(0.f, 0.f);
-  const float2 one2 = make_float2(1.f, 1.f), p2 = make_float2(p, p);
   uint32_t gmax = 0;
 #pragma unroll 1
   for (int c = 0; c < COLS / 32; ++c) {
     const int64_t col = j0 + c * 32;
     float dh[32], g[32], u[32], dg[32];
-    {
-      uint32_t w[16];
-      tmem_ld_32x32b_x16(tstage + 16 * c, w);
-      tmem_ld_wait();
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        dh[2 * m] = u2f(w[m] << 16);
-        dh[2 * m + 1] = u2f(w[m] & 0xffff0000u);
-      }
-    }
+    unpark_dh(tstage, c, dh);
     load_bf16_32(P.gu_save + r * (2 * I) + col, g);
     load_bf16_32(P.gu_save + r * (2 * I) + I + col, u);
-#pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      // lanes i, i + 1 as packed pairs; s = sigmoid(g), sl = silu(g),
-      // d silu(g)/dg = s (1 + g (1 - s)) = s + sl (1 - s)
-      const float2 g2 = make_float2(g[i], g[i + 1]), u2 = make_float2(u[i], u[i + 1]);
-      const float2 dh2 = make_float2(dh[i], dh[i + 1]);
-      const float2 d2 = add2(one2, make_float2(__expf(-g2.x), __expf(-g2.y)));
-      const float2 s2 = make_float2(__fdividef(1.f, d2.x), __fdividef(1.f, d2.y));
-      const float2 sl2 = mul2(g2, s2);
-      const float2 t2 = mul2(dh2, u2);
-      dp2 = fma2(t2, sl2, dp2);
-      const float2 dg2 = mul2(mul2(t2, p2), fma2(sl2, sub2(one2, s2), s2));
-      const float2 du2 = mul2(mul2(dh2, p2), sl2);
-      dg[i] = dg2.x;
-      dg[i + 1] = dg2.y;
-      u[i] = du2.x;
-      u[i + 1] = du2.y;
-    }
-    if constexpr (OPK != OPK_MX) {
-      gmax = max(gmax, row_store_bf16_amax(dg, P.y_row + r * P.y_row_ld + col));
-      gmax = max(gmax, row_store_bf16_amax(u, P.y_row + r * P.y_row_ld + I + col));
-      if (P.y_col != nullptr) {
-        col_store_bf16(dg, P.y_col, P.y_col_ld, col, tok0, lane);
-        col_store_bf16(u, P.y_col, P.y_col_ld, I + col, tok0, lane);
-      }
-    } else {
-      uint32_t sb = row_quant32(dg, P.q_out + r * P.q_out_ld + col);
-      P.s_out[sf_mma_offset(r, col >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-      col_quant32_slots(dg, slots, 20, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, col, tok0, lane);
-      sb = row_quant32(u, P.q_out + r * P.q_out_ld + I + col);
-      P.s_out[sf_mma_offset(r, (I + col) >> 5, P.s_out_rows)] = static_cast<uint8_t>(sb);
-      col_quant32_slots(u, slots, 20, P.qc_out, P.sc_out, P.qc_ld, P.sc_rows, I + col, tok0, lane);
+    dswiglu32(dh, g, u, p, dp2, dg);
+    gmax = max(gmax, row_store_bf16_amax(dg, P.y_row + r * P.y_row_ld + col));
+    gmax = max(gmax, row_store_bf16_amax(u, P.y_row + r * P.y_row_ld + I + col));
+    if (P.y_col != nullptr) {
+      col_store_bf16(dg, P.y_col, P.y_col_ld, col, tok0, lane);
+      col_store_bf16(u, P.y_col, P.y_col_ld, I + col, tok0, lane);
     }
   }
   P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp2.x + dp2.y;
   if constexpr (OPK == OPK_F8) warp_amax_to(P.amax_out + tc.e, gmax, lane);
 }
 
+// The MXFP8 dgrad-down epilogue at BN = 256 stores its dGU codes with TMA,
+// not with per-lane global stores: an epilogue lane owns one row, so a warp's
+// global store touches 32 rows (32 L1 wavefronts per instruction), and with
+// those the SM's L1 data path was the busiest unit of the kernel (LSU
+// wavefronts at 65 % of peak beside the operand stream's 26 %, ncu).  Per
+// epilogue warp, in shared memory:
+//   out  : 4 KB, the chunk's dGU codes, row-wise dg | du (32 rows x 32 bytes
+//          each) and column-wise dg | du (32 columns x 32 tokens each),
+//          32-byte swizzle, stored by TMA while the next chunk is computed;
+//   slots: the column quantiser's 32 x 20-word scratch.
+// The saved g|u stay plain 32-byte loads: reading them by TMA as well (4 KB
+// more per warp, a four-stage ring) measured slower.
+struct DsTma {
+  uint8_t* out;
+  float* slots;
+};
+
+__device__ __forceinline__ void epi_dswiglu_tma(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
+                                                int hf, const AccRelease& tempty, uint32_t tstage, const DsTma& d,
+                                                const CUtensorMap* tmQ, const CUtensorMap* tmQC) {
+  constexpr int COLS = 128;
+  const int tok0 = tc.m0 + q * 32;
+  const int64_t r = tok0 + lane;
+  park_dh<OPK_MX>(P, tc, tb, hf, lane, tempty, tstage);
+  const float p = P.probs_perm[r];
+  const int I = P.I;
+  const int j0 = tc.nt * 256 + hf * COLS;
+  const uint16_t* gr = P.gu_save + r * (2 * static_cast<int64_t>(I));
+  float2 dp2 = make_float2(0.f, 0.f);
+  uint32_t sbg = 0, sbu = 0;
+#pragma unroll 1
+  for (int c = 0; c < COLS / 32; ++c) {
+    const int col = j0 + c * 32;
+    float dh[32], g[32], u[32], dg[32];
+    unpark_dh(tstage, c, dh);
+    load_bf16_32(gr + col, g);
+    load_bf16_32(gr + I + col, u);
+    dswiglu32(dh, g, u, p, dp2, dg);
+    // the previous chunk's code stores have finished reading the staging tiles
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+    sbg |= row_quant32_staged(dg, d.out, lane) << (8 * c);
+    sbu |= row_quant32_staged(u, d.out + 1024, lane) << (8 * c);
+    col_quant32_slots<true>(dg, d.slots, 20, d.out + 2048, P.sc_out, 0, P.sc_rows, col, tok0, lane);
+    col_quant32_slots<true>(u, d.slots, 20, d.out + 3072, P.sc_out, 0, P.sc_rows, I + col, tok0, lane);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmQ, d.out, col, tok0);
+      tma_store_2d(tmQ, d.out + 1024, I + col, tok0);
+      tma_store_2d(tmQC, d.out + 2048, tok0, col);
+      tma_store_2d(tmQC, d.out + 3072, tok0, I + col);
+      bulk_commit_group();
+    }
+  }
+  // the row's four scale bytes of each half are adjacent (j0 and I are
+  // multiples of 128, so the first block index is a multiple of 4)
+  *reinterpret_cast<uint32_t*>(P.s_out + sf_mma_offset(r, j0 >> 5, P.s_out_rows)) = sbg;
+  *reinterpret_cast<uint32_t*>(P.s_out + sf_mma_offset(r, (I + j0) >> 5, P.s_out_rows)) = sbu;
+  P.dp_part[r * P.dp_ld + 2 * tc.nt + hf] = dp2.x + dp2.y;
+}
+
 template <int BN, int EPI, bool KG, bool PAIR, int OPK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, const GemmArgs P) {
+                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQC, const GemmArgs P) {
   using C = Cfg<BN, EPI, PAIR, OPK>;
   constexpr int CG = C::CG;
   extern __shared__ uint8_t smem_raw[];
@@ -668,6 +784,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (PAIR) {
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
+    }
+    if (C::kDsTma) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmQC);
     }
   }
   __syncthreads();
@@ -953,6 +1073,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q * 32 + lane;
     float* my_xpose = xpose + (warp - 4) * 32 * 33;
     uint32_t acc = 0, acc_phase = 0;
+    DsTma dt{};
+    if constexpr (C::kDsTma) {
+      uint8_t* base = reinterpret_cast<uint8_t*>(xpose);
+      const int w = warp - 4;
+      dt.out = base + w * 4096;
+      dt.slots = reinterpret_cast<float*>(base + 8 * 4096 + w * 32 * 20 * 4);
+    }
     for (int64_t t = tile0; t < total; t += tstep) {
       const TileCoord tc = decode(t);
       if (tc.num_k == 0) {
@@ -989,11 +1116,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (EPI == EPI_SWIGLU) {
         epi_swiglu<BN, OPK>(P, tc, tb, q, lane, hf, rel, xpose + (warp - 4) * 32 * 20);
       } else if constexpr (EPI == EPI_DSWIGLU) {
-        if constexpr (BN == 256)
-          epi_dswiglu_staged<OPK>(P, tc, tb, q, lane, hf, rel,
-                                  tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kDsCol + hf * 64,
-                                  xpose + (warp - 4) * 32 * 20);
-        else epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
+        const uint32_t tstage = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kDsCol + hf * 64;
+        if constexpr (C::kDsTma) {
+          epi_dswiglu_tma(P, tc, tb, q, lane, hf, rel, tstage, dt, &tmQ, &tmQC);
+        } else if constexpr (BN == 256) {
+          epi_dswiglu_staged<OPK>(P, tc, tb, q, lane, hf, rel, tstage);
+        } else {
+          epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
+        }
       } else if constexpr (EPI == EPI_ACC_F32) {
         epi_acc_f32<BN>(P, tc, tb, row, hf, rel, lane);
       } else {
@@ -1003,6 +1133,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc = 0;
         acc_phase ^= 1;
       }
+    }
+    if constexpr (C::kDsTma) {
+      // the code stores have completed before the CTA exits
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
     }
   }
 
@@ -1057,6 +1192,21 @@ bool encode_bf16(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, u
   const cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D tensor map over [rows][cols] elements of `esize` bytes, rows
+// `row_bytes` apart, with a box_cols x box_rows box and the given swizzle.
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int64_t cols, int64_t rows,
+               int64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw,
+               CUtensorMapL2promotion l2) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1123,7 +1273,17 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
     if (!encode_atoms(&tsb, g.sb, (g.b_rows / 128) * (g.b_cols / 128), EPI == EPI_SWIGLU ? 1 : 2))
       return cudaErrorInvalidValue;
   }
-  err = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, g);
+  // MXFP8 dSwiGLU at BN = 256: the row-wise dGU codes ([rows][2I]) and the
+  // column-wise ones ([2I][token capacity]), 32 x 32-byte boxes, 32-byte swizzle
+  CUtensorMap tq = ta, tqc = ta;
+  if (C::kDsTma) {
+    if (!encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.q_out, g.q_out_ld, g.M, g.q_out_ld, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
+        !encode_2d(&tqc, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.qc_out, g.qc_ld, g.sc_rows, g.qc_ld, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE))
+      return cudaErrorInvalidValue;
+  }
+  err = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, tq, tqc, g);
   count_launch();
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
