@@ -697,13 +697,32 @@ __device__ __forceinline__ void epi_dswiglu_tma(const GemmArgs& P, const TileCoo
   const uint16_t* gr = P.gu_save + r * (2 * static_cast<int64_t>(I));
   float2 dp2 = make_float2(0.f, 0.f);
   uint32_t sbg = 0, sbu = 0;
+  // the saved g|u of chunk c + 1 are requested (as raw bf16 pairs) before
+  // chunk c's math, so their latency overlaps it: 64 experts top-8 0.932
+  // (paired), the Mixtral layer unchanged
+  uint32_t gw[16], uw[16];
+  ld_global_nc_v8(gr + j0, gw);
+  ld_global_nc_v8(gr + j0 + 16, gw + 8);
+  ld_global_nc_v8(gr + I + j0, uw);
+  ld_global_nc_v8(gr + I + j0 + 16, uw + 8);
 #pragma unroll 1
   for (int c = 0; c < COLS / 32; ++c) {
     const int col = j0 + c * 32;
     float dh[32], g[32], u[32], dg[32];
     unpark_dh(tstage, c, dh);
-    load_bf16_32(gr + col, g);
-    load_bf16_32(gr + I + col, u);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      g[2 * j] = u2f(gw[j] << 16);
+      g[2 * j + 1] = u2f(gw[j] & 0xffff0000u);
+      u[2 * j] = u2f(uw[j] << 16);
+      u[2 * j + 1] = u2f(uw[j] & 0xffff0000u);
+    }
+    if (c + 1 < COLS / 32) {
+      ld_global_nc_v8(gr + col + 32, gw);
+      ld_global_nc_v8(gr + col + 48, gw + 8);
+      ld_global_nc_v8(gr + I + col + 32, uw);
+      ld_global_nc_v8(gr + I + col + 48, uw + 8);
+    }
     dswiglu32(dh, g, u, p, dp2, dg);
     // the previous chunk's code stores have finished reading the staging tiles
     if (lane == 0) bulk_wait_group_read<0>();

@@ -144,6 +144,17 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
+// Loads from a cluster shared-memory address (this or another CTA of the cluster).
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_shared_cluster_s32(uint32_t cluster_addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
 // 4-byte store into another CTA's shared memory that completes 4 bytes of
 // transaction count on that CTA's mbarrier (both cluster addresses).
 __device__ __forceinline__ void st_async_complete_tx(uint32_t cluster_addr, uint32_t value, uint32_t cluster_bar) {
