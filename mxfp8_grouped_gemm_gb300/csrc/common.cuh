@@ -127,8 +127,9 @@ __device__ __forceinline__ void encode32_x4(const float (&v)[32], uint32_t (&w)[
 // rounds of a warp argmax (ties to the lower id) pick the experts in
 // descending order, then softmax over the chosen logits.  `row` may be global
 // or shared memory.
-__device__ __forceinline__ void warp_topk_softmax(const float* row, int E, int k, int lane, int32_t* ids_out,
-                                                  float* probs_out) {
+// Returns, on lane j < k, the id it wrote to ids_out[j].
+__device__ __forceinline__ int warp_topk_softmax(const float* row, int E, int k, int lane, int32_t* ids_out,
+                                                 float* probs_out) {
   float v[8];
   uint32_t taken = 0;
 #pragma unroll
@@ -173,6 +174,47 @@ __device__ __forceinline__ void warp_topk_softmax(const float* row, int E, int k
     ids_out[lane] = my_id;
     probs_out[lane] = w / sum;
   }
+  return my_id;
+}
+
+// The same route by one thread (E <= 64, k <= 8): k passes over the row pick
+// the largest untaken logit (ties to the lower id), and the softmax sums the
+// chosen weights in the order of the warp version's butterfly
+// ((w0 + w4) + (w2 + w6)) + ((w1 + w5) + (w3 + w7)) (missing terms are
+// zeros), so ids and probabilities are bit-identical to warp_topk_softmax.
+// Writes ids_out[0..k) and probs_out[0..k); sel[0..k) receives the ids.
+__device__ __forceinline__ void thread_topk_softmax(const float* row, int E, int k, int32_t* ids_out,
+                                                   float* probs_out, int (&sel)[8]) {
+  float val[8];
+  uint64_t taken = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    sel[j] = 0;
+    val[j] = 0.f;
+    if (j >= k) continue;
+    float bv = -FLT_MAX;
+    int bi = -1;
+    for (int e = 0; e < E; ++e) {
+      const float v = row[e];
+      if (!((taken >> e) & 1ull) && (bi < 0 || v > bv)) {
+        bv = v;
+        bi = e;
+      }
+    }
+    taken |= 1ull << bi;
+    val[j] = bv;
+    sel[j] = bi;
+  }
+  float w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = j < k ? expf(val[j] - val[0]) : 0.f;
+  const float sum = ((w[0] + w[4]) + (w[2] + w[6])) + ((w[1] + w[5]) + (w[3] + w[7]));
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < k) {
+      ids_out[j] = sel[j];
+      probs_out[j] = w[j] / sum;
+    }
 }
 
 // ------------------------------------------------------- scale-factor layout

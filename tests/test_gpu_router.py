@@ -132,3 +132,18 @@ def test_router_fwd_permute_equals_router_then_permute(T, H, E, k):
     assert torch.equal(lo, lo2) and torch.equal(ids, ids2) and torch.equal(probs, probs2)
     for name in pm2:
         assert torch.equal(pm[name], pm2[name]), name
+
+
+@pytest.mark.parametrize("T,H,E,k", CASES + [(1000, 512, 64, 8), (300, 256, 33, 3), (500, 256, 16, 4)])
+def test_router_route_equals_route_topk_on_its_logits(T, H, E, k):
+    """The router's fused route (one thread per token while E k <= 64, one
+    warp per token beyond) is bit-identical to mxg_route_topk (one
+    warp per token) on the logits the router wrote: same ids, same
+    probabilities (the softmax sums in the same order)."""
+    m = require_gpu()
+    x, w = _inputs(T, H, E, 400 + E)
+    logits, ids, probs = m.mxg_router_fwd(x.cuda(), w.cuda(), k)
+    ids2, probs2 = m.mxg_route_topk(logits, k)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids2)
+    assert torch.equal(probs, probs2)
