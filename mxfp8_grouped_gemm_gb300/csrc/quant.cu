@@ -27,18 +27,20 @@ constexpr int kStride = kCols + 8;   // bf16 per smem row (272 bytes: 16-byte al
 // groups.
 __device__ __forceinline__ int chunk_pos(int r, int c) { return c ^ (((r >> 3) & 3) << 1); }
 
-// Largest magnitude of packed bf16 pairs, as fp32 bits (non-negative bf16
-// values compare like floats; the sign bits are cleared first).
+// Largest magnitude of packed bf16 pairs, as fp32 bits: max.xorsign.abs
+// keeps the larger magnitude of each lane pair (its sign bit, the XOR of the
+// operands' signs, is cleared at the end), one instruction per word.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 __device__ __forceinline__ uint32_t pair_max_bits(const uint32_t* w, int n) {
-  const uint32_t z = 0;
-  __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162*>(&z);
+  uint32_t m = w[0];
 #pragma unroll
-  for (int i = 0; i < n; ++i) {
-    const uint32_t a = w[i] & 0x7fff7fffu;
-    m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162*>(&a));
-  }
-  const uint32_t mm = *reinterpret_cast<const uint32_t*>(&m);
-  return max(mm << 16, mm & 0xffff0000u);
+  for (int i = 1; i < n; ++i) m = absmax_bf16x2(m, w[i]);
+  m &= 0x7fff7fffu;
+  return max(m << 16, m & 0xffff0000u);
 }
 
 __device__ __forceinline__ void quant_store32(float (&v)[32], uint8_t* dst, uint8_t* sdst, uint32_t amax) {
