@@ -12,7 +12,19 @@ namespace mxg {
 
 namespace {
 
-// One thread per 8 consecutive columns (16-byte vectors) of one token.
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& q) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] += __uint_as_float(w[i] << 16);
+    acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// One thread per 8 consecutive columns (16-byte vectors) of one token.  Up to
+// eight slots, the thread requests all its row indices and then all its rows
+// before it adds any (the adds still run in slot order), so k loads are in
+// flight per thread instead of one dependent pair at a time.
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ src,
                                                       const int32_t* __restrict__ prow_of_src, int T, int k,
                                                       int H, uint16_t* __restrict__ out, int64_t src_rows,
@@ -25,19 +37,32 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const int pr = prow_of_src[static_cast<int64_t>(t) * k + j];
-    if (pr < 0) continue;
-    if (pr >= src_rows) {
-      if (v == 0) report(status, MXG_ERR_INDEX);
-      continue;
-    }
-    const uint4 q = *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(pr) * H + v * 8);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  if (k <= 8) {
+    int pr[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] += __uint_as_float(w[i] << 16);
-      acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+    for (int j = 0; j < 8; ++j) pr[j] = j < k ? prow_of_src[static_cast<int64_t>(t) * k + j] : -1;
+    uint4 q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (pr[j] >= src_rows) {
+        if (v == 0) report(status, MXG_ERR_INDEX);
+        pr[j] = -1;
+      }
+      q[j] = pr[j] >= 0 ? *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(pr[j]) * H + v * 8)
+                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (pr[j] >= 0) add_bf16x8(acc, q[j]);
+  } else {
+    for (int j = 0; j < k; ++j) {
+      const int pr = prow_of_src[static_cast<int64_t>(t) * k + j];
+      if (pr < 0) continue;
+      if (pr >= src_rows) {
+        if (v == 0) report(status, MXG_ERR_INDEX);
+        continue;
+      }
+      add_bf16x8(acc, *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(pr) * H + v * 8));
     }
   }
   uint4 o;
