@@ -28,15 +28,16 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 
 // --------------------------------------------------------------- permute ----
 constexpr int kChunk = kPermuteChunk;     // flat entries per CTA
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;             // the scan
+constexpr int kWide = 1024;               // count and scatter: a chunk in four passes
 constexpr int kMaxE = 256;
 
-__global__ void __launch_bounds__(kThreads) count_kernel(const PermuteParams P) {
+__global__ void __launch_bounds__(kWide) count_kernel(const PermuteParams P) {
   __shared__ int hist[kMaxE];
-  for (int e = threadIdx.x; e < P.E; e += kThreads) hist[e] = 0;
+  for (int e = threadIdx.x; e < P.E; e += kWide) hist[e] = 0;
   __syncthreads();
   const int base = blockIdx.x * kChunk;
-  for (int i = threadIdx.x; i < kChunk; i += kThreads) {
+  for (int i = threadIdx.x; i < kChunk; i += kWide) {
     const int f = base + i;
     if (f >= P.R) break;
     const int e = P.ids[f];
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(kThreads) count_kernel(const PermuteParams P) 
     else atomicAdd(&hist[e], 1);
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < P.E; e += kThreads) P.counts[blockIdx.x * P.E + e] = hist[e];
+  for (int e = threadIdx.x; e < P.E; e += kWide) P.counts[blockIdx.x * P.E + e] = hist[e];
 }
 
 // One CTA: per-expert totals, exclusive scans (plain and padded) and the
@@ -80,27 +81,32 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const PermuteParams P, i
     for (int b = 0; b < nblk; ++b) P.bases[b * P.E + e] += off[e];
 }
 
-__global__ void __launch_bounds__(kThreads) scatter_kernel(const PermuteParams P) {
+// Stable scatter of one chunk: each pass takes kWide consecutive entries;
+// within a warp, entries of the same expert are ranked by __match_any_sync,
+// warps ahead in the pass by their per-expert counts, and earlier passes and
+// chunks by the running base of each expert.
+__global__ void __launch_bounds__(kWide) scatter_kernel(const PermuteParams P) {
+  constexpr int kWarps = kWide / 32;
   __shared__ int run[kMaxE];
   __shared__ int off[kMaxE + 1];
   __shared__ int poff[kMaxE + 1];
-  __shared__ int wcnt[kThreads / 32][kMaxE];
+  __shared__ int wcnt[kWarps][kMaxE];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = threadIdx.x; e < P.E; e += kThreads) run[e] = P.bases[blockIdx.x * P.E + e];
-  for (int e = threadIdx.x; e <= P.E; e += kThreads) {
+  for (int e = threadIdx.x; e < P.E; e += kWide) run[e] = P.bases[blockIdx.x * P.E + e];
+  for (int e = threadIdx.x; e <= P.E; e += kWide) {
     off[e] = P.offsets[e];
     poff[e] = P.padded_offsets[e];
   }
   const unsigned lt_mask = (1u << lane) - 1u;
   const int base = blockIdx.x * kChunk;
-  for (int it = 0; it < kChunk / kThreads; ++it) {
-    const int f = base + it * kThreads + threadIdx.x;
+  for (int it = 0; it < kChunk / kWide; ++it) {
+    const int f = base + it * kWide + threadIdx.x;
     int e = -1;
     if (f < P.R) {
       e = P.ids[f];
       if (e < 0 || e >= P.E) e = -1;
     }
-    for (int i = threadIdx.x; i < (kThreads / 32) * P.E; i += kThreads) (&wcnt[0][0])[(i / P.E) * kMaxE + i % P.E] = 0;
+    for (int i = threadIdx.x; i < kWarps * P.E; i += kWide) (&wcnt[0][0])[(i / P.E) * kMaxE + i % P.E] = 0;
     __syncthreads();
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lt_mask);
@@ -120,13 +126,13 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const PermuteParams P
       if (P.prow_of_src) P.prow_of_src[f] = -1;
     }
     __syncthreads();
-    for (int ee = threadIdx.x; ee < P.E; ee += kThreads) {
+    for (int ee = threadIdx.x; ee < P.E; ee += kWide) {
       int s = 0;
-      for (int w = 0; w < kThreads / 32; ++w) s += wcnt[w][ee];
+      for (int w = 0; w < kWarps; ++w) s += wcnt[w][ee];
       run[ee] += s;
     }
     __syncthreads();
-    if (base + (it + 1) * kThreads >= P.R) break;
+    if (base + (it + 1) * kWide >= P.R) break;
   }
 }
 
@@ -148,7 +154,7 @@ cudaError_t launch_permute_from_counts(const PermuteParams& p, cudaStream_t s) {
   if (nblk == 0) return cudaSuccess;
   scan_kernel<<<1, kThreads, 0, s>>>(p, nblk);
   count_launch();
-  scatter_kernel<<<nblk, kThreads, 0, s>>>(p);
+  scatter_kernel<<<nblk, kWide, 0, s>>>(p);
   count_launch();
   return cudaGetLastError();
 }
@@ -156,11 +162,11 @@ cudaError_t launch_permute_from_counts(const PermuteParams& p, cudaStream_t s) {
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s) {
   const int nblk = permute_num_blocks(p.R);
   if (nblk == 0) return cudaSuccess;
-  count_kernel<<<nblk, kThreads, 0, s>>>(p);
+  count_kernel<<<nblk, kWide, 0, s>>>(p);
   count_launch();
   scan_kernel<<<1, kThreads, 0, s>>>(p, nblk);
   count_launch();
-  scatter_kernel<<<nblk, kThreads, 0, s>>>(p);
+  scatter_kernel<<<nblk, kWide, 0, s>>>(p);
   count_launch();
   return cudaGetLastError();
 }
