@@ -194,9 +194,11 @@ __device__ __forceinline__ void stage_tile(const uint16_t* xc, int64_t ld_x, int
 // matrix loads (quant_col_block).  The mode (gathered rows, row-wise and
 // column-wise outputs, per-tensor scale) is a template argument, so the tile
 // loop carries no run-time mode tests; the bf16 pass-through outputs of the
-// BF16 path stay run-time options.
+// BF16 path stay run-time options.  Ten CTAs per SM (48 registers, no spills):
+// the kernel waits mostly on shared-memory and shuffle results, and two more
+// CTAs than eight gave the gathered passes 2 % (twelve spill and lose 2-6 %).
 template <bool GATHER, bool ROW, bool COL, bool PT>
-__global__ void __launch_bounds__(128, 8) quant_kernel(const QuantParams P) {
+__global__ void __launch_bounds__(128, 10) quant_kernel(const QuantParams P) {
   __shared__ __align__(16) uint16_t tile[2][kRows * kStride];
   __shared__ int64_t s_off[GATHER ? kTilesPerCta * kRows : 1];
   const int c0 = blockIdx.y * kCols;
