@@ -26,6 +26,17 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
                     probs + static_cast<int64_t>(warp) * k);
 }
 
+// One thread per token while E k <= 64 (thread_topk_softmax: the same ids and
+// probabilities as the warp route, bit for bit).
+__global__ void __launch_bounds__(256) topk_thread_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                          int32_t* __restrict__ ids, float* __restrict__ probs) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  int sel[8];
+  thread_topk_softmax(logits + static_cast<int64_t>(t) * E, E, k, ids + static_cast<int64_t>(t) * k,
+                      probs + static_cast<int64_t>(t) * k, sel);
+}
+
 // --------------------------------------------------------------- permute ----
 constexpr int kChunk = kPermuteChunk;     // flat entries per CTA
 constexpr int kThreads = 256;             // the scan
@@ -139,6 +150,13 @@ __global__ void __launch_bounds__(kWide) scatter_kernel(const PermuteParams P) {
 }  // namespace
 
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* probs, cudaStream_t s) {
+  if (E * k <= 64) {
+    const int grid = (T + 255) / 256;
+    if (grid == 0) return cudaSuccess;
+    topk_thread_kernel<<<grid, 256, 0, s>>>(logits, T, E, k, ids, probs);
+    count_launch();
+    return cudaGetLastError();
+  }
   const int warps_per_block = 8;
   const int grid = (T + warps_per_block - 1) / warps_per_block;
   if (grid == 0) return cudaSuccess;

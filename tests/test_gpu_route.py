@@ -43,3 +43,22 @@ def test_permute_reports_bad_expert_id():
     row_of_src = np_(perm["row_of_src"])
     assert row_of_src[3] == -1 and row_of_src[6] == -1    # dropped entries
     assert int(np_(perm["split_sizes"]).sum()) == 6
+
+
+@pytest.mark.parametrize("T,E,k", [(4096, 8, 2), (1000, 16, 4), (300, 64, 1), (77, 5, 3)])
+def test_thread_route_equals_warp_route(T, E, k):
+    """While E k <= 64 the route runs one thread per token; padding the logits
+    with experts that are never chosen (E + 60 columns of -1e30) sends the same
+    rows through the one-warp-per-token route.  Ids and probabilities must be
+    bit-identical (same picks, same softmax summation order)."""
+    m = require_gpu()
+    rng = np.random.default_rng(7 * T + E)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[: T // 8, -1] = logits[: T // 8, 0]            # ties go to the lower id on both routes
+    padded = np.concatenate([logits, np.full((T, 60), -1e30, np.float32)], axis=1)
+    assert E * k <= 64 < (E + 60) * k
+    ids_t, probs_t = m.mxg_route_topk(torch.from_numpy(logits).cuda(), k)
+    ids_w, probs_w = m.mxg_route_topk(torch.from_numpy(padded).cuda(), k)
+    torch.cuda.synchronize()
+    assert torch.equal(ids_t, ids_w)
+    assert torch.equal(probs_t, probs_w)
