@@ -61,7 +61,7 @@ constexpr int kThreads = 384;
 // with one scale per expert tensor applied in the epilogue.
 enum Opk { OPK_MX = 0, OPK_BF16 = 1, OPK_F8 = 2 };
 
-template <int BN, int EPI, bool PAIR, int OPK = OPK_MX>
+template <int BN, int EPI, bool PAIR, int OPK = OPK_MX, bool KG = false>
 struct Cfg {
   // contraction elements per stage: one 128-byte swizzle row of A and B
   static constexpr int kKElems = OPK == OPK_BF16 ? 64 : 128;
@@ -87,7 +87,12 @@ struct Cfg {
   // scratch: a five-stage ring.
   static constexpr bool kDsTma = EPI == 2 && BN == 256 && OPK == OPK_MX;
   static constexpr int kDsWarpBytes = 4096 + 32 * 20 * 4;
+  // Token-grouped MXFP8 pair GEMMs (the weight gradients) write their bf16 dW,
+  // or add into the fp32 main_grad, by TMA from a 2 KB shared tile per
+  // epilogue warp (epi_kg_tma): the ring keeps six stages.
+  static constexpr bool kKgTma = KG && PAIR && OPK == OPK_MX && (EPI == 0 || EPI == 3);
   static constexpr int kXposeBytes = kDsTma                                    ? 8 * kDsWarpBytes
+                                     : kKgTma                                  ? 8 * 2048
                                      : EPI == 2 && BN == 128                   ? 8 * 32 * 33 * 4
                                      : (EPI == 1 || EPI == 2) && OPK == OPK_MX ? 8 * 32 * 20 * 4
                                                                                : 0;
@@ -451,6 +456,53 @@ __device__ __forceinline__ void epi_acc_f32(const GemmArgs& P, const TileCoord& 
   }
 }
 
+// Token-grouped MXFP8 pair tiles (weight gradients): the thread's 128
+// accumulator columns leave through the warp's 2 KB shared tile, a 32-row x
+// 64-byte box (64-byte swizzle: 16-byte chunk j of row r at
+// (j ^ ((r / 2) % 4)) · 16, conflict-free), by TMA: stored as bf16 dW (four
+// boxes of 32 columns), or added into the fp32 main_grad by the memory system
+// (eight boxes of 16 columns; a tensor-map reduce-add, the same single fp32
+// addition per element as a read-modify-write).  One lane per output row made
+// the per-lane global stores touch 32 rows per instruction.
+template <int BN, bool ACC>
+__device__ __forceinline__ void epi_kg_tma(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int hf,
+                                           const AccRelease& tempty, int lane, uint8_t* stg, const CUtensorMap* tmO) {
+  constexpr int COLS = BN / 2;
+  uint32_t v[COLS / 32][32];
+#pragma unroll
+  for (int c = 0; c < COLS / 32; ++c) tmem_ld_32x32b_x32(tb + hf * COLS + c * 32, v[c]);
+  tmem_ld_wait();
+  release_acc(tempty, lane);
+  const int y = tc.e * P.M + tc.m0 + q * 32;          // this warp's 32 rows of the [E·M][N] output
+  const int x0 = tc.nt * BN + hf * COLS;
+  const int sw = (lane >> 1) & 3;
+  uint8_t* row = stg + lane * 64;
+  constexpr int BOXES = ACC ? COLS / 16 : COLS / 32;    // 64-byte rows: 16 fp32 or 32 bf16
+#pragma unroll
+  for (int bx = 0; bx < BOXES; ++bx) {
+    uint32_t w[16];
+    if constexpr (ACC) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = v[bx / 2][16 * (bx % 2) + i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(u2f(v[bx][2 * i]), u2f(v[bx][2 * i + 1]));
+    }
+    if (lane == 0) bulk_wait_group_read<0>();   // the previous box has been read out of the tile
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4*>(row + ((j ^ sw) << 4)) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (ACC) tma_reduce_add_2d(tmO, stg, x0 + 16 * bx, y);
+      else tma_store_2d(tmO, stg, x0 + 32 * bx, y);
+      bulk_commit_group();
+    }
+  }
+}
+
 // Gate-up tile: accumulator columns [0, BN/2) = gate j0.., [BN/2, BN) = up j0..
 // (j0 = nt * BN/2).  The thread owns BN/4 h columns (half hf).  It drains its
 // accumulator columns into registers, releases the accumulator, then computes
@@ -686,7 +738,7 @@ struct DsTma {
 
 __device__ __forceinline__ void epi_dswiglu_tma(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
                                                 int hf, const AccRelease& tempty, uint32_t tstage, const DsTma& d,
-                                                const CUtensorMap* tmQ, const CUtensorMap* tmQC) {
+                                                const CUtensorMap* tmO1, const CUtensorMap* tmO2) {
   constexpr int COLS = 128;
   const int tok0 = tc.m0 + q * 32;
   const int64_t r = tok0 + lane;
@@ -734,10 +786,10 @@ __device__ __forceinline__ void epi_dswiglu_tma(const GemmArgs& P, const TileCoo
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(tmQ, d.out, col, tok0);
-      tma_store_2d(tmQ, d.out + 1024, I + col, tok0);
-      tma_store_2d(tmQC, d.out + 2048, tok0, col);
-      tma_store_2d(tmQC, d.out + 3072, tok0, I + col);
+      tma_store_2d(tmO1, d.out, col, tok0);
+      tma_store_2d(tmO1, d.out + 1024, I + col, tok0);
+      tma_store_2d(tmO2, d.out + 2048, tok0, col);
+      tma_store_2d(tmO2, d.out + 3072, tok0, I + col);
       bulk_commit_group();
     }
   }
@@ -752,8 +804,8 @@ template <int BN, int EPI, bool KG, bool PAIR, int OPK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQC, const GemmArgs P) {
-  using C = Cfg<BN, EPI, PAIR, OPK>;
+                const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2, const GemmArgs P) {
+  using C = Cfg<BN, EPI, PAIR, OPK, KG>;
   constexpr int CG = C::CG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -804,9 +856,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
     }
-    if (C::kDsTma) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmQC);
+    if (C::kDsTma || C::kKgTma) {
+      tma_prefetch_desc(&tmO1);
+      tma_prefetch_desc(&tmO2);
     }
   }
   __syncthreads();
@@ -1137,12 +1189,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if constexpr (EPI == EPI_DSWIGLU) {
         const uint32_t tstage = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kDsCol + hf * 64;
         if constexpr (C::kDsTma) {
-          epi_dswiglu_tma(P, tc, tb, q, lane, hf, rel, tstage, dt, &tmQ, &tmQC);
+          epi_dswiglu_tma(P, tc, tb, q, lane, hf, rel, tstage, dt, &tmO1, &tmO2);
         } else if constexpr (BN == 256) {
           epi_dswiglu_staged<OPK>(P, tc, tb, q, lane, hf, rel, tstage);
         } else {
           epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
         }
+      } else if constexpr (C::kKgTma) {
+        epi_kg_tma<BN, EPI == EPI_ACC_F32>(P, tc, tb, q, hf, rel, lane,
+                                           reinterpret_cast<uint8_t*>(xpose) + (warp - 4) * 2048, &tmO1);
       } else if constexpr (EPI == EPI_ACC_F32) {
         epi_acc_f32<BN>(P, tc, tb, row, hf, rel, lane);
       } else {
@@ -1153,8 +1208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1;
       }
     }
-    if constexpr (C::kDsTma) {
-      // the code stores have completed before the CTA exits
+    if constexpr (C::kDsTma || C::kKgTma) {
+      // the TMA stores have completed before the CTA exits
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
     }
@@ -1255,7 +1310,7 @@ int num_sms() {
 
 template <int BN, int EPI, bool KG, bool PAIR, int OPK = OPK_MX>
 cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
-  using C = Cfg<BN, EPI, PAIR, OPK>;
+  using C = Cfg<BN, EPI, PAIR, OPK, KG>;
   CUtensorMap ta, tb;
   const int b_box = (EPI == EPI_SWIGLU && !PAIR) ? 128 : C::kBRows;
   if (OPK == OPK_BF16) {
@@ -1295,6 +1350,16 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
   // MXFP8 dSwiGLU at BN = 256: the row-wise dGU codes ([rows][2I]) and the
   // column-wise ones ([2I][token capacity]), 32 x 32-byte boxes, 32-byte swizzle
   CUtensorMap tq = ta, tqc = ta;
+  // token-grouped pair tiles: the [E·M][N] output (bf16 dW, or the fp32
+  // main_grad added into), 32-row x 64-byte boxes, 64-byte swizzle
+  if (C::kKgTma) {
+    const bool acc = EPI == EPI_ACC_F32;
+    if (!encode_2d(&tq, acc ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   acc ? static_cast<const void*>(g.dacc) : static_cast<const void*>(g.d), g.N,
+                   static_cast<int64_t>(g.E) * g.M, static_cast<int64_t>(g.N) * (acc ? 4 : 2), acc ? 16 : 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE))
+      return cudaErrorInvalidValue;
+  }
   if (C::kDsTma) {
     if (!encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.q_out, g.q_out_ld, g.M, g.q_out_ld, 32, 32,
                    CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
