@@ -87,12 +87,15 @@ struct Cfg {
   // scratch: a five-stage ring.
   static constexpr bool kDsTma = EPI == 2 && BN == 256 && OPK == OPK_MX;
   static constexpr int kDsWarpBytes = 4096 + 32 * 20 * 4;
-  // Token-grouped MXFP8 pair GEMMs (the weight gradients) write their bf16 dW,
-  // or add into the fp32 main_grad, by TMA from a 2 KB shared tile per
-  // epilogue warp (epi_kg_tma): the ring keeps six stages.
-  static constexpr bool kKgTma = KG && PAIR && OPK == OPK_MX && (EPI == 0 || EPI == 3);
+  // MXFP8 pair GEMMs with a bf16 epilogue (the weight gradients' dW, down and
+  // dgrad-gate-up when no combine is fused) or the fp32 main_grad epilogue
+  // write by TMA from a 2 KB shared tile per epilogue warp (epi_tma_out): the
+  // ring keeps six stages.
+  // Row-grouped bf16 outputs without a fused combine take the same path (the
+  // fused combine synchronises on the rows in global memory: per-lane stores).
+  static constexpr bool kTmaOut = PAIR && OPK == OPK_MX && (EPI == 0 || (KG && EPI == 3));
   static constexpr int kXposeBytes = kDsTma                                    ? 8 * kDsWarpBytes
-                                     : kKgTma                                  ? 8 * 2048
+                                     : kTmaOut                                  ? 8 * 2048
                                      : EPI == 2 && BN == 128                   ? 8 * 32 * 33 * 4
                                      : (EPI == 1 || EPI == 2) && OPK == OPK_MX ? 8 * 32 * 20 * 4
                                                                                : 0;
@@ -456,7 +459,8 @@ __device__ __forceinline__ void epi_acc_f32(const GemmArgs& P, const TileCoord& 
   }
 }
 
-// Token-grouped MXFP8 pair tiles (weight gradients): the thread's 128
+// MXFP8 pair tiles with a plain output (weight gradients; down and
+// dgrad-gate-up without a fused combine): the thread's 128
 // accumulator columns leave through the warp's 2 KB shared tile, a 32-row x
 // 64-byte box (64-byte swizzle: 16-byte chunk j of row r at
 // (j ^ ((r / 2) % 4)) · 16, conflict-free), by TMA: stored as bf16 dW (four
@@ -464,8 +468,8 @@ __device__ __forceinline__ void epi_acc_f32(const GemmArgs& P, const TileCoord& 
 // (eight boxes of 16 columns; a tensor-map reduce-add, the same single fp32
 // addition per element as a read-modify-write).  One lane per output row made
 // the per-lane global stores touch 32 rows per instruction.
-template <int BN, bool ACC>
-__device__ __forceinline__ void epi_kg_tma(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int hf,
+template <int BN, bool KG, bool ACC>
+__device__ __forceinline__ void epi_tma_out(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int hf,
                                            const AccRelease& tempty, int lane, uint8_t* stg, const CUtensorMap* tmO) {
   constexpr int COLS = BN / 2;
   uint32_t v[COLS / 32][32];
@@ -473,7 +477,8 @@ __device__ __forceinline__ void epi_kg_tma(const GemmArgs& P, const TileCoord& t
   for (int c = 0; c < COLS / 32; ++c) tmem_ld_32x32b_x32(tb + hf * COLS + c * 32, v[c]);
   tmem_ld_wait();
   release_acc(tempty, lane);
-  const int y = tc.e * P.M + tc.m0 + q * 32;          // this warp's 32 rows of the [E·M][N] output
+  // this warp's 32 rows: of the [E·M][N] weight gradient, or of the padded rows
+  const int y = (KG ? tc.e * P.M : 0) + tc.m0 + q * 32;
   const int x0 = tc.nt * BN + hf * COLS;
   const int sw = (lane >> 1) & 3;
   uint8_t* row = stg + lane * 64;
@@ -856,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
     }
-    if (C::kDsTma || C::kKgTma) {
+    if (C::kDsTma || C::kTmaOut) {
       tma_prefetch_desc(&tmO1);
       tma_prefetch_desc(&tmO2);
     }
@@ -1195,9 +1200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           epi_dswiglu<BN>(P, tc, tb, q, lane, hf, rel, my_xpose);
         }
-      } else if constexpr (C::kKgTma) {
-        epi_kg_tma<BN, EPI == EPI_ACC_F32>(P, tc, tb, q, hf, rel, lane,
-                                           reinterpret_cast<uint8_t*>(xpose) + (warp - 4) * 2048, &tmO1);
+      } else if (C::kTmaOut && (KG || P.cmb_out == nullptr)) {
+        epi_tma_out<BN, KG, EPI == EPI_ACC_F32>(P, tc, tb, q, hf, rel, lane,
+                                               reinterpret_cast<uint8_t*>(xpose) + (warp - 4) * 2048, &tmO1);
       } else if constexpr (EPI == EPI_ACC_F32) {
         epi_acc_f32<BN>(P, tc, tb, row, hf, rel, lane);
       } else {
@@ -1208,7 +1213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1;
       }
     }
-    if constexpr (C::kDsTma || C::kKgTma) {
+    if constexpr (C::kDsTma || C::kTmaOut) {
       // the TMA stores have completed before the CTA exits
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
@@ -1352,12 +1357,14 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
   CUtensorMap tq = ta, tqc = ta;
   // token-grouped pair tiles: the [E·M][N] output (bf16 dW, or the fp32
   // main_grad added into), 32-row x 64-byte boxes, 64-byte swizzle
-  if (C::kKgTma) {
+  if (C::kTmaOut && (KG || g.cmb_out == nullptr)) {
     const bool acc = EPI == EPI_ACC_F32;
+    // token-grouped: [E·M][N] with rows N apart; row-grouped: [M][N] with rows ldd apart
+    const int64_t rows = KG ? static_cast<int64_t>(g.E) * g.M : g.M;
+    const int64_t ld = KG ? g.N : g.ldd;
     if (!encode_2d(&tq, acc ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                   acc ? static_cast<const void*>(g.dacc) : static_cast<const void*>(g.d), g.N,
-                   static_cast<int64_t>(g.E) * g.M, static_cast<int64_t>(g.N) * (acc ? 4 : 2), acc ? 16 : 32, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE))
+                   acc ? static_cast<const void*>(g.dacc) : static_cast<const void*>(g.d), g.N, rows,
+                   ld * (acc ? 4 : 2), acc ? 16 : 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE))
       return cudaErrorInvalidValue;
   }
   if (C::kDsTma) {
