@@ -400,9 +400,13 @@ __device__ __forceinline__ void fused_combine(const GemmArgs& P, const TileCoord
   }
 }
 
+// stg / tmO (MXFP8 pair tiles with a fused combine): the warp's 2 KB shared
+// tile and the output's tensor map; the rows then leave by TMA and complete
+// before the combine's counters see them (otherwise stg is null).
 template <int BN, bool KG, int OPK>
 __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int row, int hf,
-                                         const AccRelease& tempty, int lane) {
+                                         const AccRelease& tempty, int lane, uint8_t* stg = nullptr,
+                                         const CUtensorMap* tmO = nullptr) {
   constexpr int COLS = BN / 2;
   const float f = tile_scale<OPK>(P, tc);
   uint32_t packed[COLS / 2];
@@ -424,11 +428,43 @@ __device__ __forceinline__ void epi_bf16(const GemmArgs& P, const TileCoord& tc,
     }
   }
   release_acc(tempty, lane);
-  uint16_t* drow = KG ? P.d + static_cast<int64_t>(tc.e) * P.M * P.N + static_cast<int64_t>(tc.m0 + row) * P.N +
-                            tc.nt * BN + hf * COLS
-                      : P.d + static_cast<int64_t>(tc.m0 + row) * P.ldd + tc.nt * BN + hf * COLS;
+  if (stg != nullptr) {
+    // 32-row x 64-byte boxes through the warp's tile (64-byte swizzle), as in
+    // epi_tma_out; then every box has been written to global memory and made
+    // visible to generic loads (the combine's readers) before any lane of the
+    // warp signals its row through the combine counter
+    const int y = tc.m0 + (row & ~31);
+    const int x0 = tc.nt * BN + hf * COLS;
+    const int sw = (lane >> 1) & 3;
+    uint8_t* srow = stg + lane * 64;
 #pragma unroll
-  for (int j = 0; j < COLS / 16; ++j) st_global_v8(drow + 16 * j, packed + 8 * j);
+    for (int bx = 0; bx < COLS / 32; ++bx) {
+      if (lane == 0) bulk_wait_group_read<0>();
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(srow + ((j ^ sw) << 4)) =
+            make_uint4(packed[16 * bx + 4 * j], packed[16 * bx + 4 * j + 1], packed[16 * bx + 4 * j + 2],
+                       packed[16 * bx + 4 * j + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmO, stg, x0 + 32 * bx, y);
+        bulk_commit_group();
+      }
+    }
+    if (lane == 0) {
+      bulk_wait_group<0>();
+      fence_proxy_async_global();
+    }
+    __syncwarp();
+  } else {
+    uint16_t* drow = KG ? P.d + static_cast<int64_t>(tc.e) * P.M * P.N + static_cast<int64_t>(tc.m0 + row) * P.N +
+                              tc.nt * BN + hf * COLS
+                        : P.d + static_cast<int64_t>(tc.m0 + row) * P.ldd + tc.nt * BN + hf * COLS;
+#pragma unroll
+    for (int j = 0; j < COLS / 16; ++j) st_global_v8(drow + 16 * j, packed + 8 * j);
+  }
   if constexpr (!KG)
     if (P.cmb_out != nullptr) fused_combine<BN, COLS>(P, tc, row, hf, packed);
 }
@@ -1205,6 +1241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                reinterpret_cast<uint8_t*>(xpose) + (warp - 4) * 2048, &tmO1);
       } else if constexpr (EPI == EPI_ACC_F32) {
         epi_acc_f32<BN>(P, tc, tb, row, hf, rel, lane);
+      } else if constexpr (C::kTmaOut) {     // fused combine: rows by TMA, completed before the counters
+        epi_bf16<BN, KG, OPK>(P, tc, tb, row, hf, rel, lane, reinterpret_cast<uint8_t*>(xpose) + (warp - 4) * 2048,
+                              &tmO1);
       } else {
         epi_bf16<BN, KG, OPK>(P, tc, tb, row, hf, rel, lane);
       }
@@ -1357,7 +1396,7 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
   CUtensorMap tq = ta, tqc = ta;
   // token-grouped pair tiles: the [E·M][N] output (bf16 dW, or the fp32
   // main_grad added into), 32-row x 64-byte boxes, 64-byte swizzle
-  if (C::kTmaOut && (KG || g.cmb_out == nullptr)) {
+  if (C::kTmaOut) {
     const bool acc = EPI == EPI_ACC_F32;
     // token-grouped: [E·M][N] with rows N apart; row-grouped: [M][N] with rows ldd apart
     const int64_t rows = KG ? static_cast<int64_t>(g.E) * g.M : g.M;

@@ -124,6 +124,11 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
+// Orders this thread's async-proxy (TMA) global-memory accesses that have
+// completed with its later generic-proxy accesses (and the other way round).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 // Orders this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
