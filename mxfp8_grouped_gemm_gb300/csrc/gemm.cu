@@ -94,6 +94,8 @@ struct Cfg {
   // Row-grouped bf16 outputs without a fused combine take the same path (the
   // fused combine synchronises on the rows in global memory: per-lane stores).
   static constexpr bool kTmaOut = PAIR && OPK == OPK_MX && (EPI == 0 || (KG && EPI == 3));
+  // MXFP8 gate-up: the saved g|u by TMA through the column quantiser's scratch
+  static constexpr bool kSwTma = EPI == 1 && OPK == OPK_MX;
   static constexpr int kXposeBytes = kDsTma                                    ? 8 * kDsWarpBytes
                                      : kTmaOut                                  ? 8 * 2048
                                      : EPI == 2 && BN == 128                   ? 8 * 32 * 33 * 4
@@ -548,9 +550,13 @@ __device__ __forceinline__ void epi_tma_out(const GemmArgs& P, const TileCoord& 
 // (j0 = nt * BN/2).  The thread owns BN/4 h columns (half hf).  It drains its
 // accumulator columns into registers, releases the accumulator, then computes
 // h in fp32 and quantises and stores while the next tile's MMAs run.
+// MXFP8 (tmGU non-null): the saved g|u leave by TMA through the warp's
+// column-quantiser scratch (2 KB of it as a 32-row x 64-byte box, 64-byte
+// swizzle), one box at a time, before the column quantiser takes it back.
 template <int BN, int OPK>
 __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
-                                           int hf, const AccRelease& tempty, float* slots) {
+                                           int hf, const AccRelease& tempty, float* slots,
+                                           const CUtensorMap* tmGU = nullptr) {
   constexpr int HC = BN / 2;          // h columns per tile
   constexpr int CH = HC / 64;         // 32-column chunks per thread
   const int64_t tok0 = tc.m0 + q * 32;
@@ -594,11 +600,34 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& t
         gp[i] = pack_bf16x2(u2f(g[c][2 * i]), u2f(g[c][2 * i + 1]));
         up[i] = pack_bf16x2(u2f(u[c][2 * i]), u2f(u[c][2 * i + 1]));
       }
-      uint16_t* gs = P.gu_save + r * (2 * I) + col;
-      st_global_v8(gs, gp);
-      st_global_v8(gs + 16, gp + 8);
-      st_global_v8(gs + I, up);
-      st_global_v8(gs + I + 16, up + 8);
+      if (OPK == OPK_MX && tmGU != nullptr) {
+        uint8_t* stg = reinterpret_cast<uint8_t*>(slots);
+        uint8_t* srow = stg + lane * 64;
+        const int sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t* w = half ? up : gp;
+          if (lane == 0) bulk_wait_group_read<0>();    // the previous box has left the scratch
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(srow + ((j ^ sw) << 4)) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(tmGU, stg, static_cast<int>(half ? I + col : col), static_cast<int>(tok0));
+            bulk_commit_group();
+          }
+        }
+        if (lane == 0) bulk_wait_group_read<0>();      // the scratch is the column quantiser's again
+        __syncwarp();
+      } else {
+        uint16_t* gs = P.gu_save + r * (2 * I) + col;
+        st_global_v8(gs, gp);
+        st_global_v8(gs + 16, gp + 8);
+        st_global_v8(gs + I, up);
+        st_global_v8(gs + I + 16, up + 8);
+      }
     }
     if constexpr (OPK != OPK_MX) {
       hmax = max(hmax, row_store_bf16_amax(h, P.y_row + r * P.y_row_ld + col));
@@ -897,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
     }
-    if (C::kDsTma || C::kTmaOut) {
+    if (C::kDsTma || C::kTmaOut || C::kSwTma) {
       tma_prefetch_desc(&tmO1);
       tma_prefetch_desc(&tmO2);
     }
@@ -1226,7 +1255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       rel.bar = rel.peer ? map_to_rank(smem_u32(&tempty[acc]), 0) : smem_u32(&tempty[acc]);
       rel.land = rel.peer ? map_to_rank(smem_u32(&landing[warp - 4]), 0) : 0u;
       if constexpr (EPI == EPI_SWIGLU) {
-        epi_swiglu<BN, OPK>(P, tc, tb, q, lane, hf, rel, xpose + (warp - 4) * 32 * 20);
+        epi_swiglu<BN, OPK>(P, tc, tb, q, lane, hf, rel, xpose + (warp - 4) * 32 * 20,
+                            C::kSwTma && P.gu_save != nullptr ? &tmO1 : nullptr);
       } else if constexpr (EPI == EPI_DSWIGLU) {
         const uint32_t tstage = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kDsCol + hf * 64;
         if constexpr (C::kDsTma) {
@@ -1252,7 +1282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1;
       }
     }
-    if constexpr (C::kDsTma || C::kTmaOut) {
+    if constexpr (C::kDsTma || C::kTmaOut || C::kSwTma) {
       // the TMA stores have completed before the CTA exits
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
@@ -1396,6 +1426,11 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
   CUtensorMap tq = ta, tqc = ta;
   // token-grouped pair tiles: the [E·M][N] output (bf16 dW, or the fp32
   // main_grad added into), 32-row x 64-byte boxes, 64-byte swizzle
+  // MXFP8 gate-up: the saved g|u ([rows][2I] bf16, 32 x 32 boxes, 64-byte swizzle)
+  if (C::kSwTma && g.gu_save != nullptr &&
+      !encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.gu_save, 2 * static_cast<int64_t>(g.I), g.M,
+                 4 * static_cast<int64_t>(g.I), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE))
+    return cudaErrorInvalidValue;
   if (C::kTmaOut) {
     const bool acc = EPI == EPI_ACC_F32;
     // token-grouped: [E·M][N] with rows N apart; row-grouped: [M][N] with rows ldd apart
