@@ -87,17 +87,16 @@ struct Cfg {
   // scratch: a five-stage ring.
   static constexpr bool kDsTma = EPI == 2 && BN == 256 && OPK == OPK_MX;
   static constexpr int kDsWarpBytes = 4096 + 32 * 20 * 4;
-  // MXFP8 pair GEMMs with a bf16 epilogue (the weight gradients' dW, down and
-  // dgrad-gate-up when no combine is fused) or the fp32 main_grad epilogue
-  // write by TMA from a 2 KB shared tile per epilogue warp (epi_tma_out): the
-  // ring keeps six stages.
-  // Row-grouped bf16 outputs without a fused combine take the same path (the
-  // fused combine synchronises on the rows in global memory: per-lane stores).
+  // MXFP8 pair GEMMs with a bf16 epilogue (the weight gradients' dW, down,
+  // dgrad-gate-up) or the fp32 main_grad epilogue write by TMA from a 2 KB
+  // shared tile per epilogue warp (epi_tma_out; epi_bf16 when a combine is
+  // fused, its stores completed before the combine counters): the ring keeps
+  // six stages.
   static constexpr bool kTmaOut = PAIR && OPK == OPK_MX && (EPI == 0 || (KG && EPI == 3));
   // MXFP8 gate-up: the saved g|u by TMA through the column quantiser's scratch
   static constexpr bool kSwTma = EPI == 1 && OPK == OPK_MX;
   static constexpr int kXposeBytes = kDsTma                                    ? 8 * kDsWarpBytes
-                                     : kTmaOut                                  ? 8 * 2048
+                                     : kTmaOut                                 ? 8 * 2048
                                      : EPI == 2 && BN == 128                   ? 8 * 32 * 33 * 4
                                      : (EPI == 1 || EPI == 2) && OPK == OPK_MX ? 8 * 32 * 20 * 4
                                                                                : 0;
