@@ -1,5 +1,5 @@
 """The derived per-element parity bounds (tests/parity_bounds.py), checked on
-the CPU before they judge a GPU run:
+the CPU before they are applied to a GPU run:
 
   * they accept a layer computed with the GPU path's storage choices (fp32
     accumulators and activations, GU and dH held in bf16 for the backward,
