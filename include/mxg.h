@@ -585,8 +585,12 @@ int mxg_grouped_mlp_fp8_bwd_stage(const mxg_mlp_bwd_args* args, int stage, void*
 const void* mxg_mlp_fp8_saved_view(const void* saved, int T, int H, int I, int E, int k, int which);
 
 /* Debug views into `saved` (device pointers; NULL on bad arguments) used by the
- * tests to compare intermediates: 0 = GU (bf16 [m_cap][2I], the gate-up GEMM
- * output before the activation; m_cap = mxg_mlp_row_capacity), 1 =
+ * tests to compare intermediates: 0 = GU (the gate-up GEMM output before the
+ * activation, m_cap x 2I bf16 values, m_cap = mxg_mlp_row_capacity) in 32 x 32
+ * tiles: the tile of rows 32rb.. and gate columns 32cb.. (cb < I/32) starts at
+ * element (rb*I/32 + cb)*2048 and holds the gate block, then the up block of
+ * the same columns, each as two 16-column halves of 32 rows x 16 values (row r
+ * of half h at h*512 + r*16), 1 =
  * padded_offsets (int32 [E+1], multiples of mxg_mlp_group_align()), 2 =
  * row_of_src in the padded layout (int32 [T*k]), 3 / 4 = x's token-column-wise
  * codes (uint8 [H][m_cap]) / scales (tensor-core layout, H rows x m_cap/32

@@ -20,7 +20,8 @@
 //                 (ScaledSwiGLU, "Fusing precision conversion and expert
 //                 computation"), re-quantised to MXFP8 row-wise (the down
 //                 GEMM's A) and token-column-wise (the down wgrad's B); the
-//                 pre-activation g|u is kept in bf16 for the backward.
+//                 pre-activation g|u is kept in bf16 for the backward (MXFP8:
+//                 in 32 x 32 tiles, gu_tile_offset).
 //   EPI_DSWIGLU : dH tile -> dg = dH p u s (1 + g (1-s)), du = dH p g s
 //                 (s = sigmoid(g)), d(prob) partial sum_i dH g s u; dGU
 //                 quantised row-wise (dgrad A) and token-column-wise (wgrad A).
@@ -93,7 +94,8 @@ struct Cfg {
   // fused, its stores completed before the combine counters): the ring keeps
   // six stages.
   static constexpr bool kTmaOut = PAIR && OPK == OPK_MX && (EPI == 0 || (KG && EPI == 3));
-  // MXFP8 gate-up: the saved g|u by TMA through the column quantiser's scratch
+  // MXFP8 gate-up: the saved g|u leave as bulk copies through the column
+  // quantiser's scratch
   static constexpr bool kSwTma = EPI == 1 && OPK == OPK_MX;
   static constexpr int kXposeBytes = kDsTma                                    ? 8 * kDsWarpBytes
                                      : kTmaOut                                 ? 8 * 2048
@@ -132,6 +134,31 @@ __device__ __forceinline__ void load_bf16_32(const uint16_t* src, float (&v)[32]
   uint32_t w[16];
   ld_global_nc_v8(src, w);
   ld_global_nc_v8(src + 16, w + 8);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    v[2 * j] = u2f(w[j] << 16);
+    v[2 * j + 1] = u2f(w[j] & 0xffff0000u);
+  }
+}
+
+// The MXFP8 path keeps the gate-up output g|u for the backward in 32 x 32
+// tiles: the tile of rows 32·rb.. and columns 32·cb.. of the gate half (cb <
+// I/32) starts at element (rb·I/32 + cb)·2048 and holds the gate block, then
+// the up block of the same columns, each as two 16-column halves of 32 rows x
+// 16 values (row r of half h at h·512 + r·16).  A warp owning the tile's 32
+// rows reads each half as one contiguous kilobyte (lane r: its row's 32
+// bytes), where rows of a [rows][2I] matrix are 4I bytes apart and every lane
+// touched its own sector: those scattered loads slowed the concurrent MMAs of
+// the dgrad-down GEMM (its tensor pipe by ~7 %).
+__device__ __forceinline__ int64_t gu_tile_offset(int I, int tok0, int col) {
+  return (static_cast<int64_t>(tok0 >> 5) * (I >> 5) + (col >> 5)) * 2048;
+}
+
+// Lane `lane`'s 32 values of one block (gate or up) of a g|u tile, as fp32.
+__device__ __forceinline__ void load_gu_block32(const uint16_t* blk, int lane, float (&v)[32]) {
+  uint32_t w[16];
+  ld_global_nc_v8(blk + lane * 16, w);
+  ld_global_nc_v8(blk + 512 + lane * 16, w + 8);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     v[2 * j] = u2f(w[j] << 16);
@@ -549,13 +576,12 @@ __device__ __forceinline__ void epi_tma_out(const GemmArgs& P, const TileCoord& 
 // (j0 = nt * BN/2).  The thread owns BN/4 h columns (half hf).  It drains its
 // accumulator columns into registers, releases the accumulator, then computes
 // h in fp32 and quantises and stores while the next tile's MMAs run.
-// MXFP8 (tmGU non-null): the saved g|u leave by TMA through the warp's
-// column-quantiser scratch (2 KB of it as a 32-row x 64-byte box, 64-byte
-// swizzle), one box at a time, before the column quantiser takes it back.
+// MXFP8 (stage_gu): the saved g|u leave as 2 KB bulk copies (one gate or up
+// block of a g|u tile, gu_tile_offset) through the warp's column-quantiser
+// scratch, one block at a time, before the column quantiser takes it back.
 template <int BN, int OPK>
 __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& tc, uint32_t tb, int q, int lane,
-                                           int hf, const AccRelease& tempty, float* slots,
-                                           const CUtensorMap* tmGU = nullptr) {
+                                           int hf, const AccRelease& tempty, float* slots, bool stage_gu = false) {
   constexpr int HC = BN / 2;          // h columns per tile
   constexpr int CH = HC / 64;         // 32-column chunks per thread
   const int64_t tok0 = tc.m0 + q * 32;
@@ -599,22 +625,32 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& P, const TileCoord& t
         gp[i] = pack_bf16x2(u2f(g[c][2 * i]), u2f(g[c][2 * i + 1]));
         up[i] = pack_bf16x2(u2f(u[c][2 * i]), u2f(u[c][2 * i + 1]));
       }
-      if (OPK == OPK_MX && tmGU != nullptr) {
+      if (OPK == OPK_MX && stage_gu) {
+        // the gate block, then the up block, of g|u tile (tok0/32, col/32),
+        // each staged in its global order: lane's 32 bytes of half h at
+        // (32·h + lane)·32, written as two 16-byte pieces of which lanes with
+        // bit 2 set write the second first (eight consecutive lanes then
+        // cover the 32 banks once)
         uint8_t* stg = reinterpret_cast<uint8_t*>(slots);
-        uint8_t* srow = stg + lane * 64;
-        const int sw = (lane >> 1) & 3;
+        const int sw = (lane >> 2) & 1;
+        uint16_t* dst = P.gu_save + gu_tile_offset(static_cast<int>(I), static_cast<int>(tok0), static_cast<int>(col));
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const uint32_t* w = half ? up : gp;
-          if (lane == 0) bulk_wait_group_read<0>();    // the previous box has left the scratch
+          if (lane == 0) bulk_wait_group_read<0>();    // the previous block has left the scratch
           __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(srow + ((j ^ sw) << 4)) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          for (int h = 0; h < 2; ++h) {
+            uint8_t* srow = stg + (32 * h + lane) * 32;
+            const uint4 a = make_uint4(w[8 * h], w[8 * h + 1], w[8 * h + 2], w[8 * h + 3]);
+            const uint4 b = make_uint4(w[8 * h + 4], w[8 * h + 5], w[8 * h + 6], w[8 * h + 7]);
+            *reinterpret_cast<uint4*>(srow + (sw << 4)) = sw ? b : a;
+            *reinterpret_cast<uint4*>(srow + ((sw ^ 1) << 4)) = sw ? a : b;
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(tmGU, stg, static_cast<int>(half ? I + col : col), static_cast<int>(tok0));
+            bulk_store_s2g(dst + 1024 * half, stg, 2048);
             bulk_commit_group();
           }
         }
@@ -658,8 +694,9 @@ __device__ __forceinline__ void epi_dswiglu(const GemmArgs& P, const TileCoord& 
     tmem_ld_32x32b_x32(tb + hf * COLS + c * 32, dh);
     const int64_t col = j0 + c * 32;
     float g[32], u[32], dg[32];
-    load_bf16_32(P.gu_save + r * (2 * I) + col, g);
-    load_bf16_32(P.gu_save + r * (2 * I) + I + col, u);
+    const uint16_t* blk = P.gu_save + gu_tile_offset(static_cast<int>(I), static_cast<int>(tok0), static_cast<int>(col));
+    load_gu_block32(blk, lane, g);
+    load_gu_block32(blk + 1024, lane, u);
     tmem_ld_wait();
     if (c == COLS / 32 - 1) release_acc(tempty, lane);
 #pragma unroll
@@ -815,17 +852,19 @@ __device__ __forceinline__ void epi_dswiglu_tma(const GemmArgs& P, const TileCoo
   const float p = P.probs_perm[r];
   const int I = P.I;
   const int j0 = tc.nt * 256 + hf * COLS;
-  const uint16_t* gr = P.gu_save + r * (2 * static_cast<int64_t>(I));
+  // this lane's row in the g|u tiles of the warp's four chunks (consecutive
+  // tiles: gu_tile_offset)
+  const uint16_t* gt = P.gu_save + gu_tile_offset(I, tok0, j0) + lane * 16;
   float2 dp2 = make_float2(0.f, 0.f);
   uint32_t sbg = 0, sbu = 0;
   // the saved g|u of chunk c + 1 are requested (as raw bf16 pairs) before
   // chunk c's math, so their latency overlaps it: 64 experts top-8 0.932
   // (paired), the Mixtral layer unchanged
   uint32_t gw[16], uw[16];
-  ld_global_nc_v8(gr + j0, gw);
-  ld_global_nc_v8(gr + j0 + 16, gw + 8);
-  ld_global_nc_v8(gr + I + j0, uw);
-  ld_global_nc_v8(gr + I + j0 + 16, uw + 8);
+  ld_global_nc_v8(gt, gw);
+  ld_global_nc_v8(gt + 512, gw + 8);
+  ld_global_nc_v8(gt + 1024, uw);
+  ld_global_nc_v8(gt + 1536, uw + 8);
 #pragma unroll 1
   for (int c = 0; c < COLS / 32; ++c) {
     const int col = j0 + c * 32;
@@ -839,10 +878,11 @@ __device__ __forceinline__ void epi_dswiglu_tma(const GemmArgs& P, const TileCoo
       u[2 * j + 1] = u2f(uw[j] & 0xffff0000u);
     }
     if (c + 1 < COLS / 32) {
-      ld_global_nc_v8(gr + col + 32, gw);
-      ld_global_nc_v8(gr + col + 48, gw + 8);
-      ld_global_nc_v8(gr + I + col + 32, uw);
-      ld_global_nc_v8(gr + I + col + 48, uw + 8);
+      const uint16_t* nt = gt + (c + 1) * 2048;
+      ld_global_nc_v8(nt, gw);
+      ld_global_nc_v8(nt + 512, gw + 8);
+      ld_global_nc_v8(nt + 1024, uw);
+      ld_global_nc_v8(nt + 1536, uw + 8);
     }
     dswiglu32(dh, g, u, p, dp2, dg);
     // the previous chunk's code stores have finished reading the staging tiles
@@ -925,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
     }
-    if (C::kDsTma || C::kTmaOut || C::kSwTma) {
+    if (C::kDsTma || C::kTmaOut) {
       tma_prefetch_desc(&tmO1);
       tma_prefetch_desc(&tmO2);
     }
@@ -1255,7 +1295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       rel.land = rel.peer ? map_to_rank(smem_u32(&landing[warp - 4]), 0) : 0u;
       if constexpr (EPI == EPI_SWIGLU) {
         epi_swiglu<BN, OPK>(P, tc, tb, q, lane, hf, rel, xpose + (warp - 4) * 32 * 20,
-                            C::kSwTma && P.gu_save != nullptr ? &tmO1 : nullptr);
+                            C::kSwTma && P.gu_save != nullptr);
       } else if constexpr (EPI == EPI_DSWIGLU) {
         const uint32_t tstage = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kDsCol + hf * 64;
         if constexpr (C::kDsTma) {
@@ -1425,11 +1465,8 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
   CUtensorMap tq = ta, tqc = ta;
   // token-grouped pair tiles: the [E·M][N] output (bf16 dW, or the fp32
   // main_grad added into), 32-row x 64-byte boxes, 64-byte swizzle
-  // MXFP8 gate-up: the saved g|u ([rows][2I] bf16, 32 x 32 boxes, 64-byte swizzle)
-  if (C::kSwTma && g.gu_save != nullptr &&
-      !encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.gu_save, 2 * static_cast<int64_t>(g.I), g.M,
-                 4 * static_cast<int64_t>(g.I), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE))
-    return cudaErrorInvalidValue;
+  // MXFP8 gate-up: the saved g|u in 32 x 32 tiles (gu_tile_offset)
+  if (C::kSwTma && g.gu_save != nullptr && (g.M % 32 != 0 || g.I % 32 != 0)) return cudaErrorInvalidValue;
   if (C::kTmaOut) {
     const bool acc = EPI == EPI_ACC_F32;
     // token-grouped: [E·M][N] with rows N apart; row-grouped: [M][N] with rows ldd apart

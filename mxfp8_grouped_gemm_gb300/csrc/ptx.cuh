@@ -113,6 +113,12 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const 
                "r"(smem_u32(smem_src)), "r"(x), "r"(y)
                : "memory");
 }
+// Bulk copy shared -> global of `bytes` contiguous bytes (both addresses
+// 16-byte aligned, bytes a multiple of 16), bulk group completion.
+__device__ __forceinline__ void bulk_store_s2g(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // All but the newest N committed bulk groups have finished reading shared memory.
 template <int N>

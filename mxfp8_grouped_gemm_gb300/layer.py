@@ -12,6 +12,15 @@ def precision_is_not_mx(layer) -> bool:
     return layer.precision != "mxfp8"
 
 
+def gu_rows_from_tiles(t: torch.Tensor, m_cap: int, I: int) -> torch.Tensor:
+    """[m_cap, 2I] rows from the MXFP8 path's saved g|u tiles (flat, m_cap*2I
+    values): the tile of rows 32rb.. and gate columns 32cb.. (cb < I/32) starts
+    at element (rb*I/32 + cb)*2048 and holds the gate block, then the up block,
+    each as two 16-column halves of 32 rows x 16 values."""
+    t = t.view(m_cap // 32, I // 32, 2, 2, 32, 16)          # [rb][cb][gate/up][half][row][16]
+    return t.permute(0, 4, 2, 1, 3, 5).reshape(m_cap, 2 * I)  # [rb][row][gate/up][cb][half][16]
+
+
 class GroupedMLP:
     """precision "mxfp8" (the path), "bf16" (the like-for-like BF16 reference) or
     "fp8" (per-tensor FP8, one scale per expert tensor); bf16 and fp8 need H and
@@ -98,13 +107,15 @@ class GroupedMLP:
         return int(self.dev_status.item())
 
     def gu_view(self) -> torch.Tensor:
-        """The gate-up GEMM output (bf16 [m_cap, 2I]) kept in the saved buffer (MXFP8 path)."""
+        """The gate-up GEMM output kept in the saved buffer (MXFP8 path), as a
+        bf16 [m_cap, 2I] tensor in row order (gate columns, then up columns):
+        a copy of the buffer's 32 x 32 tiles (gu_rows_from_tiles)."""
         if precision_is_not_mx(self):
             raise NotImplementedError("gu_view reads the MXFP8 path's saved layout")
         base = self.saved.data_ptr()
         off = _lib.mxg_mlp_saved_view(self.saved, self.T, self.H, self.I, self.E, self.k, 0) - base
         m_cap = self.padded_rows_capacity()
-        return self.saved[off:off + m_cap * 2 * self.I * 2].view(torch.bfloat16).view(m_cap, 2 * self.I)
+        return gu_rows_from_tiles(self.saved[off:off + m_cap * 2 * self.I * 2].view(torch.bfloat16), m_cap, self.I)
 
     def padded_offsets(self) -> torch.Tensor:
         if precision_is_not_mx(self):

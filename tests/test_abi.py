@@ -280,3 +280,24 @@ def test_fp8_mlp_sizes_and_validation(L):
     assert L.mxg_grouped_mlp_fp8_fwd_stage(ctypes.byref(a), 99, None) == 1
     assert L.mxg_mlp_fp8_saved_view(None, 256, 256, 512, 4, 2, 0) is None
     assert L.mxg_mlp_fp8_saved_view(FAKE, 256, 256, 512, 4, 2, 9) is None
+
+
+def test_saved_gu_tile_layout_reads_back_in_row_order():
+    """The saved g|u tiles (documented in include/mxg.h, saved view 0) read
+    back as [m_cap, 2I] rows: every element placed by the header's formula
+    lands at its (row, column)."""
+    import torch
+    from mxfp8_grouped_gemm_gb300.layer import gu_rows_from_tiles
+    m_cap, I = 96, 64
+    want = torch.arange(m_cap * 2 * I, dtype=torch.float64).view(m_cap, 2 * I)
+    flat = torch.full((m_cap * 2 * I,), -1.0, dtype=torch.float64)
+    for row in range(m_cap):
+        for col in range(2 * I):
+            gate_up, j = divmod(col, I)
+            rb, r = divmod(row, 32)
+            cb, c = divmod(j, 32)
+            h, c16 = divmod(c, 16)
+            off = (rb * (I // 32) + cb) * 2048 + gate_up * 1024 + h * 512 + r * 16 + c16
+            flat[off] = want[row, col]
+    assert bool((flat >= 0).all())
+    assert torch.equal(gu_rows_from_tiles(flat, m_cap, I), want)
