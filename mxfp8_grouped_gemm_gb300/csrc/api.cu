@@ -169,8 +169,6 @@ cudaError_t launch_weight_quant(const uint16_t* w_gate_up, const uint16_t* w_dow
     wq.sf_col_rows = E * H;
   }
   wq.layout = MXG_LAYOUT_MMA;
-  cudaError_t err = launch_quant(wq, s);
-  if (err != cudaSuccess) return err;
   QuantParams dq = wq;
   dq.x = w_down;
   dq.ld_x = I;
@@ -186,7 +184,7 @@ cudaError_t launch_weight_quant(const uint16_t* w_gate_up, const uint16_t* w_dow
     dq.ld_col = H;
     dq.sf_col_rows = E * I;
   }
-  return launch_quant(dq, s);
+  return launch_quant2(wq, dq, s);
 }
 
 }  // namespace

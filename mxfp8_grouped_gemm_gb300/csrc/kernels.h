@@ -50,6 +50,9 @@ struct QuantParams {
   int32_t groups;
 };
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
+// Two tensors quantised by one launch when their modes match (else two launches);
+// the outputs are those of launch_quant(a) then launch_quant(b).
+cudaError_t launch_quant2(const QuantParams& a, const QuantParams& b, cudaStream_t s);
 
 // Padded layout of grouped rows: poff[g] = sum over g' < g of the group sizes
 // off[g'+1] - off[g'] each rounded up to `align`.  off must start at 0, be

@@ -198,13 +198,13 @@ __device__ __forceinline__ void stage_tile(const uint16_t* xc, int64_t ld_x, int
 // the kernel waits mostly on shared-memory and shuffle results, and two more
 // CTAs than eight gave the gathered passes 2 % (twelve spill and lose 2-6 %).
 template <bool GATHER, bool ROW, bool COL, bool PT>
-__global__ void __launch_bounds__(128, 10) quant_kernel(const QuantParams P) {
+__device__ __forceinline__ void quant_tiles(const QuantParams& P, int bx, int by, int bz) {
   __shared__ __align__(16) uint16_t tile[2][kRows * kStride];
   __shared__ int64_t s_off[GATHER ? kTilesPerCta * kRows : 1];
-  const int c0 = blockIdx.y * kCols;
-  const int b = blockIdx.z;
+  const int c0 = by * kCols;
+  const int b = bz;
   const int tid = threadIdx.x;
-  const int first = blockIdx.x * kTilesPerCta * kRows;
+  const int first = bx * kTilesPerCta * kRows;
   int limit = P.rows;
   if (P.rows_valid != nullptr) limit = min(limit, *P.rows_valid);
   const int ntiles = min(kTilesPerCta, (limit - first + kRows - 1) / kRows);
@@ -306,6 +306,27 @@ __global__ void __launch_bounds__(128, 10) quant_kernel(const QuantParams P) {
       copy_col_block(P, buf, warp * 32, static_cast<int64_t>(b) * P.cols + c0 + warp * 32, p0, tid & 31);
     }
     __syncthreads();   // buffer t&1 is refilled two tiles later
+  }
+}
+
+template <bool GATHER, bool ROW, bool COL, bool PT>
+__global__ void __launch_bounds__(128, 10) quant_kernel(const QuantParams P) {
+  quant_tiles<GATHER, ROW, COL, PT>(P, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// Two tensors of the same mode in one launch (the weights: W_gate_up, then
+// W_down): blocks [0, n0) walk the first tensor's grid (gx0 x gy0 x batch,
+// x fastest), the rest the second's.  As two launches, each ended with a
+// partly filled last wave; here the second tensor's blocks fill the first's.
+template <bool GATHER, bool ROW, bool COL, bool PT>
+__global__ void __launch_bounds__(128, 10) quant_kernel2(const QuantParams P0, const QuantParams P1, int gx0, int gy0,
+                                                          int n0, int gx1, int gy1) {
+  const int id = static_cast<int>(blockIdx.x);
+  if (id < n0) {
+    quant_tiles<GATHER, ROW, COL, PT>(P0, id % gx0, (id / gx0) % gy0, id / (gx0 * gy0));
+  } else {
+    const int j = id - n0;
+    quant_tiles<GATHER, ROW, COL, PT>(P1, j % gx1, (j / gx1) % gy1, j / (gx1 * gy1));
   }
 }
 
@@ -415,11 +436,42 @@ void launch_mode(const QuantParams& p, dim3 grid, cudaStream_t s) {
   quant_kernel<G, R, C, PT><<<grid, 128, 0, s>>>(p);
 }
 
+static int quant_mode(const QuantParams& p) {
+  return (p.src_rows != nullptr || p.grp_off != nullptr ? 1 : 0) | (p.q_row != nullptr ? 2 : 0) |
+         (p.q_col != nullptr ? 4 : 0) | (p.pt_amax != nullptr ? 8 : 0);
+}
+
+static dim3 quant_grid(const QuantParams& p) {
+  return dim3((p.rows / kRows + kTilesPerCta - 1) / kTilesPerCta, p.cols / kCols, p.batch);
+}
+
+cudaError_t launch_quant2(const QuantParams& a, const QuantParams& b, cudaStream_t s) {
+  const dim3 ga = quant_grid(a), gb = quant_grid(b);
+  const int64_t na = static_cast<int64_t>(ga.x) * ga.y * ga.z, nb = static_cast<int64_t>(gb.x) * gb.y * gb.z;
+  // the same outputs as two launches; one launch needs one mode and a grid that fits
+  if (quant_mode(a) != quant_mode(b) || na == 0 || nb == 0 || na + nb > INT32_MAX) {
+    cudaError_t err = launch_quant(a, s);
+    return err != cudaSuccess ? err : launch_quant(b, s);
+  }
+  const unsigned n = static_cast<unsigned>(na + nb);
+  const int gx0 = static_cast<int>(ga.x), gy0 = static_cast<int>(ga.y), n0 = static_cast<int>(na);
+  const int gx1 = static_cast<int>(gb.x), gy1 = static_cast<int>(gb.y);
+  switch (quant_mode(a)) {
+    case 6: quant_kernel2<false, true, true, false><<<n, 128, 0, s>>>(a, b, gx0, gy0, n0, gx1, gy1); break;
+    case 2: quant_kernel2<false, true, false, false><<<n, 128, 0, s>>>(a, b, gx0, gy0, n0, gx1, gy1); break;
+    default: {
+      cudaError_t err = launch_quant(a, s);
+      return err != cudaSuccess ? err : launch_quant(b, s);
+    }
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s) {
-  dim3 grid((p.rows / kRows + kTilesPerCta - 1) / kTilesPerCta, p.cols / kCols, p.batch);
+  dim3 grid = quant_grid(p);
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
-  const int mode = (p.src_rows != nullptr || p.grp_off != nullptr ? 1 : 0) | (p.q_row != nullptr ? 2 : 0) |
-                   (p.q_col != nullptr ? 4 : 0) | (p.pt_amax != nullptr ? 8 : 0);
+  const int mode = quant_mode(p);
   switch (mode) {
     case 0: launch_mode<false, false, false, false>(p, grid, s); break;
     case 1: launch_mode<true, false, false, false>(p, grid, s); break;
