@@ -182,8 +182,7 @@ int mxg_route_permute(const int32_t* ids, int T, int k, int E, int32_t* split_si
  *     larger calls return MXG_ERR_WORKSPACE without launching (16,773,120
  *     entries for E = 8, 2,093,056 for E = 64, 520,192 for E = 256).
  *   - The first call on each device looks up the array's device address (a
- *     host-side runtime query, no allocation); make that first call before any
- *     stream capture that contains the entry point.
+ *     host-side runtime query, no allocation).
  *   - All calls share the one array.  Calls whose kernels overlap on the GPU
  *     (different streams without ordering) race and give wrong results;
  *     serialise them.  Nothing needs clearing between calls: every scratch

@@ -2,9 +2,9 @@
 // device array instead of a caller-provided workspace.
 //
 // For callers that cannot allocate device memory at the point where they route
-// tokens — e.g. code running inside a framework's memory pool or a stream
-// capture where cudaMalloc is not allowed, or a host runtime that owns all
-// allocations and hands out only the input and output buffers.  The call still
+// tokens — e.g. code running inside a framework's memory pool, or a host
+// runtime that owns all allocations and hands out only the input and output
+// buffers.  The call still
 // takes the caller's inputs and outputs; only the per-call scratch (per-chunk
 // expert counts and bases, the row offsets) lives in a fixed-size array that
 // every GPU loading this library keeps until the process exits.
