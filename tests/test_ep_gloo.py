@@ -12,7 +12,8 @@ recipe": expert parallelism, data x expert parallel sizes = GPU count):
   * y, dx, dprobs per rank and each rank's experts' dW_gate_up, dW_down:
     the same fp64 arithmetic on the same rows, equal to 1e-12 relative
     (BLAS may block the products differently for differently placed rows).
-Not measured on hardware: every GPU machine here has one GPU."""
+Not measured across GPUs: the exchange runs here between CPU ranks, and the
+single-GPU test (test_gpu_ep.py) runs the ranks as virtual ranks on one device."""
 import os
 import socket
 
