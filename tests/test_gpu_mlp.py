@@ -25,6 +25,10 @@ def _inputs(name):
         return (300, 256, 384, 6, 2), synthetic.make_case(300, 256, 384, 6, 2, seed=5, empty_experts=(1, 4))
     if name == "ragged_k1":
         return (200, 128, 128, 3, 1), synthetic.make_case(200, 128, 128, 3, 1, seed=6)
+    if name == "wide_e256":      # the largest expert count, top-8: ~16 rows per expert, each in its own tile
+        return (512, 256, 256, 256, 8), synthetic.make_case(512, 256, 256, 256, 8, seed=7)
+    if name == "all_experts":    # k = E: every token goes to every expert
+        return (256, 128, 256, 4, 4), synthetic.make_case(256, 128, 256, 4, 4, seed=8)
     wl = synthetic.WORKLOADS[name]
     inp = synthetic.make_inputs(wl)
     if "dy" not in inp:          # the forward-only workload still gets a backward check here
@@ -84,7 +88,7 @@ def run_gpu(m, shape, inp):
     return out
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_k1", "mid"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_k1", "mid", "wide_e256", "all_experts"])
 def test_mlp_fwd_bwd_matches_oracle(name):
     m = require_gpu()
     shape, inp = _inputs(name)
