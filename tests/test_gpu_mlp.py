@@ -29,6 +29,10 @@ def _inputs(name):
         return (512, 256, 256, 256, 8), synthetic.make_case(512, 256, 256, 256, 8, seed=7)
     if name == "all_experts":    # k = E: every token goes to every expert
         return (256, 128, 256, 4, 4), synthetic.make_case(256, 128, 256, 4, 4, seed=8)
+    if name == "top32":          # the largest k: 32 of 64 experts per token, combines over 32 rows
+        return (128, 128, 128, 64, 32), synthetic.make_case(128, 128, 128, 64, 32, seed=9)
+    if name == "one_token":      # a single token: two one-row groups, every tile mostly padding
+        return (1, 128, 128, 4, 2), synthetic.make_case(1, 128, 128, 4, 2, seed=10)
     wl = synthetic.WORKLOADS[name]
     inp = synthetic.make_inputs(wl)
     if "dy" not in inp:          # the forward-only workload still gets a backward check here
@@ -88,7 +92,8 @@ def run_gpu(m, shape, inp):
     return out
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_k1", "mid", "wide_e256", "all_experts"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_k1", "mid", "wide_e256", "all_experts", "top32",
+                                  "one_token"])
 def test_mlp_fwd_bwd_matches_oracle(name):
     m = require_gpu()
     shape, inp = _inputs(name)
