@@ -223,3 +223,35 @@ def test_pregrouped_mx_forward_equals_the_bf16_rows_forward():
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and ex.status() == 0
     assert torch.equal(y_mx, y_ref)
+
+
+def test_pregrouped_all_rows_in_one_expert():
+    """Every pre-grouped row belongs to one expert (the others get none): the
+    forward and backward match the oracle on those rows, and the idle experts'
+    weight gradients are exact zeros."""
+    m = require_gpu()
+    R, H, I, E, hot = 200, 128, 256, 4, 2
+    case = synthetic.make_case(R, H, I, E, 1, seed=12)
+    split = torch.zeros(E, dtype=torch.int32)
+    split[hot] = R
+    p = torch.from_numpy(np.random.default_rng(12).uniform(0.1, 1.0, R).astype(np.float32))
+    dev = "cuda"
+    ex = m.GroupedExperts(R, H, I, E)
+    y = ex.forward(case["x"].to(dev), split.to(dev), p.to(dev), case["w_gate_up"].to(dev), case["w_down"].to(dev))
+    dx, dwgu, dwd, dp = ex.backward(case["dy"].to(dev))
+    torch.cuda.synchronize()
+    assert ex.status() == 0
+    for e in range(E):
+        if e != hot:
+            assert not np_(dwgu[e]).any() and not np_(dwd[e]).any()
+    ids1 = np.full((R, 1), hot, dtype=np.int32)
+    xg, dyg = case["x"].double().numpy(), case["dy"].double().numpy()
+    ctx = moe.mlp_fwd(xg, ids1, p.double().numpy().reshape(R, 1), case["w_gate_up"].double().numpy(),
+                      case["w_down"].double().numpy())
+    gr = moe.mlp_bwd(ctx, dyg)
+    W = {hot: moe.expert_weights(case["w_gate_up"][hot].double().numpy(), case["w_down"][hot].double().numpy())}
+    bnd = pb.full_bounds(ctx, gr, W, dyg)
+    rec = {"test": "pregrouped", "workload": "one_expert", "precision": "mxfp8"}
+    for key, got, ref in (("y", y, ctx["y"]), ("dx", dx, gr["dx"]), ("dprobs", dp, gr["dprobs"]),
+                          ("dw_gate_up", dwgu, gr["dw_gate_up"]), ("dw_down", dwd, gr["dw_down"])):
+        pb.check(np_(got), ref, bnd[key], key, rec)
